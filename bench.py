@@ -1,0 +1,501 @@
+#!/usr/bin/env python
+"""Benchmark of the q8ta int8 quantized contraction hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. quantize_per_tensor        fp32 [64Mi] -> int8                (HBM bound)
+  2. quantize -> linear operand fp32 [2048, 4096] -> int8 x_q + bf16 operand
+  3. q8ta_linear GEMM           2048 x 4096 x 11008, packed weight (tensor cores)
+  4. q8ta_linear_gemv           1 x 4096 x 4096                    (HBM bound)
+  5. q8ta_conv2d_transposed     [8,256,64,64] -> [8,128,128,128], K=3 s=2 p=1 op=1
+
+value = int8 TOPS of the step: (2*M*N*K of the linear + 2*K*N of the gemv +
+2 * valid-tap MACs of the transposed convolution) / step time.  Per-op
+figures (GB/s, TOPS, outputs/s) are reported under "ops".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs its own replica (the ops are data parallel:
+independent problems, no collective on the data path); value sums all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "q8ta_linear int8 TOPS & gemv/quantize HBM GB/s vs roofline; conv_t outputs/s"
+
+# ---- workload sizes (the five benchmark workloads of the q8ta pages) -------
+Q = synth.CONFIGS["quantize_64Mi"]
+L = synth.CONFIGS["linear_chain_2048x4096x11008"]
+G = synth.CONFIGS["gemv_1x4096x4096"]
+C = synth.CONFIGS["conv_t_8x256x64x64_k3s2"]
+
+QN = Q.dims["numel"]
+LM, LK, LN = L.dims["M"], L.dims["K"], L.dims["N"]
+GK, GN = G.dims["K"], G.dims["N"]
+CD = C.dims
+CHo, CWo = synth.output_hw(CD["H_in"], CD["W_in"], CD["Kh"], CD["Kw"], CD["s"], CD["s"], CD["p"],
+                           CD["p"], CD["op"], CD["op"])
+
+
+def conv_valid_macs(d, Ho, Wo):
+    """Multiply-adds over valid taps only (the work the op defines): the
+    valid (kh, kw) pairs of an output factor into valid rows x valid columns."""
+    def valid(o, K, n_in):
+        return sum(1 for k in range(K)
+                   if (o + d["p"] - k) >= 0 and (o + d["p"] - k) % d["s"] == 0
+                   and (o + d["p"] - k) // d["s"] < n_in)
+    rows = sum(valid(o, d["Kh"], d["H_in"]) for o in range(Ho))
+    cols = sum(valid(o, d["Kw"], d["W_in"]) for o in range(Wo))
+    return d["N"] * d["OC"] * d["IC"] * rows * cols
+
+
+OPS_LINEAR = 2 * LM * LN * LK
+OPS_GEMV = 2 * GK * GN
+CONV_MACS = conv_valid_macs(CD, CHo, CWo)
+OPS_CONV = 2 * CONV_MACS
+OPS_STEP = OPS_LINEAR + OPS_GEMV + OPS_CONV
+CONV_OUTPUTS = CD["N"] * CD["OC"] * CHo * CWo
+# algorithmic bytes (each input read once, each output written once)
+BYTES_QUANT = QN * (4 + 1)
+BYTES_GEMV = GN * GK + GK + GN + 2 * GN * 4
+BYTES_CHAIN_PREP = LM * LK * (4 + 1 + 2)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6786.9), d.get("bf16_tflops", 1887.4), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler (nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# inputs
+# ---------------------------------------------------------------------------
+def host_inputs():
+    qp, lp, gp, cp = Q.params, L.params, G.params, C.params
+    xq = synth.normal(Q.seed, "x", (QN,), qp["x_mean"], qp["x_var"])
+    lx, lw, lws, lb = synth.linear_inputs(L.seed, LM, LK, LN, x_kind="fp32", p=lp)
+    gx, gw, gws, gb = synth.linear_inputs(G.seed, 1, GK, GN, x_kind="int8", p=gp)
+    cx, cw, cws, cb = synth.conv_t_inputs(C.seed, CD, cp)
+    return dict(xq=xq, lx=lx, lw=lw, lws=lws, lb=lb, gx=gx, gw=gw, gws=gws, gb=gb, cx=cx, cw=cw,
+                cws=cws, cb=cb)
+
+
+# ---------------------------------------------------------------------------
+# our CUDA path
+# ---------------------------------------------------------------------------
+class Path:
+    """Device-resident buffers and one step of the hot path."""
+
+    def __init__(self, h, dev, only="all"):
+        import torch
+        import int8_quantized_q8ta_gb300 as q8
+        self.q8, self.torch, self.dev, self.only = q8, torch, dev, only
+        T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        self.xq = T(h["xq"])
+        self.q_out = torch.empty(QN, dtype=torch.int8, device=dev)
+        self.lx = T(h["lx"])
+        self.packed = q8.pack_weight(T(h["lw"]))
+        self.lws, self.lb = T(h["lws"]), T(h["lb"])
+        self.l_xq = torch.empty((LM, LK), dtype=torch.int8, device=dev)
+        self.operand = q8.operand_buffer(LM, LK, dev)
+        self.l_out = torch.empty((LM, LN), dtype=torch.int8, device=dev)
+        self.gx, self.gw = T(h["gx"]), T(h["gw"])
+        self.gws, self.gb = T(h["gws"]), T(h["gb"])
+        self.g_out = torch.empty((1, GN), dtype=torch.int8, device=dev)
+        self.cx, self.cw = T(h["cx"]), T(h["cw"])
+        self.cws, self.cb = T(h["cws"]), T(h["cb"])
+        self.c_out = torch.empty((CD["N"], CD["OC"], CHo, CWo), dtype=torch.int8, device=dev)
+        shape = q8.conv_t_shape(tuple(self.cx.shape), tuple(self.cw.shape), CD["Kh"], CD["Kw"],
+                                CHo, CWo, CD["s"], CD["p"], CD["op"])
+        import ctypes
+        self.c_ws = torch.empty(q8.lib().q8_conv2d_transposed_workspace_bytes(ctypes.byref(shape)),
+                                dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def launches_per_step(self):
+        n = {"quantize": 1, "chain_prep": 1, "linear": 1, "gemv": 1, "conv_t": 3}
+        if self.only == "all":
+            return sum(n.values())
+        return {"quantize": 1, "linear": 2, "gemv": 1, "conv_t": 3}[self.only]
+
+    def step(self, ev=None):
+        """Enqueue one step; ev (list of 6 CUDA events) brackets each op."""
+        q8, qp, lp, gp, cp = self.q8, Q.params, L.params, G.params, C.params
+        rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
+        rec(0)
+        if self.only in ("all", "quantize"):
+            q8.quantize_per_tensor(self.xq, qp["in_scale"], qp["in_zp"], out=self.q_out)
+        rec(1)
+        if self.only in ("all", "linear"):
+            q8.quantize_to_operand(self.lx, lp["in_scale"], lp["in_zp"], x_q=self.l_xq,
+                                   operand=self.operand)
+        rec(2)
+        if self.only in ("all", "linear"):
+            q8.linear_operand_packed(self.operand, lp["in_scale"], self.packed, self.lws, self.lb,
+                                     lp["out_scale"], lp["out_zp"], out=self.l_out)
+        rec(3)
+        if self.only in ("all", "gemv"):
+            q8.linear_gemv(self.gx, gp["in_scale"], gp["in_zp"], self.gw, None, self.gws, self.gb,
+                           gp["out_scale"], gp["out_zp"], out=self.g_out)
+        rec(4)
+        if self.only in ("all", "conv_t"):
+            q8.conv2d_transposed(self.cx, cp["in_scale"], cp["in_zp"], self.cw, None, self.cws,
+                                 self.cb, cp["out_scale"], cp["out_zp"], CD["Kh"], stride=CD["s"],
+                                 padding=CD["p"], output_padding=CD["op"], out=self.c_out,
+                                 workspace=self.c_ws)
+        rec(5)
+
+
+def e2e_measure(path, h, steps):
+    """Same step through the public API with host buffers: pinned host ->
+    device copies of every activation, the step, device -> pinned host copies
+    of every output, all inside the timed region."""
+    torch = path.torch
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    hx = {k: pin(h[k]) for k in ("xq", "lx", "gx", "cx")}
+    dst = {"xq": path.xq, "lx": path.lx, "gx": path.gx, "cx": path.cx}
+    outs = [path.q_out, path.l_out, path.g_out, path.c_out]
+    houts = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def one():
+        for k, t in hx.items():
+            dst[k].copy_(t, non_blocking=True)
+        path.step()
+        for o, ho in zip(outs, houts):
+            ho.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+def cpu_oracle_step_estimate(h, budget_s=12.0):
+    """Time the oracle on a bounded sample of each op on all host cores and
+    scale each op to its full size.  Returns (seconds per full step, cores,
+    sample description)."""
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    qp, lp, gp, cp = Q.params, L.params, G.params, C.params
+    # sample sizes (units of work that scale linearly)
+    q_n = 1 << 22                        # elements of the quantize
+    l_rows = max(cores, 8)               # rows of the 2048-row prefill
+    c_oc = 2                             # output channels of one conv image
+    xq_l = oracle.quantize_per_tensor(h["lx"][:l_rows], lp["in_scale"], lp["in_zp"])
+    Ho, Wo = CHo, CWo
+
+    def run_quant(i):
+        n = q_n // cores
+        oracle.quantize_per_tensor(h["xq"][i * n:(i + 1) * n], qp["in_scale"], qp["in_zp"])
+
+    def run_lin(i):
+        oracle.linear(xq_l[i:i + 1], lp["in_scale"], lp["in_zp"], h["lw"], h["lws"], h["lb"],
+                      lp["out_scale"], lp["out_zp"])
+
+    def run_gemv(i):
+        if i == 0:
+            oracle.linear(h["gx"], gp["in_scale"], gp["in_zp"], h["gw"], h["gws"], h["gb"],
+                          gp["out_scale"], gp["out_zp"])
+
+    def run_conv(i):
+        if i < c_oc:
+            oracle.conv2d_transposed(h["cx"][:1], cp["in_scale"], cp["in_zp"], h["cw"][i:i + 1],
+                                     CD["Kh"], CD["Kw"], h["cws"][i:i + 1], h["cb"][i:i + 1],
+                                     cp["out_scale"], cp["out_zp"], Ho, Wo, (CD["s"], CD["s"]),
+                                     (CD["p"], CD["p"]))
+
+    def timed(fn, n_items):
+        t0 = time.perf_counter()
+        with cf.ThreadPoolExecutor(max_workers=cores) as ex:   # ctypes releases the GIL
+            list(ex.map(fn, range(n_items)))
+        return time.perf_counter() - t0
+
+    t_q = timed(run_quant, cores) * (QN / (q_n // cores * cores))
+    t_l = timed(run_lin, l_rows) * (LM / l_rows)
+    t_g = timed(run_gemv, 1)
+    t_c = timed(run_conv, c_oc) * (CD["N"] * CD["OC"] / c_oc)
+    # the chain's quantize of [2048, 4096] at the quantize's measured rate
+    t_cq = t_q * (LM * LK) / QN
+    total = t_q + t_cq + t_l + t_g + t_c
+    sample = (f"quantize {q_n} of {QN} elements; linear {l_rows} of {LM} rows; gemv full; "
+              f"conv_t 1 of {CD['N']} images x {c_oc} of {CD['OC']} channels; "
+              f"each scaled linearly to the full op")
+    return total, cores, sample, dict(quantize=t_q, chain_quantize=t_cq, linear=t_l, gemv=t_g,
+                                      conv_t=t_c)
+
+
+def traffic_from_profile():
+    """dram read+write bytes per GEMM launch from the committed ncu summary,
+    valid only while the GEMM source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "int8_quantized_q8ta_gb300", "csrc", "tc_gemm.cu")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    e = d.get("tc_gemm_linear_2048x4096x11008")
+    if not e or e.get("source_sha256_16") != digest:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    h = host_inputs()
+    path = Path(h, dev, args.only)
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    for _ in range(args.warmup):
+        path.step()
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t_start.record()
+    for k in range(K):
+        path.step(evs[k])
+    t_end.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if dist:
+        tdist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_step = ms_total / K
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    names = ["quantize", "chain_prep", "linear", "gemv", "conv_t"]
+    per = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
+           for i, n in enumerate(names)}
+    hbm, bf16, peak_src = measured_peaks()
+    us = {n: per[n] * 1e3 for n in names}
+
+    ops = {
+        "quantize_64Mi": {"us": us["quantize"], "GB/s": BYTES_QUANT / us["quantize"] / 1e3,
+                          "frac_hbm": BYTES_QUANT / us["quantize"] / 1e3 / hbm},
+        "chain_quantize_to_operand_2048x4096": {
+            "us": us["chain_prep"], "GB/s": BYTES_CHAIN_PREP / us["chain_prep"] / 1e3},
+        "q8ta_linear_2048x4096x11008": {"us": us["linear"],
+                                        "TOPS": OPS_LINEAR / us["linear"] / 1e6,
+                                        "frac_bf16_peak": OPS_LINEAR / us["linear"] / 1e6 / bf16},
+        "q8ta_linear_gemv_1x4096x4096": {"us": us["gemv"], "GB/s": BYTES_GEMV / us["gemv"] / 1e3,
+                                         "frac_hbm": BYTES_GEMV / us["gemv"] / 1e3 / hbm},
+        "q8ta_conv2d_transposed_8x256x64x64": {
+            "us": us["conv_t"], "outputs/s": CONV_OUTPUTS / us["conv_t"] * 1e6,
+            "TOPS_valid_taps": OPS_CONV / us["conv_t"] / 1e6},
+    }
+    achieved = OPS_LINEAR / us["linear"] / 1e6
+    roofline = {"kernel": "tc_gemm_kernel (q8ta_linear 2048x4096x11008)", "bound": "tensor",
+                "achieved": achieved, "peak": bf16,
+                "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)",
+                "unit": "TFLOP/s", "frac": achieved / bf16,
+                "traffic": traffic_from_profile(),
+                "algorithmic_flops_per_launch": OPS_LINEAR}
+
+    result = {
+        "metric": METRIC, "value": world * OPS_STEP / (ms_step * 1e-3) / 1e12,
+        "unit": "int8 TOPS (2 x int8 MACs of linear + gemv + conv_t valid taps, per step)",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8", "data": "synthetic",
+        "config": {"workload": "q8ta hot path: quantize_per_tensor 64Mi; quantize->q8ta_linear "
+                               "2048x4096x11008; q8ta_linear_gemv 1x4096x4096; "
+                               "q8ta_conv2d_transposed 8x256x64x64 k3 s2 p1 op1",
+                   "inputs": "seeded synthetic, distributions of the five workloads",
+                   "l2": "each step streams > 0.5 GB (L2 is 129 MB), so no input is L2-resident "
+                         "from the previous step",
+                   "weights": "linear weight packed to bf16 once, outside the timed region "
+                              "(load time); gemv and conv_t weights raw int8",
+                   "parallelism": f"replicas x{world}"},
+        "ops": ops, "roofline": roofline, "clocks": clocks,
+        "gpu_launches": path.launches_per_step() * K,
+    }
+    if args.only != "all":
+        result["config"]["only"] = args.only
+    if rank == 0 and not args.no_e2e and args.only == "all":
+        e2e_ms, h2d, d2h = e2e_measure(path, h, max(3, min(K, 10)))
+        result["e2e"] = {"value": world * OPS_STEP / (e2e_ms * 1e-3) / 1e12,
+                         "unit": result["unit"], "ms_per_step": e2e_ms,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "note": "activations copied in from pinned host memory and every output "
+                                 "copied back each step; weights resident"}
+    if rank == 0 and not args.no_cpu_baseline and args.only == "all":
+        t_cpu, cores, sample, parts = cpu_oracle_step_estimate(h)
+        result["cpu_baseline"] = {"value": OPS_STEP / t_cpu / 1e12, "unit": result["unit"],
+                                  "cores": cores, "kind": "oracle", "sample": sample,
+                                  "seconds_per_full_step": t_cpu,
+                                  "seconds_by_op": parts}
+    return result
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, on bounded samples of the
+    same workload; each step is one bounded sample."""
+    h = host_inputs()
+    for _ in range(args.warmup):
+        cpu_oracle_step_estimate(h)
+    ts, last = [], None
+    for _ in range(args.steps):
+        t, cores, sample, parts = cpu_oracle_step_estimate(h)
+        ts.append(t)
+        last = (cores, sample)
+    t = statistics.median(ts)
+    v = OPS_STEP / t / 1e12
+    unit = "int8 TOPS (2 x int8 MACs of linear + gemv + conv_t valid taps, per step)"
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic",
+            "config": {"workload": "q8ta hot path (same as the CUDA arm), CPU oracle on "
+                                   "bounded samples scaled to the full step"},
+            "cpu_baseline": {"value": v, "unit": unit, "cores": last[0], "kind": "oracle",
+                             "sample": last[1]},
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only", choices=["all", "quantize", "linear", "gemv", "conv_t"],
+                    default="all", help="run one op per step (for profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.only == "all":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,252 @@
+/*
+ * q8ta.h -- C ABI of the GB300 (sm_103a) q8ta int8 quantized contraction.
+ *
+ * The operations follow three ExecuTorch WebGPU pull-request pages:
+ *   [quantize] "Add quantize_per_tensor op (int8 buffer path)", PR #21187,
+ *              Solution and Implementation paragraphs;
+ *   [linear]   "Add q8ta_linear op", PR #21197, Solution, Implementation
+ *              and Constraints paragraphs;
+ *   [conv_t]   "Add q8ta_conv2d_transposed op (int8 transposed conv)",
+ *              PR #21205, Solution, Implementation and Constraints paragraphs.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is caller-owned DEVICE memory (cudaMalloc, a torch
+ *   CUDA tensor, ...), unless a parameter says "host".  The library keeps
+ *   no pointer after a call returns and allocates no device memory: scratch
+ *   space is passed in as `workspace` (size from the matching
+ *   *_workspace_bytes query).
+ * - All work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *   default stream) and is asynchronous: inputs, outputs and workspace must
+ *   stay valid until the stream has passed the call.  Calls that share a
+ *   workspace must be ordered on one stream.
+ * - Tensors are dense, row-major (C order) unless stated.  int8 outputs are
+ *   plain bytes; the pages' "4 int8 packed per 32-bit word" layout is the
+ *   same memory read as little-endian words (byte j of word i is element
+ *   4*i + j).
+ * - Every argument check runs on the host BEFORE anything is enqueued; a
+ *   failing check returns its status and launches nothing ("fail-loud" on
+ *   the pages).  Q8_ERR_CUDA reports a failed launch or runtime call.
+ * - Rounding is round-half-to-even everywhere.  Scales arrive as double
+ *   (the schema's float); reciprocals are taken in double and cast to f32:
+ *   inv_scale = (float)(1.0 / scale)                                [quantize]
+ *   inv_output_scale = (float)(1.0 / output_scale)   (same convention)
+ *   The dequantize/requantize epilogue is evaluated in f32, one rounding per
+ *   step, in this order and without fused multiply-add:
+ *     a = (float)acc; t = a * (float)input_scale; t = t * weight_scales[n];
+ *     v = t + bias[n]; u = v * inv_output_scale;
+ *     q = clamp(rint(u) + output_zero_point, -128, 127)        [linear]
+ * - Scales must be finite and > 0; zero points must lie in [-128, 127]
+ *   (they are zero points of int8 tensors); otherwise Q8_ERR_ARG.
+ */
+#ifndef Q8TA_H_
+#define Q8TA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* q8_stream_t;
+
+typedef enum q8_status {
+  Q8_OK = 0,
+  Q8_ERR_NULL = 1,        /* a required pointer is NULL */
+  Q8_ERR_SHAPE = 2,       /* a size or shape guard failed */
+  Q8_ERR_ALIGN = 3,       /* a pointer misses a documented alignment */
+  Q8_ERR_UNSUPPORTED = 4, /* activation != "none", groups != 1, dilation != 1 */
+  Q8_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required */
+  Q8_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+  Q8_ERR_DEVICE = 7,      /* a kernel raised the library's device error word */
+  Q8_ERR_ARG = 8          /* a scalar argument is out of range */
+} q8_status;
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* q8_status_string(int status);
+
+/* Library ABI version, currently 1. */
+int q8_version(void);
+
+/*
+ * Device error word.  Kernels that wait on pipeline barriers give every wait
+ * a time limit (about one second); on expiry they record a code here, stop
+ * issuing work and return, leaving the CUDA context usable.  This call
+ * synchronizes the current device, copies the word to *code (host pointer)
+ * and, if clear != 0, resets it to 0.  Q8_OK is returned when the copy
+ * succeeded, whatever the word holds.
+ */
+q8_status q8_device_error(uint32_t* code, int clear);
+
+/* ------------------------------------------------------------------------ */
+/* quantize_per_tensor: fp32 -> int8                               [quantize] */
+/* ------------------------------------------------------------------------ */
+/*
+ * out[i] = clamp(rint(x[i] * inv_scale) + zero_point, -128, 127).
+ * x: float32[numel]; out: int8[numel].
+ * Guards (as on the page): x, out non-NULL; numel % 4 == 0 (the page's
+ * packed-word binding); numel >= 0 (0 is a no-op).
+ */
+q8_status q8_quantize_per_tensor(const float* x, int64_t numel, double scale,
+                                 int32_t zero_point, int8_t* out, q8_stream_t stream);
+
+/*
+ * dequantize_per_tensor: int8 -> fp32, the op that closes the
+ * quantize -> q8ta_* -> dequantize subgraph named in the Problem paragraphs
+ * of [linear] and [conv_t].  out[i] = ((float)q[i] - (float)zero_point) *
+ * (float)scale, one f32 rounding per step.  Same guards as quantize.
+ */
+q8_status q8_dequantize_per_tensor(const int8_t* q, int64_t numel, double scale,
+                                   int32_t zero_point, float* out, q8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* q8ta_linear / q8ta_linear_gemv                                   [linear] */
+/* ------------------------------------------------------------------------ */
+/*
+ * acc[m,n] = sum_k (x[m,k] - input_zero_point) * weight[n,k]   (exact int32,
+ * wrapping modulo 2^32), then the epilogue above with weight_scales[n] and
+ * bias[n]; out[m,n] int8.
+ *   x             int8 [M, K] row-major
+ *   weight        int8 [N, K] row-major (per-output-channel symmetric)
+ *   weight_sums   accepted and ignored (the pages fold the zero point per
+ *                 element instead of using precomputed sums); may be NULL
+ *   weight_scales float [>= N]; only [0, N) is read
+ *   bias          float [>= N] or NULL (= zero bias)
+ *   activation    host C string; must be "none" (Q8_ERR_UNSUPPORTED else)
+ *   out           int8 [M, N] row-major
+ * Guards (as on the page): N % 4 == 0, (M*K) % 4 == 0, (N*K) % 4 == 0,
+ * M, N, K >= 1.
+ *
+ * The contraction runs on the tcgen05 tensor cores with bf16 operands that
+ * hold the int8 values exactly; workspace holds the bf16 operand copies:
+ * q8_linear_workspace_bytes(M, K, N) bytes, 256-byte aligned.  When
+ * M == 1 the bandwidth-bound gemv kernel runs instead and workspace may be
+ * NULL (the query returns 0).
+ */
+size_t q8_linear_workspace_bytes(int64_t M, int64_t K, int64_t N);
+q8_status q8_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
+                    int32_t input_zero_point, const int8_t* weight, int64_t N,
+                    const int32_t* weight_sums, const float* weight_scales, const float* bias,
+                    double output_scale, int32_t output_zero_point, const char* activation,
+                    int8_t* out, void* workspace, size_t workspace_bytes, q8_stream_t stream);
+
+/* The M == 1 case with the identical schema; returns Q8_ERR_SHAPE unless
+ * M == 1.  Needs no workspace (pass NULL, 0). */
+q8_status q8_linear_gemv(const int8_t* x, int64_t M, int64_t K, double input_scale,
+                         int32_t input_zero_point, const int8_t* weight, int64_t N,
+                         const int32_t* weight_sums, const float* weight_scales,
+                         const float* bias, double output_scale, int32_t output_zero_point,
+                         const char* activation, int8_t* out, void* workspace,
+                         size_t workspace_bytes, q8_stream_t stream);
+
+/*
+ * Load-time weight packing.  A linear layer's weight is a constant, so the
+ * bf16 copy the tensor cores read can be made once:
+ *   q8_linear_pack_weight writes q8_linear_packed_weight_bytes(N, K) bytes
+ *   (256-byte aligned buffer) from the int8 [N, K] weight.
+ * Results of every *_packed call are identical to q8_linear.
+ */
+size_t q8_linear_packed_weight_bytes(int64_t N, int64_t K);
+q8_status q8_linear_pack_weight(const int8_t* weight, int64_t N, int64_t K, void* packed,
+                                size_t packed_bytes, q8_stream_t stream);
+
+/*
+ * The activation operand: the bf16 copy of x - input_zero_point that the
+ * tensor cores read, q8_linear_operand_bytes(M, K) bytes (256-byte aligned).
+ *   q8_linear_prepare_operand      from int8 x [M, K];
+ *   q8_quantize_to_linear_operand  from fp32 x [M, K]: quantize_per_tensor
+ *       with (input_scale, input_zero_point) exactly as
+ *       q8_quantize_per_tensor does, fused with the operand preparation
+ *       (the pages' quantize -> q8ta_linear subgraph); x_q (int8 [M, K],
+ *       may be NULL) receives the quantized activations.
+ *   q8_linear_operand_packed       runs the contraction and the epilogue
+ *       from a prepared operand and a packed weight (one kernel).
+ * Guards: those of q8_linear (and of quantize for the fp32 form).
+ */
+size_t q8_linear_operand_bytes(int64_t M, int64_t K);
+q8_status q8_linear_prepare_operand(const int8_t* x, int64_t M, int64_t K,
+                                    int32_t input_zero_point, void* operand,
+                                    size_t operand_bytes, q8_stream_t stream);
+q8_status q8_quantize_to_linear_operand(const float* x_f32, int64_t M, int64_t K,
+                                        double input_scale, int32_t input_zero_point,
+                                        int8_t* x_q, void* operand, size_t operand_bytes,
+                                        q8_stream_t stream);
+q8_status q8_linear_operand_packed(const void* operand, int64_t M, int64_t K, double input_scale,
+                                   const void* packed_weight, int64_t N,
+                                   const float* weight_scales, const float* bias,
+                                   double output_scale, int32_t output_zero_point,
+                                   const char* activation, int8_t* out, q8_stream_t stream);
+
+/* Convenience forms: prepare the operand into `workspace`
+ * (q8_linear_operand_bytes(M, K) bytes), then q8_linear_operand_packed. */
+q8_status q8_linear_packed(const int8_t* x, int64_t M, int64_t K, double input_scale,
+                           int32_t input_zero_point, const void* packed_weight, int64_t N,
+                           const float* weight_scales, const float* bias, double output_scale,
+                           int32_t output_zero_point, const char* activation, int8_t* out,
+                           void* workspace, size_t workspace_bytes, q8_stream_t stream);
+q8_status q8_quantize_linear_packed(const float* x_f32, int64_t M, int64_t K, double input_scale,
+                                    int32_t input_zero_point, const void* packed_weight,
+                                    int64_t N, const float* weight_scales, const float* bias,
+                                    double output_scale, int32_t output_zero_point,
+                                    const char* activation, int8_t* x_q, int8_t* out,
+                                    void* workspace, size_t workspace_bytes, q8_stream_t stream);
+
+/* Test and debugging form of q8_linear_packed: writes the exact int32
+ * accumulators acc[m,n] (int32 [M, N]) instead of the int8 output. */
+q8_status q8_linear_packed_acc32(const int8_t* x, int64_t M, int64_t K, int32_t input_zero_point,
+                                 const void* packed_weight, int64_t N, int32_t* acc,
+                                 void* workspace, size_t workspace_bytes, q8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* q8ta_conv2d_transposed                                            [conv_t] */
+/* ------------------------------------------------------------------------ */
+typedef struct q8_conv2d_transposed_shape {
+  int64_t N, IC, H_in, W_in;          /* x      int8 [N, IC, H_in, W_in] (NCHW) */
+  int64_t OC, Kh, Kw;                 /* weight int8 [OC, weight_row_stride]    */
+  int64_t weight_row_stride;          /* >= Kh*Kw*IC (tolerates row padding)    */
+  int64_t H_out, W_out;               /* out    int8 [N, OC, H_out, W_out]      */
+  int64_t stride_h, stride_w;         /* >= 1                                   */
+  int64_t pad_h, pad_w;               /* >= 0                                   */
+  int64_t output_padding_h, output_padding_w; /* accepted, unused: the output
+                                         size is H_out/W_out as given           */
+  int64_t dilation_h, dilation_w;     /* must be 1 (Q8_ERR_UNSUPPORTED else)    */
+  int64_t groups;                     /* must be 1 (Q8_ERR_UNSUPPORTED else)    */
+} q8_conv2d_transposed_shape;
+
+/*
+ * For every output (n, oc, oh, ow):
+ *   acc = sum over ic, kh, kw of (x[n,ic,ih,iw] - input_zero_point) *
+ *         weight[oc, (kh*Kw + kw)*IC + ic]
+ * where ih = (oh + pad_h - kh) / stride_h is used only when the numerator is
+ * >= 0, divisible by stride_h and ih < H_in (iw likewise); taps that fail
+ * contribute nothing.  Then the epilogue above with weight_scales[oc] and
+ * bias[oc] (arrays of length >= OC; only [0, OC) is read).
+ * Guards (as on the page): groups == 1, dilation == 1, stride >= 1,
+ * activation == "none", W_out % 4 == 0, weight_row_stride >= Kh*Kw*IC;
+ * plus every size >= 1 and pad >= 0.  weight_sums is accepted and ignored.
+ * workspace: q8_conv2d_transposed_workspace_bytes(shape) bytes, 256-byte
+ * aligned (an NHWC bf16 copy of x - input_zero_point and a bf16 copy of the
+ * weight).
+ */
+size_t q8_conv2d_transposed_workspace_bytes(const q8_conv2d_transposed_shape* shape);
+q8_status q8_conv2d_transposed(const int8_t* x, const q8_conv2d_transposed_shape* shape,
+                               double input_scale, int32_t input_zero_point,
+                               const int8_t* weight, const int32_t* weight_sums,
+                               const float* weight_scales, const float* bias,
+                               double output_scale, int32_t output_zero_point,
+                               const char* activation, int8_t* out, void* workspace,
+                               size_t workspace_bytes, q8_stream_t stream);
+
+/* Test and debugging form: writes the exact int32 accumulators
+ * acc int32 [N, OC, H_out, W_out] instead of the int8 output. */
+q8_status q8_conv2d_transposed_acc32(const int8_t* x, const q8_conv2d_transposed_shape* shape,
+                                     int32_t input_zero_point, const int8_t* weight,
+                                     int32_t* acc, void* workspace, size_t workspace_bytes,
+                                     q8_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q8TA_H_ */

@@ -1,0 +1,419 @@
+// api.cu -- the extern "C" boundary declared in include/q8ta.h.
+//
+// Each entry point validates every argument on the host before anything is
+// enqueued (the "fail-loud" guards of the three q8ta pages' Implementation
+// paragraphs), forms the f32 reciprocals in double, lays out the caller's
+// workspace and enqueues the kernels on the caller's stream.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "q8ta.h"
+#include "q8ta_internal.h"
+
+namespace {
+
+using q8::align_ws;
+using q8::kTileK;
+using q8::round_up;
+
+inline cudaStream_t cs(q8_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline q8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? Q8_OK : Q8_ERR_CUDA; }
+
+inline bool scale_ok(double s) { return std::isfinite(s) && s > 0.0; }
+inline bool zp_ok(int32_t z) { return z >= -128 && z <= 127; }
+
+// (float)(1.0 / scale): the reciprocal in double, then one rounding to f32
+// ("Add quantize_per_tensor op", Solution paragraph).
+inline float recip_f32(double scale) { return static_cast<float>(1.0 / scale); }
+
+inline bool activation_none(const char* a) { return a != nullptr && std::strcmp(a, "none") == 0; }
+
+inline bool mul_ok(int64_t a, int64_t b) { return a == 0 || b <= INT64_MAX / a; }
+
+q8::Requant make_rq(double input_scale, double output_scale, int32_t ozp) {
+  q8::Requant r;
+  r.s_in = static_cast<float>(input_scale);
+  r.inv_out = recip_f32(output_scale);
+  r.ozp = static_cast<float>(ozp);
+  return r;
+}
+
+// Guards shared by q8_linear and q8_linear_gemv ("Add q8ta_linear op",
+// Implementation paragraph): int8 operands (typed), N % 4 == 0,
+// (M*K) % 4 == 0, (N*K) % 4 == 0, activation == "none".
+q8_status check_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
+                       int32_t izp, const void* weight, int64_t N, const float* ws,
+                       double output_scale, int32_t ozp, const char* activation,
+                       const void* out) {
+  if (!x || !weight || !ws || !out || !activation) return Q8_ERR_NULL;
+  if (M < 1 || K < 1 || N < 1) return Q8_ERR_SHAPE;
+  if (!mul_ok(M, K) || !mul_ok(N, K) || !mul_ok(M, N)) return Q8_ERR_SHAPE;
+  if (N % 4 != 0 || (M * K) % 4 != 0 || (N * K) % 4 != 0) return Q8_ERR_SHAPE;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX / 2) return Q8_ERR_SHAPE;
+  if (!activation_none(activation)) return Q8_ERR_UNSUPPORTED;
+  if (!scale_ok(input_scale) || !scale_ok(output_scale) || !zp_ok(izp) || !zp_ok(ozp))
+    return Q8_ERR_ARG;
+  return Q8_OK;
+}
+
+size_t bf16_rows_bytes(int64_t rows, int64_t K) {
+  return align_ws(static_cast<size_t>(rows) * static_cast<size_t>(round_up(K, kTileK)) * 2);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* q8_status_string(int status) {
+  switch (status) {
+    case Q8_OK: return "Q8_OK";
+    case Q8_ERR_NULL: return "Q8_ERR_NULL: a required pointer is NULL";
+    case Q8_ERR_SHAPE: return "Q8_ERR_SHAPE: a size or shape guard failed";
+    case Q8_ERR_ALIGN: return "Q8_ERR_ALIGN: a pointer misses a documented alignment";
+    case Q8_ERR_UNSUPPORTED:
+      return "Q8_ERR_UNSUPPORTED: activation, groups or dilation not supported";
+    case Q8_ERR_WORKSPACE: return "Q8_ERR_WORKSPACE: workspace missing or too small";
+    case Q8_ERR_CUDA: return "Q8_ERR_CUDA: a CUDA call or kernel launch failed";
+    case Q8_ERR_DEVICE: return "Q8_ERR_DEVICE: a kernel raised the device error word";
+    case Q8_ERR_ARG: return "Q8_ERR_ARG: a scale or zero point is out of range";
+    default: return "unknown q8_status";
+  }
+}
+
+int q8_version(void) { return 1; }
+
+q8_status q8_device_error(uint32_t* code, int clear) {
+  if (!code) return Q8_ERR_NULL;
+  return cuda_status(q8::read_device_error(code, clear != 0));
+}
+
+// ---------------------------------------------------------------- quantize
+q8_status q8_quantize_per_tensor(const float* x, int64_t numel, double scale, int32_t zero_point,
+                                 int8_t* out, q8_stream_t stream) {
+  if (!x || !out) return Q8_ERR_NULL;
+  if (numel < 0 || numel % 4 != 0) return Q8_ERR_SHAPE;
+  if (!scale_ok(scale) || !zp_ok(zero_point)) return Q8_ERR_ARG;
+  return cuda_status(q8::launch_quantize(x, numel, recip_f32(scale),
+                                         static_cast<float>(zero_point), out, cs(stream)));
+}
+
+q8_status q8_dequantize_per_tensor(const int8_t* q, int64_t numel, double scale,
+                                   int32_t zero_point, float* out, q8_stream_t stream) {
+  if (!q || !out) return Q8_ERR_NULL;
+  if (numel < 0 || numel % 4 != 0) return Q8_ERR_SHAPE;
+  if (!scale_ok(scale) || !zp_ok(zero_point)) return Q8_ERR_ARG;
+  return cuda_status(q8::launch_dequantize(q, numel, static_cast<float>(scale),
+                                           static_cast<float>(zero_point), out, cs(stream)));
+}
+
+// ---------------------------------------------------------------- linear
+size_t q8_linear_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+  if (M <= 1 || K < 1 || N < 1) return 0;
+  return bf16_rows_bytes(M, K) + bf16_rows_bytes(N, K);
+}
+
+size_t q8_linear_packed_weight_bytes(int64_t N, int64_t K) {
+  if (N < 1 || K < 1) return 0;
+  return bf16_rows_bytes(N, K);
+}
+
+size_t q8_linear_operand_bytes(int64_t M, int64_t K) {
+  if (M < 1 || K < 1) return 0;
+  return bf16_rows_bytes(M, K);
+}
+
+q8_status q8_linear_gemv(const int8_t* x, int64_t M, int64_t K, double input_scale,
+                         int32_t input_zero_point, const int8_t* weight, int64_t N,
+                         const int32_t* weight_sums, const float* weight_scales,
+                         const float* bias, double output_scale, int32_t output_zero_point,
+                         const char* activation, int8_t* out, void* workspace,
+                         size_t workspace_bytes, q8_stream_t stream) {
+  (void)weight_sums;
+  (void)workspace;
+  (void)workspace_bytes;
+  q8_status st = check_linear(x, M, K, input_scale, input_zero_point, weight, N, weight_scales,
+                              output_scale, output_zero_point, activation, out);
+  if (st != Q8_OK) return st;
+  if (M != 1) return Q8_ERR_SHAPE;
+  return cuda_status(q8::launch_gemv(x, K, input_zero_point, weight, N, weight_scales, bias,
+                                     make_rq(input_scale, output_scale, output_zero_point), out,
+                                     cs(stream)));
+}
+
+q8_status q8_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
+                    int32_t input_zero_point, const int8_t* weight, int64_t N,
+                    const int32_t* weight_sums, const float* weight_scales, const float* bias,
+                    double output_scale, int32_t output_zero_point, const char* activation,
+                    int8_t* out, void* workspace, size_t workspace_bytes, q8_stream_t stream) {
+  q8_status st = check_linear(x, M, K, input_scale, input_zero_point, weight, N, weight_scales,
+                              output_scale, output_zero_point, activation, out);
+  if (st != Q8_OK) return st;
+  if (M == 1)
+    return q8_linear_gemv(x, M, K, input_scale, input_zero_point, weight, N, weight_sums,
+                          weight_scales, bias, output_scale, output_zero_point, activation, out,
+                          nullptr, 0, stream);
+  const size_t need = q8_linear_workspace_bytes(M, K, N);
+  if (!workspace || workspace_bytes < need) return Q8_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
+  const int64_t Kp = round_up(K, kTileK);
+  auto* a = static_cast<__nv_bfloat16*>(workspace);
+  auto* b = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) + bf16_rows_bytes(M, K));
+  cudaError_t e = q8::launch_rows_to_bf16(x, M, K, K, input_zero_point, a, Kp, cs(stream));
+  if (e == cudaSuccess) e = q8::launch_rows_to_bf16(weight, N, K, K, 0, b, Kp, cs(stream));
+  if (e != cudaSuccess) return Q8_ERR_CUDA;
+  q8::TcLinear L{};
+  L.a = a;
+  L.b = b;
+  L.M = M;
+  L.N = N;
+  L.Kp = Kp;
+  L.ws = weight_scales;
+  L.bias = bias;
+  L.rq = make_rq(input_scale, output_scale, output_zero_point);
+  L.out = out;
+  return cuda_status(q8::launch_tc_linear(L, cs(stream)));
+}
+
+q8_status q8_linear_pack_weight(const int8_t* weight, int64_t N, int64_t K, void* packed,
+                                size_t packed_bytes, q8_stream_t stream) {
+  if (!weight || !packed) return Q8_ERR_NULL;
+  if (N < 1 || K < 1 || !mul_ok(N, K) || N > INT32_MAX || K > INT32_MAX / 2) return Q8_ERR_SHAPE;
+  if (packed_bytes < q8_linear_packed_weight_bytes(N, K)) return Q8_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(packed) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
+  return cuda_status(q8::launch_rows_to_bf16(weight, N, K, K, 0,
+                                             static_cast<__nv_bfloat16*>(packed),
+                                             round_up(K, kTileK), cs(stream)));
+}
+
+static q8_status check_operand(const void* operand, size_t operand_bytes, int64_t M, int64_t K) {
+  if (!operand) return Q8_ERR_WORKSPACE;
+  if (operand_bytes < q8_linear_operand_bytes(M, K)) return Q8_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(operand) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
+  return Q8_OK;
+}
+
+q8_status q8_linear_prepare_operand(const int8_t* x, int64_t M, int64_t K,
+                                    int32_t input_zero_point, void* operand,
+                                    size_t operand_bytes, q8_stream_t stream) {
+  if (!x) return Q8_ERR_NULL;
+  if (M < 1 || K < 1 || !mul_ok(M, K) || (M * K) % 4 != 0) return Q8_ERR_SHAPE;
+  if (M > INT32_MAX || K > INT32_MAX / 2) return Q8_ERR_SHAPE;
+  if (!zp_ok(input_zero_point)) return Q8_ERR_ARG;
+  q8_status st = check_operand(operand, operand_bytes, M, K);
+  if (st != Q8_OK) return st;
+  return cuda_status(q8::launch_rows_to_bf16(x, M, K, K, input_zero_point,
+                                             static_cast<__nv_bfloat16*>(operand),
+                                             round_up(K, kTileK), cs(stream)));
+}
+
+q8_status q8_quantize_to_linear_operand(const float* x_f32, int64_t M, int64_t K,
+                                        double input_scale, int32_t input_zero_point,
+                                        int8_t* x_q, void* operand, size_t operand_bytes,
+                                        q8_stream_t stream) {
+  if (!x_f32) return Q8_ERR_NULL;
+  if (M < 1 || K < 1 || !mul_ok(M, K) || (M * K) % 4 != 0) return Q8_ERR_SHAPE;
+  if (M > INT32_MAX || K > INT32_MAX / 2) return Q8_ERR_SHAPE;
+  if (!scale_ok(input_scale) || !zp_ok(input_zero_point)) return Q8_ERR_ARG;
+  q8_status st = check_operand(operand, operand_bytes, M, K);
+  if (st != Q8_OK) return st;
+  return cuda_status(q8::launch_quantize_rows_bf16(
+      x_f32, M, K, recip_f32(input_scale), input_zero_point, x_q,
+      static_cast<__nv_bfloat16*>(operand), round_up(K, kTileK), cs(stream)));
+}
+
+static q8_status run_operand_packed(const void* operand, int64_t M, int64_t K, double input_scale,
+                                    const void* packed, int64_t N, const float* ws,
+                                    const float* bias, double output_scale, int32_t ozp,
+                                    int8_t* out, int32_t* acc_out, q8_stream_t stream) {
+  if (reinterpret_cast<uintptr_t>(packed) % q8::kWorkspaceAlign != 0 ||
+      reinterpret_cast<uintptr_t>(operand) % q8::kWorkspaceAlign != 0)
+    return Q8_ERR_ALIGN;
+  q8::TcLinear L{};
+  L.a = static_cast<const __nv_bfloat16*>(operand);
+  L.b = static_cast<const __nv_bfloat16*>(packed);
+  L.M = M;
+  L.N = N;
+  L.Kp = round_up(K, kTileK);
+  L.ws = ws;
+  L.bias = bias;
+  L.rq = make_rq(input_scale, output_scale, ozp);
+  L.out = out;
+  L.acc_out = acc_out;
+  return cuda_status(q8::launch_tc_linear(L, cs(stream)));
+}
+
+q8_status q8_linear_operand_packed(const void* operand, int64_t M, int64_t K, double input_scale,
+                                   const void* packed_weight, int64_t N,
+                                   const float* weight_scales, const float* bias,
+                                   double output_scale, int32_t output_zero_point,
+                                   const char* activation, int8_t* out, q8_stream_t stream) {
+  if (!operand) return Q8_ERR_NULL;
+  // input_zero_point is already applied inside the operand; 0 passes its guard
+  q8_status st = check_linear(static_cast<const int8_t*>(operand), M, K, input_scale, 0,
+                              packed_weight, N, weight_scales, output_scale, output_zero_point,
+                              activation, out);
+  if (st != Q8_OK) return st;
+  return run_operand_packed(operand, M, K, input_scale, packed_weight, N, weight_scales, bias,
+                            output_scale, output_zero_point, out, nullptr, stream);
+}
+
+q8_status q8_linear_packed(const int8_t* x, int64_t M, int64_t K, double input_scale,
+                           int32_t input_zero_point, const void* packed_weight, int64_t N,
+                           const float* weight_scales, const float* bias, double output_scale,
+                           int32_t output_zero_point, const char* activation, int8_t* out,
+                           void* workspace, size_t workspace_bytes, q8_stream_t stream) {
+  q8_status st = check_linear(x, M, K, input_scale, input_zero_point, packed_weight, N,
+                              weight_scales, output_scale, output_zero_point, activation, out);
+  if (st != Q8_OK) return st;
+  st = q8_linear_prepare_operand(x, M, K, input_zero_point, workspace, workspace_bytes, stream);
+  if (st != Q8_OK) return st;
+  return run_operand_packed(workspace, M, K, input_scale, packed_weight, N, weight_scales, bias,
+                            output_scale, output_zero_point, out, nullptr, stream);
+}
+
+q8_status q8_quantize_linear_packed(const float* x_f32, int64_t M, int64_t K, double input_scale,
+                                    int32_t input_zero_point, const void* packed_weight,
+                                    int64_t N, const float* weight_scales, const float* bias,
+                                    double output_scale, int32_t output_zero_point,
+                                    const char* activation, int8_t* x_q, int8_t* out,
+                                    void* workspace, size_t workspace_bytes, q8_stream_t stream) {
+  if (!x_f32) return Q8_ERR_NULL;
+  // the quantize op's guard (numel % 4) is implied by (M*K) % 4 == 0 below
+  q8_status st = check_linear(reinterpret_cast<const int8_t*>(x_f32), M, K, input_scale,
+                              input_zero_point, packed_weight, N, weight_scales, output_scale,
+                              output_zero_point, activation, out);
+  if (st != Q8_OK) return st;
+  st = q8_quantize_to_linear_operand(x_f32, M, K, input_scale, input_zero_point, x_q, workspace,
+                                     workspace_bytes, stream);
+  if (st != Q8_OK) return st;
+  return run_operand_packed(workspace, M, K, input_scale, packed_weight, N, weight_scales, bias,
+                            output_scale, output_zero_point, out, nullptr, stream);
+}
+
+q8_status q8_linear_packed_acc32(const int8_t* x, int64_t M, int64_t K, int32_t input_zero_point,
+                                 const void* packed_weight, int64_t N, int32_t* acc,
+                                 void* workspace, size_t workspace_bytes, q8_stream_t stream) {
+  static const float kOne = 1.0f;
+  q8_status st = check_linear(x, M, K, 1.0, input_zero_point, packed_weight, N, &kOne, 1.0, 0,
+                              "none", acc);
+  if (st != Q8_OK) return st;
+  st = q8_linear_prepare_operand(x, M, K, input_zero_point, workspace, workspace_bytes, stream);
+  if (st != Q8_OK) return st;
+  return run_operand_packed(workspace, M, K, 1.0, packed_weight, N, nullptr, nullptr, 1.0, 0,
+                            nullptr, acc, stream);
+}
+
+// ---------------------------------------------------------------- conv_t
+static q8_status check_conv_t(const int8_t* x, const q8_conv2d_transposed_shape* sh,
+                              const int8_t* weight, const void* out) {
+  if (!x || !sh || !weight || !out) return Q8_ERR_NULL;
+  const q8_conv2d_transposed_shape& s = *sh;
+  if (s.groups != 1 || s.dilation_h != 1 || s.dilation_w != 1) return Q8_ERR_UNSUPPORTED;
+  if (s.stride_h < 1 || s.stride_w < 1) return Q8_ERR_SHAPE;
+  if (s.N < 1 || s.IC < 1 || s.H_in < 1 || s.W_in < 1 || s.OC < 1 || s.Kh < 1 || s.Kw < 1 ||
+      s.H_out < 1 || s.W_out < 1)
+    return Q8_ERR_SHAPE;
+  if (s.pad_h < 0 || s.pad_w < 0 || s.output_padding_h < 0 || s.output_padding_w < 0)
+    return Q8_ERR_SHAPE;
+  if (s.W_out % 4 != 0) return Q8_ERR_SHAPE;
+  if (!mul_ok(s.Kh, s.Kw) || !mul_ok(s.Kh * s.Kw, s.IC)) return Q8_ERR_SHAPE;
+  if (s.weight_row_stride < s.Kh * s.Kw * s.IC) return Q8_ERR_SHAPE;
+  // sizes the kernels index with 32-bit tile coordinates
+  const int64_t lim = INT32_MAX / 4;
+  if (s.N > lim || s.IC > lim || s.H_in > lim || s.W_in > lim || s.OC > lim || s.H_out > lim ||
+      s.W_out > lim || s.Kh > 4096 || s.Kw > 4096 || s.stride_h > 4096 || s.stride_w > 4096 ||
+      s.pad_h > lim || s.pad_w > lim)
+    return Q8_ERR_SHAPE;
+  if (!mul_ok(s.N * s.H_in, s.W_in) || !mul_ok(s.N * s.H_in * s.W_in, round_up(s.IC, kTileK)))
+    return Q8_ERR_SHAPE;
+  return Q8_OK;
+}
+
+size_t q8_conv2d_transposed_workspace_bytes(const q8_conv2d_transposed_shape* sh) {
+  if (!sh || sh->N < 1 || sh->IC < 1 || sh->H_in < 1 || sh->W_in < 1 || sh->OC < 1 ||
+      sh->Kh < 1 || sh->Kw < 1)
+    return 0;
+  const int64_t ICp = round_up(sh->IC, kTileK);
+  return align_ws(static_cast<size_t>(sh->N * sh->H_in * sh->W_in) * ICp * 2) +
+         align_ws(static_cast<size_t>(sh->OC * sh->Kh * sh->Kw) * ICp * 2);
+}
+
+static q8_status conv_t_common(const int8_t* x, const q8_conv2d_transposed_shape* sh,
+                               double input_scale, int32_t izp, const int8_t* weight,
+                               const float* ws, const float* bias, double output_scale,
+                               int32_t ozp, int8_t* out, int32_t* acc_out, void* workspace,
+                               size_t workspace_bytes, q8_stream_t stream) {
+  const q8_conv2d_transposed_shape& s = *sh;
+  const size_t need = q8_conv2d_transposed_workspace_bytes(sh);
+  if (!workspace || workspace_bytes < need) return Q8_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
+  const int64_t ICp = round_up(s.IC, kTileK);
+  auto* a = static_cast<__nv_bfloat16*>(workspace);
+  auto* b = reinterpret_cast<__nv_bfloat16*>(
+      static_cast<char*>(workspace) + align_ws(static_cast<size_t>(s.N * s.H_in * s.W_in) * ICp * 2));
+  cudaError_t e = q8::launch_nchw_to_nhwc_bf16(x, s.N, s.IC, s.H_in, s.W_in, izp, a, ICp, cs(stream));
+  if (e == cudaSuccess)
+    e = q8::launch_convt_weight_bf16(weight, s.OC, s.Kh * s.Kw, s.IC, s.weight_row_stride, b, ICp,
+                                     cs(stream));
+  if (e != cudaSuccess) return Q8_ERR_CUDA;
+  q8::TcConvT C{};
+  C.a = a;
+  C.b = b;
+  C.N = s.N;
+  C.ICp = ICp;
+  C.H_in = s.H_in;
+  C.W_in = s.W_in;
+  C.OC = s.OC;
+  C.Kh = s.Kh;
+  C.Kw = s.Kw;
+  C.H_out = s.H_out;
+  C.W_out = s.W_out;
+  C.stride_h = s.stride_h;
+  C.stride_w = s.stride_w;
+  C.pad_h = s.pad_h;
+  C.pad_w = s.pad_w;
+  C.ws = ws;
+  C.bias = bias;
+  C.rq = make_rq(input_scale, output_scale, ozp);
+  C.out = out;
+  C.acc_out = acc_out;
+  return cuda_status(q8::launch_tc_conv_t(C, cs(stream)));
+}
+
+q8_status q8_conv2d_transposed(const int8_t* x, const q8_conv2d_transposed_shape* shape,
+                               double input_scale, int32_t input_zero_point,
+                               const int8_t* weight, const int32_t* weight_sums,
+                               const float* weight_scales, const float* bias,
+                               double output_scale, int32_t output_zero_point,
+                               const char* activation, int8_t* out, void* workspace,
+                               size_t workspace_bytes, q8_stream_t stream) {
+  (void)weight_sums;
+  q8_status st = check_conv_t(x, shape, weight, out);
+  if (st != Q8_OK) return st;
+  if (!weight_scales || !activation) return Q8_ERR_NULL;
+  if (!activation_none(activation)) return Q8_ERR_UNSUPPORTED;
+  if (!scale_ok(input_scale) || !scale_ok(output_scale) || !zp_ok(input_zero_point) ||
+      !zp_ok(output_zero_point))
+    return Q8_ERR_ARG;
+  return conv_t_common(x, shape, input_scale, input_zero_point, weight, weight_scales, bias,
+                       output_scale, output_zero_point, out, nullptr, workspace, workspace_bytes,
+                       stream);
+}
+
+q8_status q8_conv2d_transposed_acc32(const int8_t* x, const q8_conv2d_transposed_shape* shape,
+                                     int32_t input_zero_point, const int8_t* weight, int32_t* acc,
+                                     void* workspace, size_t workspace_bytes,
+                                     q8_stream_t stream) {
+  q8_status st = check_conv_t(x, shape, weight, acc);
+  if (st != Q8_OK) return st;
+  if (!zp_ok(input_zero_point)) return Q8_ERR_ARG;
+  return conv_t_common(x, shape, 1.0, input_zero_point, weight, nullptr, nullptr, 1.0, 0, nullptr,
+                       acc, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

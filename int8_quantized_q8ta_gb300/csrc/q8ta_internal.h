@@ -1,0 +1,75 @@
+// q8ta_internal.h -- host-side declarations shared by the library's
+// translation units (kernel launchers and the tensor-core GEMM plan).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "device_common.cuh"
+
+namespace q8 {
+
+constexpr int64_t kTileK = 64;          // bf16 elements per 128-byte swizzled row
+constexpr size_t kWorkspaceAlign = 256;
+
+inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+inline size_t align_ws(size_t v) { return (v + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign; }
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// ---- bandwidth-bound kernels (stream_kernels.cu) --------------------------
+cudaError_t launch_quantize(const float* x, int64_t numel, float inv_scale, float zp, int8_t* out,
+                            cudaStream_t s);
+cudaError_t launch_dequantize(const int8_t* q, int64_t numel, float scale, float zp, float* out,
+                              cudaStream_t s);
+cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w, int64_t N,
+                        const float* ws, const float* bias, Requant rq, int8_t* out,
+                        cudaStream_t s);
+// dst[r, k] = bf16(src[r*ld + k] - zp) for k < K, 0 for K <= k < Kp.
+cudaError_t launch_rows_to_bf16(const int8_t* src, int64_t rows, int64_t K, int64_t ld, int32_t zp,
+                                __nv_bfloat16* dst, int64_t Kp, cudaStream_t s);
+// Fused quantize of fp32 rows: q = quantize(x) (written to xq when non-null)
+// and dst[r, k] = bf16(q - zp), zero-padded to Kp.
+cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, float inv_scale,
+                                      int32_t zp, int8_t* xq, __nv_bfloat16* dst, int64_t Kp,
+                                      cudaStream_t s);
+// dst[n, h, w, c] = bf16(x[n, c, h, w] - zp) for c < C, 0 for C <= c < Cp.
+cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t C, int64_t H, int64_t W,
+                                     int32_t zp, __nv_bfloat16* dst, int64_t Cp, cudaStream_t s);
+// dst[oc, t*ICp + ic] = bf16(w[oc*ldw + t*IC + ic]) for ic < IC, else 0.
+cudaError_t launch_convt_weight_bf16(const int8_t* w, int64_t OC, int64_t taps, int64_t IC,
+                                     int64_t ldw, __nv_bfloat16* dst, int64_t ICp, cudaStream_t s);
+
+// ---- tensor-core GEMM (tc_gemm.cu) -----------------------------------------
+struct TcLinear {
+  const __nv_bfloat16* a;  // [M, Kp] bf16, values x - input_zero_point
+  const __nv_bfloat16* b;  // [N, Kp] bf16, weight values
+  int64_t M, N, Kp;
+  const float* ws;
+  const float* bias;
+  Requant rq;
+  int8_t* out;       // [M, N] (or null when acc_out is set)
+  int32_t* acc_out;  // [M, N] int32 debug output, or null
+};
+cudaError_t launch_tc_linear(const TcLinear& p, cudaStream_t s);
+
+struct TcConvT {
+  const __nv_bfloat16* a;  // [N, H_in, W_in, ICp] bf16, values x - input_zero_point
+  const __nv_bfloat16* b;  // [OC, Kh*Kw*ICp] bf16
+  int64_t N, ICp, H_in, W_in, OC, Kh, Kw, H_out, W_out;
+  int64_t stride_h, stride_w, pad_h, pad_w;
+  const float* ws;
+  const float* bias;
+  Requant rq;
+  int8_t* out;       // [N, OC, H_out, W_out]
+  int32_t* acc_out;  // int32 debug output, or null
+};
+cudaError_t launch_tc_conv_t(const TcConvT& p, cudaStream_t s);
+
+// Device error word (written by kernels whose pipeline waits time out).
+cudaError_t read_device_error(uint32_t* code, bool clear);
+
+}  // namespace q8

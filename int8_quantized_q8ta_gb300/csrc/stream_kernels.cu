@@ -1,0 +1,450 @@
+// stream_kernels.cu -- the HBM-bandwidth-bound q8ta kernels for sm_103a:
+// quantize_per_tensor, dequantize_per_tensor, the M == 1 q8ta_linear_gemv,
+// and the int8 -> bf16 operand preparation for the tensor-core GEMM.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "q8ta_internal.h"
+
+namespace q8 {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static int stream_grid(int64_t work_items, int threads, int blocks_per_sm) {
+  int64_t want = (work_items + threads - 1) / threads;
+  int64_t cap = static_cast<int64_t>(device_sm_count()) * blocks_per_sm;
+  return static_cast<int>(std::max<int64_t>(1, std::min(want, cap)));
+}
+
+// ---------------------------------------------------------------------------
+// quantize_per_tensor ("Add quantize_per_tensor op", Solution paragraph):
+// q = clamp(rint(x * inv_scale) + zp, -128, 127).
+// Vector path: one float4 in, one packed 32-bit word out per item; U items
+// per thread per round are loaded before any is converted.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int8_t quantize_one(float x, float inv, float zp) {
+  return round_add_clamp(__fmul_rn(x, inv), zp);
+}
+
+template <int U>
+__global__ void __launch_bounds__(256) quantize_vec_kernel(const float4* __restrict__ x, int64_t n4,
+                                                           float inv, float zp,
+                                                           uint32_t* __restrict__ out) {
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * U;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * U + threadIdx.x; base < n4;
+       base += step) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = base + static_cast<int64_t>(u) * blockDim.x;
+      if (i < n4) v[u] = __ldcs(x + i);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = base + static_cast<int64_t>(u) * blockDim.x;
+      if (i < n4)
+        __stcs(out + i, pack4(quantize_one(v[u].x, inv, zp), quantize_one(v[u].y, inv, zp),
+                              quantize_one(v[u].z, inv, zp), quantize_one(v[u].w, inv, zp)));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) quantize_scalar_kernel(const float* __restrict__ x, int64_t n,
+                                                              float inv, float zp,
+                                                              int8_t* __restrict__ out) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[i] = quantize_one(x[i], inv, zp);
+}
+
+cudaError_t launch_quantize(const float* x, int64_t numel, float inv, float zp, int8_t* out,
+                            cudaStream_t s) {
+  if (numel == 0) return cudaSuccess;
+  const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(out) % 4 == 0) && (numel % 4 == 0);
+  if (vec) {
+    constexpr int U = 4;
+    const int64_t n4 = numel / 4;
+    const int grid = stream_grid((n4 + U - 1) / U, 256, 8);
+    quantize_vec_kernel<U><<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(x), n4, inv, zp,
+                                                reinterpret_cast<uint32_t*>(out));
+  } else {
+    quantize_scalar_kernel<<<stream_grid(numel, 256, 8), 256, 0, s>>>(x, numel, inv, zp, out);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// dequantize_per_tensor: y = ((float)q - (float)zp) * scale.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dequantize_kernel(const int8_t* __restrict__ q, int64_t n,
+                                                         float scale, float zp,
+                                                         float* __restrict__ out) {
+  const bool vec = (reinterpret_cast<uintptr_t>(q) % 4 == 0) &&
+                   (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  if (vec) {
+    const int64_t n4 = n / 4;
+    const uint32_t* q4 = reinterpret_cast<const uint32_t*>(q);
+    float4* o4 = reinterpret_cast<float4*>(out);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += stride) {
+      const uint32_t w = __ldcs(q4 + i);
+      float4 r;
+      r.x = __fmul_rn(__fsub_rn(static_cast<float>(static_cast<int8_t>(w & 0xff)), zp), scale);
+      r.y = __fmul_rn(__fsub_rn(static_cast<float>(static_cast<int8_t>((w >> 8) & 0xff)), zp),
+                      scale);
+      r.z = __fmul_rn(__fsub_rn(static_cast<float>(static_cast<int8_t>((w >> 16) & 0xff)), zp),
+                      scale);
+      r.w = __fmul_rn(__fsub_rn(static_cast<float>(static_cast<int8_t>(w >> 24)), zp), scale);
+      __stcs(o4 + i, r);
+    }
+    for (int64_t i = n4 * 4 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += stride)
+      out[i] = __fmul_rn(__fsub_rn(static_cast<float>(q[i]), zp), scale);
+  } else {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += stride)
+      out[i] = __fmul_rn(__fsub_rn(static_cast<float>(q[i]), zp), scale);
+  }
+}
+
+cudaError_t launch_dequantize(const int8_t* q, int64_t numel, float scale, float zp, float* out,
+                              cudaStream_t s) {
+  if (numel == 0) return cudaSuccess;
+  dequantize_kernel<<<stream_grid(numel / 4 + 1, 256, 8), 256, 0, s>>>(q, numel, scale, zp, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// q8ta_linear_gemv (M == 1): "Add q8ta_linear op", Solution paragraph, with
+// the zero point folded as sum x*w - zp * sum w (Constraints paragraph);
+// both sums are exact int32 dp4a dot products, so the fold is exact modulo
+// 2^32 like the accumulator itself.
+// One warp per output row; each lane keeps UNR 16-byte weight loads in
+// flight; a block's 4 warps produce 4 consecutive outputs = one 32-bit word.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void dp4a_acc(uint32_t w, uint32_t x, int& dot, int& wsum) {
+  dot = __dp4a(static_cast<int>(w), static_cast<int>(x), dot);
+  wsum = __dp4a(static_cast<int>(w), 0x01010101, wsum);
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(128) gemv_kernel(const int8_t* __restrict__ x, int K, int32_t izp,
+                                                   const int8_t* __restrict__ w, int N,
+                                                   const float* __restrict__ ws,
+                                                   const float* __restrict__ bias, Requant rq,
+                                                   int8_t* __restrict__ out) {
+  __shared__ int8_t res[4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 4 + warp;
+  int dot = 0, wsum = 0;
+  if (n < N) {
+    const int8_t* wr = w + static_cast<int64_t>(n) * K;
+    if constexpr (VEC == 16) {
+      constexpr int UNR = 8;
+      const int nv = K / 16;
+      const int4* w4 = reinterpret_cast<const int4*>(wr);
+      const int4* x4 = reinterpret_cast<const int4*>(x);
+      int i = lane;
+      for (; i + 32 * (UNR - 1) < nv; i += 32 * UNR) {
+        int4 wv[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) wv[u] = __ldcs(w4 + i + 32 * u);
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int4 xv = __ldg(x4 + i + 32 * u);
+          dp4a_acc(wv[u].x, xv.x, dot, wsum);
+          dp4a_acc(wv[u].y, xv.y, dot, wsum);
+          dp4a_acc(wv[u].z, xv.z, dot, wsum);
+          dp4a_acc(wv[u].w, xv.w, dot, wsum);
+        }
+      }
+      for (; i < nv; i += 32) {
+        const int4 wv = __ldcs(w4 + i), xv = __ldg(x4 + i);
+        dp4a_acc(wv.x, xv.x, dot, wsum);
+        dp4a_acc(wv.y, xv.y, dot, wsum);
+        dp4a_acc(wv.z, xv.z, dot, wsum);
+        dp4a_acc(wv.w, xv.w, dot, wsum);
+      }
+      // K % 16 tail in 4-byte words (K % 4 == 0 is a guard of the op)
+      const uint32_t* w1 = reinterpret_cast<const uint32_t*>(wr);
+      const uint32_t* x1 = reinterpret_cast<const uint32_t*>(x);
+      for (int j = nv * 4 + lane; j < K / 4; j += 32) dp4a_acc(__ldcs(w1 + j), __ldg(x1 + j), dot, wsum);
+    } else if constexpr (VEC == 4) {
+      const uint32_t* w1 = reinterpret_cast<const uint32_t*>(wr);
+      const uint32_t* x1 = reinterpret_cast<const uint32_t*>(x);
+      for (int j = lane; j < K / 4; j += 32) dp4a_acc(__ldcs(w1 + j), __ldg(x1 + j), dot, wsum);
+    } else {
+      for (int k = lane; k < K; k += 32) {
+        const int wv = wr[k];
+        dot = static_cast<int>(static_cast<uint32_t>(dot) +
+                               static_cast<uint32_t>(wv * static_cast<int>(x[k])));
+        wsum += wv;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      // modulo-2^32 sums, like the int32 accumulator they form
+      dot = static_cast<int>(static_cast<uint32_t>(dot) +
+                             static_cast<uint32_t>(__shfl_xor_sync(0xffffffffu, dot, o)));
+      wsum = static_cast<int>(static_cast<uint32_t>(wsum) +
+                              static_cast<uint32_t>(__shfl_xor_sync(0xffffffffu, wsum, o)));
+    }
+    if (lane == 0) {
+      const int32_t acc = static_cast<int32_t>(static_cast<uint32_t>(dot) -
+                                               static_cast<uint32_t>(izp) * static_cast<uint32_t>(wsum));
+      res[warp] = requant_one(acc, ws[n], bias ? bias[n] : 0.0f, rq);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int n0 = blockIdx.x * 4;
+    if (n0 + 3 < N && reinterpret_cast<uintptr_t>(out + n0) % 4 == 0) {
+      *reinterpret_cast<uint32_t*>(out + n0) = pack4(res[0], res[1], res[2], res[3]);
+    } else {
+      for (int j = 0; j < 4 && n0 + j < N; ++j) out[n0 + j] = res[j];
+    }
+  }
+}
+
+cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w, int64_t N,
+                        const float* ws, const float* bias, Requant rq, int8_t* out,
+                        cudaStream_t s) {
+  const int grid = static_cast<int>((N + 3) / 4);
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(w);
+  // 16-byte loads need every row start 16-byte aligned, hence K % 16 == 0.
+  if (xa % 16 == 0 && wa % 16 == 0 && K % 16 == 0)
+    gemv_kernel<16><<<grid, 128, 0, s>>>(x, (int)K, izp, w, (int)N, ws, bias, rq, out);
+  else if (xa % 4 == 0 && wa % 4 == 0 && K % 4 == 0)
+    gemv_kernel<4><<<grid, 128, 0, s>>>(x, (int)K, izp, w, (int)N, ws, bias, rq, out);
+  else
+    gemv_kernel<1><<<grid, 128, 0, s>>>(x, (int)K, izp, w, (int)N, ws, bias, rq, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Operand preparation for the tensor-core GEMM.  int8 values, and the
+// differences x - zp in [-255, 255], are exact in bf16 (8 significant bits).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t bf16x2_from_ints(int lo, int hi) {
+  const __nv_bfloat16 a = __float2bfloat16_rn(static_cast<float>(lo));
+  const __nv_bfloat16 b = __float2bfloat16_rn(static_cast<float>(hi));
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+// One thread writes 8 consecutive bf16 (16 bytes) of a destination row.
+__global__ void __launch_bounds__(256) rows_to_bf16_kernel(const int8_t* __restrict__ src,
+                                                           int64_t rows, int64_t K, int64_t ld,
+                                                           int32_t zp, uint4* __restrict__ dst,
+                                                           int64_t Kp) {
+  const int64_t per_row = Kp / 8;
+  const int64_t total = rows * per_row;
+  const bool vec8 = (K % 8 == 0) && (ld % 8 == 0) && (reinterpret_cast<uintptr_t>(src) % 8 == 0);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / per_row;
+    const int64_t k0 = (i - r * per_row) * 8;
+    const int8_t* sp = src + r * ld + k0;
+    int v[8];
+    if (vec8 && k0 + 8 <= K) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(sp);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[j] = static_cast<int8_t>((raw.x >> (8 * j)) & 0xff) - zp;
+        v[4 + j] = static_cast<int8_t>((raw.y >> (8 * j)) & 0xff) - zp;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = (k0 + j < K) ? static_cast<int>(sp[j]) - zp : 0;
+    }
+    uint4 o;
+    o.x = bf16x2_from_ints(v[0], v[1]);
+    o.y = bf16x2_from_ints(v[2], v[3]);
+    o.z = bf16x2_from_ints(v[4], v[5]);
+    o.w = bf16x2_from_ints(v[6], v[7]);
+    dst[i] = o;
+  }
+}
+
+cudaError_t launch_rows_to_bf16(const int8_t* src, int64_t rows, int64_t K, int64_t ld, int32_t zp,
+                                __nv_bfloat16* dst, int64_t Kp, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t items = rows * (Kp / 8);
+  rows_to_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
+      src, rows, K, ld, zp, reinterpret_cast<uint4*>(dst), Kp);
+  return cudaGetLastError();
+}
+
+// Fused quantize of fp32 rows into the GEMM operand (and the int8 op output).
+__global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
+    const float* __restrict__ x, int64_t rows, int64_t K, float inv, int32_t zp,
+    int8_t* __restrict__ xq, uint4* __restrict__ dst, int64_t Kp) {
+  const int64_t per_row = Kp / 8;
+  const int64_t total = rows * per_row;
+  const float zpf = static_cast<float>(zp);
+  const bool vec = (K % 8 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+                   (xq == nullptr || reinterpret_cast<uintptr_t>(xq) % 8 == 0);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / per_row;
+    const int64_t k0 = (i - r * per_row) * 8;
+    int8_t q[8];
+    int v[8];
+    if (vec && k0 + 8 <= K) {
+      const float4* xp = reinterpret_cast<const float4*>(x + r * K + k0);
+      const float4 a = __ldcs(xp), b = __ldcs(xp + 1);
+      q[0] = quantize_one(a.x, inv, zpf); q[1] = quantize_one(a.y, inv, zpf);
+      q[2] = quantize_one(a.z, inv, zpf); q[3] = quantize_one(a.w, inv, zpf);
+      q[4] = quantize_one(b.x, inv, zpf); q[5] = quantize_one(b.y, inv, zpf);
+      q[6] = quantize_one(b.z, inv, zpf); q[7] = quantize_one(b.w, inv, zpf);
+      if (xq) {
+        uint2 o;
+        o.x = pack4(q[0], q[1], q[2], q[3]);
+        o.y = pack4(q[4], q[5], q[6], q[7]);
+        *reinterpret_cast<uint2*>(xq + r * K + k0) = o;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = static_cast<int>(q[j]) - zp;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (k0 + j < K) {
+          q[j] = quantize_one(x[r * K + k0 + j], inv, zpf);
+          if (xq) xq[r * K + k0 + j] = q[j];
+          v[j] = static_cast<int>(q[j]) - zp;
+        } else {
+          v[j] = 0;
+        }
+      }
+    }
+    uint4 o;
+    o.x = bf16x2_from_ints(v[0], v[1]);
+    o.y = bf16x2_from_ints(v[2], v[3]);
+    o.z = bf16x2_from_ints(v[4], v[5]);
+    o.w = bf16x2_from_ints(v[6], v[7]);
+    dst[i] = o;
+  }
+}
+
+cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, float inv, int32_t zp,
+                                      int8_t* xq, __nv_bfloat16* dst, int64_t Kp, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t items = rows * (Kp / 8);
+  quantize_rows_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
+      x, rows, K, inv, zp, xq, reinterpret_cast<uint4*>(dst), Kp);
+  return cudaGetLastError();
+}
+
+// NCHW int8 -> NHWC bf16 (x - zp), channels zero-padded to Cp (padding
+// channels are exactly 0, not -zp).  A block transposes a 64-channel x
+// 64-column slab of one (n, h) row through shared memory: 16-byte loads
+// along w, 16-byte stores along c.
+__global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __restrict__ x,
+                                                                int64_t NH, int64_t C, int64_t H,
+                                                                int64_t W, int32_t zp,
+                                                                uint4* __restrict__ dst,
+                                                                int64_t Cp) {
+  __shared__ __align__(16) int8_t tile[64][72];  // [w][c]
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 64;
+  const int64_t w0 = static_cast<int64_t>(blockIdx.x) * 64;
+  const bool vec = (W % 16 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
+  const int lc = threadIdx.x >> 2, wseg = threadIdx.x & 3;
+  for (int64_t nh = blockIdx.z; nh < NH; nh += gridDim.z) {  // nh = n * H + h
+    const int64_t n = nh / H, h = nh - n * H;
+    int8_t v[16];
+    const int64_t c = c0 + lc;
+    const int64_t wb = w0 + 16 * wseg;
+    if (c < C && vec && wb + 16 <= W) {
+      const int4 raw = __ldcs(reinterpret_cast<const int4*>(x + ((n * C + c) * H + h) * W + wb));
+      const int32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = static_cast<int8_t>((r[i >> 2] >> (8 * (i & 3))) & 0xff);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[i] = (c < C && wb + i < W) ? x[((n * C + c) * H + h) * W + wb + i] : 0;
+    }
+    __syncthreads();  // the previous row's readers are done with the tile
+#pragma unroll
+    for (int i = 0; i < 16; ++i) tile[16 * wseg + i][lc] = v[i];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int item = threadIdx.x + 256 * k;
+      const int w = item >> 3, cseg = item & 7;
+      const int64_t cc = c0 + 8 * cseg;
+      if (w0 + w < W && cc < Cp) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(&tile[w][8 * cseg]);
+        int d[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          d[j] = (cc + j < C) ? static_cast<int8_t>((raw.x >> (8 * j)) & 0xff) - zp : 0;
+          d[4 + j] = (cc + 4 + j < C) ? static_cast<int8_t>((raw.y >> (8 * j)) & 0xff) - zp : 0;
+        }
+        uint4 o;
+        o.x = bf16x2_from_ints(d[0], d[1]);
+        o.y = bf16x2_from_ints(d[2], d[3]);
+        o.z = bf16x2_from_ints(d[4], d[5]);
+        o.w = bf16x2_from_ints(d[6], d[7]);
+        dst[(((n * H + h) * W + w0 + w) * Cp + cc) / 8] = o;
+      }
+    }
+  }
+}
+
+cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t C, int64_t H, int64_t W,
+                                     int32_t zp, __nv_bfloat16* dst, int64_t Cp, cudaStream_t s) {
+  if (N * H * W == 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>((W + 63) / 64), static_cast<unsigned>(Cp / 64),
+            static_cast<unsigned>(std::min<int64_t>(N * H, 65535)));
+  nchw_to_nhwc_bf16_kernel<<<grid, 256, 0, s>>>(x, N * H, C, H, W, zp,
+                                                reinterpret_cast<uint4*>(dst), Cp);
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(256) convt_weight_bf16_kernel(const int8_t* __restrict__ w,
+                                                                int64_t OC, int64_t taps,
+                                                                int64_t IC, int64_t ldw,
+                                                                uint32_t* __restrict__ dst,
+                                                                int64_t ICp) {
+  const int64_t cols = taps * ICp;
+  const int64_t total = OC * cols / 2;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t oc = (2 * i) / cols;
+    const int64_t col = 2 * i - oc * cols;
+    const int64_t t = col / ICp, ic = col - t * ICp;
+    const int a = (ic < IC) ? w[oc * ldw + t * IC + ic] : 0;
+    const int b = (ic + 1 < IC) ? w[oc * ldw + t * IC + ic + 1] : 0;
+    dst[i] = bf16x2_from_ints(a, b);
+  }
+}
+
+cudaError_t launch_convt_weight_bf16(const int8_t* w, int64_t OC, int64_t taps, int64_t IC,
+                                     int64_t ldw, __nv_bfloat16* dst, int64_t ICp, cudaStream_t s) {
+  const int64_t items = OC * taps * ICp / 2;
+  if (items == 0) return cudaSuccess;
+  convt_weight_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
+      w, OC, taps, IC, ldw, reinterpret_cast<uint32_t*>(dst), ICp);
+  return cudaGetLastError();
+}
+
+}  // namespace q8

@@ -1,0 +1,143 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library loads, exports every function include/q8ta.h declares, and its
+argument guards -- which run on the host before anything is enqueued --
+return the documented status codes.  No call here reaches a kernel launch:
+each passes an argument that a guard rejects first.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q8ta.h")
+
+q8 = pytest.importorskip("int8_quantized_q8ta_gb300")
+lib = q8.lib()
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: a guard fails first
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(q8.EXPORTS) == names
+
+
+def test_status_strings_and_version():
+    assert lib.q8_version() == 1
+    for s in range(9):
+        assert lib.q8_status_string(s).startswith(b"Q8_")
+    assert lib.q8_status_string(99) == b"unknown q8_status"
+
+
+def test_quantize_guards():
+    f = lib.q8_quantize_per_tensor
+    assert f(None, 4, 0.1, 0, FAKE, None) == q8.Q8_ERR_NULL
+    assert f(FAKE, 4, 0.1, 0, None, None) == q8.Q8_ERR_NULL
+    assert f(FAKE, 6, 0.1, 0, FAKE, None) == q8.Q8_ERR_SHAPE        # numel % 4
+    assert f(FAKE, -4, 0.1, 0, FAKE, None) == q8.Q8_ERR_SHAPE
+    assert f(FAKE, 4, 0.0, 0, FAKE, None) == q8.Q8_ERR_ARG
+    assert f(FAKE, 4, float("inf"), 0, FAKE, None) == q8.Q8_ERR_ARG
+    assert f(FAKE, 4, 0.1, 128, FAKE, None) == q8.Q8_ERR_ARG
+    assert lib.q8_dequantize_per_tensor(FAKE, 5, 0.1, 0, FAKE, None) == q8.Q8_ERR_SHAPE
+
+
+def _lin(fn, M=8, K=64, N=32, act=b"none", izp=0, ozp=0, s_in=0.02, s_out=0.05, ws=FAKE,
+         out=FAKE, workspace=None, wbytes=0):
+    return fn(FAKE, M, K, s_in, izp, FAKE, N, None, ws, None, s_out, ozp, act, out, workspace,
+              wbytes, None)
+
+
+@pytest.mark.parametrize("name", ["q8_linear", "q8_linear_gemv"])
+def test_linear_guards(name):
+    f = getattr(lib, name)
+    M = 1
+    assert _lin(f, M=M, N=30) == q8.Q8_ERR_SHAPE                    # N % 4
+    assert _lin(f, M=M, K=63) == q8.Q8_ERR_SHAPE                    # M*K % 4 with M = 1
+    assert _lin(f, M=M, act=b"relu") == q8.Q8_ERR_UNSUPPORTED
+    assert _lin(f, M=M, act=None) == q8.Q8_ERR_NULL
+    assert _lin(f, M=M, ws=None) == q8.Q8_ERR_NULL
+    assert _lin(f, M=M, out=None) == q8.Q8_ERR_NULL
+    assert _lin(f, M=M, izp=-129) == q8.Q8_ERR_ARG
+    assert _lin(f, M=M, s_out=-1.0) == q8.Q8_ERR_ARG
+    assert _lin(f, M=0) == q8.Q8_ERR_SHAPE
+
+
+def test_linear_workspace_and_gemv_shape_guards():
+    assert _lin(lib.q8_linear_gemv, M=2) == q8.Q8_ERR_SHAPE
+    assert _lin(lib.q8_linear, M=8) == q8.Q8_ERR_WORKSPACE
+    need = lib.q8_linear_workspace_bytes(8, 64, 32)
+    assert need > 0 and need % 256 == 0
+    assert _lin(lib.q8_linear, M=8, workspace=FAKE, wbytes=need - 1) == q8.Q8_ERR_WORKSPACE
+    assert _lin(lib.q8_linear, M=8, workspace=ctypes.c_void_p(0x10010), wbytes=need) == \
+        q8.Q8_ERR_ALIGN
+    assert lib.q8_linear_workspace_bytes(1, 4096, 4096) == 0
+
+
+def test_workspace_sizes():
+    # bf16 copies padded to a multiple of 64 along K, 256-byte aligned
+    assert lib.q8_linear_packed_weight_bytes(11008, 4096) == 11008 * 4096 * 2
+    assert lib.q8_linear_operand_bytes(2048, 4096) == 2048 * 4096 * 2
+    assert lib.q8_linear_packed_weight_bytes(4, 70) == (4 * 128 * 2 + 255) // 256 * 256
+    s = q8.conv_t_shape((8, 256, 64, 64), (128, 2304), 3, 3, 128, 128, 2, 1, 1)
+    assert lib.q8_conv2d_transposed_workspace_bytes(ctypes.byref(s)) == \
+        8 * 64 * 64 * 256 * 2 + 128 * 9 * 256 * 2
+
+
+def test_operand_guards():
+    assert lib.q8_linear_prepare_operand(None, 8, 64, 0, FAKE, 1 << 20, None) == q8.Q8_ERR_NULL
+    assert lib.q8_linear_prepare_operand(FAKE, 1, 3, 0, FAKE, 1 << 20, None) == q8.Q8_ERR_SHAPE
+    assert lib.q8_linear_prepare_operand(FAKE, 8, 64, 0, FAKE, 10, None) == q8.Q8_ERR_WORKSPACE
+    assert lib.q8_linear_prepare_operand(FAKE, 8, 64, 0, ctypes.c_void_p(0x10008), 1 << 20,
+                                         None) == q8.Q8_ERR_ALIGN
+    assert lib.q8_quantize_to_linear_operand(FAKE, 8, 64, 0.0, 0, None, FAKE, 1 << 20,
+                                             None) == q8.Q8_ERR_ARG
+    assert lib.q8_linear_operand_packed(FAKE, 8, 64, 0.02, FAKE, 30, FAKE, None, 0.1, 0, b"none",
+                                        FAKE, None) == q8.Q8_ERR_SHAPE
+    assert lib.q8_linear_operand_packed(FAKE, 8, 64, 0.02, FAKE, 32, FAKE, None, 0.1, 0, b"relu",
+                                        FAKE, None) == q8.Q8_ERR_UNSUPPORTED
+
+
+def _conv(**kw):
+    base = dict(x_shape=(1, 3, 5, 4), w_shape=(4, 27), Kh=3, Kw=3, H_out=10, W_out=8, stride=2,
+                padding=1, output_padding=1, dilation=1, groups=1)
+    base.update(kw)
+    s = q8.conv_t_shape(base["x_shape"], base["w_shape"], base["Kh"], base["Kw"], base["H_out"],
+                        base["W_out"], base["stride"], base["padding"], base["output_padding"],
+                        base["dilation"], base["groups"])
+    act = kw.get("act", b"none")
+    return lib.q8_conv2d_transposed(FAKE, ctypes.byref(s), 0.02, 0, FAKE, None, FAKE, None, 0.1,
+                                    0, act, FAKE, None, 0, None)
+
+
+def test_conv_t_guards():
+    assert _conv(groups=2) == q8.Q8_ERR_UNSUPPORTED
+    assert _conv(dilation=2) == q8.Q8_ERR_UNSUPPORTED
+    assert _conv(stride=0) == q8.Q8_ERR_SHAPE
+    assert _conv(W_out=9) == q8.Q8_ERR_SHAPE                       # W_out % 4
+    assert _conv(w_shape=(4, 26)) == q8.Q8_ERR_SHAPE               # row stride < Kh*Kw*IC
+    assert _conv(padding=-1) == q8.Q8_ERR_SHAPE
+    assert _conv(act=b"relu") == q8.Q8_ERR_UNSUPPORTED
+    assert _conv() == q8.Q8_ERR_WORKSPACE                          # all guards pass
+    s = q8.conv_t_shape((1, 3, 5, 4), (4, 27), 3, 3, 10, 8, 2, 1, 1)
+    assert lib.q8_conv2d_transposed(FAKE, None, 0.02, 0, FAKE, None, FAKE, None, 0.1, 0, b"none",
+                                    FAKE, None, 0, None) == q8.Q8_ERR_NULL
+    assert lib.q8_conv2d_transposed(FAKE, ctypes.byref(s), 0.02, 300, FAKE, None, FAKE, None, 0.1,
+                                    0, b"none", FAKE, None, 0, None) == q8.Q8_ERR_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError, match="CUDA"):
+        q8.quantize_per_tensor(torch.zeros(8), 0.1, 0)

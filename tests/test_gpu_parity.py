@@ -1,0 +1,254 @@
+"""GPU parity: the CUDA path against the CPU oracle, element by element.
+
+Integer results (int8 outputs, int32 accumulators) must be bit-exact.  Sizes
+span several tiles with ragged tails; the five benchmark workloads run at
+full size on the GPU, compared in full where the oracle is fast and on
+sampled rows / images / channels where it is not.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+q8 = pytest.importorskip("int8_quantized_q8ta_gb300")
+DEV = torch.device("cuda:0")
+
+
+def T(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def H(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    yield
+    assert q8.device_error(clear=True) == 0
+
+
+# --------------------------------------------------------------- quantize
+
+@pytest.mark.parametrize("n", [4, 12, 16, 1000, 4096 + 4, (1 << 20) + 12])
+@pytest.mark.parametrize("scale,zp,var", [(0.03, -5, 3.0), (0.02, 3, 1.0), (1.0, 0, 4e4)])
+def test_quantize_matches_oracle(n, scale, zp, var):
+    x = synth.normal(n, "gq", (n,), 0.0, var)
+    got = H(q8.quantize_per_tensor(T(x), scale, zp))
+    np.testing.assert_array_equal(got, oracle.quantize_per_tensor(x, scale, zp))
+
+
+def test_quantize_special_values_and_unaligned_view():
+    x = np.array([0.5, 1.5, 2.5, -0.5, -2.5, np.inf, -np.inf, 1e30, -1e30, 127.5, -128.5, 0.0],
+                 np.float32)
+    np.testing.assert_array_equal(H(q8.quantize_per_tensor(T(x), 1.0, 0)),
+                                  oracle.quantize_per_tensor(x, 1.0, 0))
+    # a view starting 4 bytes into an allocation takes the scalar path
+    base = synth.normal(7, "gu", (4101,), 0.0, 3.0)
+    xt = T(base)[1:]
+    assert xt.data_ptr() % 16 != 0
+    got = H(q8.quantize_per_tensor(xt, 0.03, -5))
+    np.testing.assert_array_equal(got, oracle.quantize_per_tensor(base[1:], 0.03, -5))
+
+
+def test_quantize_64Mi_full():
+    wl = synth.CONFIGS["quantize_64Mi"]
+    p = wl.params
+    x = synth.normal(wl.seed, "x", (wl.dims["numel"],), p["x_mean"], p["x_var"])
+    got = H(q8.quantize_per_tensor(T(x), p["in_scale"], p["in_zp"]))
+    ref = oracle.quantize_per_tensor(x, p["in_scale"], p["in_zp"])
+    np.testing.assert_array_equal(got, ref)
+    sat = np.count_nonzero((ref == 127) | (ref == -128)) / ref.size
+    assert 0.01 < sat < 0.05          # "~2% saturating"
+
+
+def test_dequantize_matches_oracle():
+    q = synth.int8_uniform(3, "dq", (4096 + 8,), -128, 127)
+    got = H(q8.dequantize_per_tensor(T(q), 0.037, -3))
+    np.testing.assert_array_equal(got.view(np.uint32),
+                                  oracle.dequantize_per_tensor(q, 0.037, -3).view(np.uint32))
+
+
+# --------------------------------------------------------------- gemv
+
+def test_gemv_1x4096x4096_full():
+    wl = synth.CONFIGS["gemv_1x4096x4096"]
+    d, p = wl.dims, wl.params
+    x, w, ws, b = synth.linear_inputs(wl.seed, 1, d["K"], d["N"], x_kind="int8", p=p)
+    got = H(q8.linear_gemv(T(x), p["in_scale"], p["in_zp"], T(w), None, T(ws), T(b),
+                           p["out_scale"], p["out_zp"]))
+    ref = oracle.linear(x, p["in_scale"], p["in_zp"], w, ws, b, p["out_scale"], p["out_zp"])
+    np.testing.assert_array_equal(got, ref)
+    # the same through q8_linear, which dispatches M == 1 to the gemv kernel
+    got2 = H(q8.linear(T(x), p["in_scale"], p["in_zp"], T(w), None, T(ws), T(b), p["out_scale"],
+                       p["out_zp"]))
+    np.testing.assert_array_equal(got2, ref)
+
+
+@pytest.mark.parametrize("K,N,izp", [(4, 4, 0), (20, 8, -128), (64, 36, 127), (100, 12, 5),
+                                     (4096 + 16, 8, -7), (1028, 40, 3)])
+def test_gemv_ragged(K, N, izp):
+    p = dict(ws_lo=0.002, ws_hi=0.01, b_mean=0.0, b_var=0.1)
+    x, w, ws, b = synth.linear_inputs(K + N, 1, K, N, x_kind="int8", p=p)
+    got = H(q8.linear_gemv(T(x), 0.02, izp, T(w), None, T(ws), T(b), 0.07, -2))
+    np.testing.assert_array_equal(got, oracle.linear(x, 0.02, izp, w, ws, b, 0.07, -2))
+    got_nb = H(q8.linear_gemv(T(x), 0.02, izp, T(w), None, T(ws), None, 0.07, -2))
+    np.testing.assert_array_equal(got_nb, oracle.linear(x, 0.02, izp, w, ws, None, 0.07, -2))
+
+
+# --------------------------------------------------------------- linear
+
+LINEAR_SHAPES = [(2, 4, 4, 0), (8, 64, 32, 3), (130, 200, 36, -128), (257, 520, 260, 127),
+                 (129, 1040, 516, -5), (300, 4096, 136, 1), (64, 1536, 64, -100)]
+
+
+@pytest.mark.parametrize("M,K,N,izp", LINEAR_SHAPES)
+def test_linear_matches_oracle(M, K, N, izp):
+    p = dict(ws_lo=0.001, ws_hi=0.005, b_mean=0.0, b_var=0.1)
+    x, w, ws, b = synth.linear_inputs(M * 3 + K + N, M, K, N, x_kind="int8", p=p)
+    ref_acc = oracle.linear_acc(x, izp, w)
+    ref = oracle.linear(x, 0.03, izp, w, ws, b, 0.1, 1)
+    got = H(q8.linear(T(x), 0.03, izp, T(w), None, T(ws), T(b), 0.1, 1))
+    np.testing.assert_array_equal(got, ref)
+    packed = q8.pack_weight(T(w))
+    np.testing.assert_array_equal(H(q8.linear_packed(T(x), 0.03, izp, packed, T(ws), T(b), 0.1,
+                                                     1)), ref)
+    np.testing.assert_array_equal(H(q8.linear_packed_acc32(T(x), izp, packed)), ref_acc)
+    operand = q8.prepare_operand(T(x), izp)
+    np.testing.assert_array_equal(H(q8.linear_operand_packed(operand, 0.03, packed, T(ws), T(b),
+                                                             0.1, 1)), ref)
+
+
+def test_linear_chain_8x64x32():
+    wl = synth.CONFIGS["linear_chain_8x64x32"]
+    d, p = wl.dims, wl.params
+    x, w, ws, b = synth.linear_inputs(wl.seed, d["M"], d["K"], d["N"], x_kind="fp32", p=p)
+    xq_ref = oracle.quantize_per_tensor(x, p["in_scale"], p["in_zp"])
+    ref = oracle.linear(xq_ref, p["in_scale"], p["in_zp"], w, ws, b, p["out_scale"], p["out_zp"])
+    xq = q8.quantize_per_tensor(T(x), p["in_scale"], p["in_zp"])
+    got = q8.linear(xq, p["in_scale"], p["in_zp"], T(w), None, T(ws), T(b), p["out_scale"],
+                    p["out_zp"])
+    np.testing.assert_array_equal(H(xq), xq_ref)
+    np.testing.assert_array_equal(H(got), ref)
+    packed = q8.pack_weight(T(w))
+    fxq, fout = q8.quantize_linear_packed(T(x), p["in_scale"], p["in_zp"], packed, T(ws), T(b),
+                                          p["out_scale"], p["out_zp"])
+    np.testing.assert_array_equal(H(fxq), xq_ref)
+    np.testing.assert_array_equal(H(fout), ref)
+
+
+def test_linear_chain_2048x4096x11008_sampled():
+    """Full-size prefill chain on the GPU (the launch configuration the
+    benchmark times); the oracle checks sampled rows spread over every
+    M tile, including the first and last rows."""
+    wl = synth.CONFIGS["linear_chain_2048x4096x11008"]
+    d, p = wl.dims, wl.params
+    x, w, ws, b = synth.linear_inputs(wl.seed, d["M"], d["K"], d["N"], x_kind="fp32", p=p)
+    packed = q8.pack_weight(T(w))
+    xq, out = q8.quantize_linear_packed(T(x), p["in_scale"], p["in_zp"], packed, T(ws), T(b),
+                                        p["out_scale"], p["out_zp"])
+    xq, out = H(xq), H(out)
+    xq_ref = oracle.quantize_per_tensor(x, p["in_scale"], p["in_zp"])
+    np.testing.assert_array_equal(xq, xq_ref)
+    rows = sorted(set([0, 1, 127, 128, 1023, 2046, 2047] +
+                      list(synth.uniform_int(99, "rows", (9,), 0, d["M"] - 1))))
+    ref = oracle.linear(xq_ref[rows], p["in_scale"], p["in_zp"], w, ws, b, p["out_scale"],
+                        p["out_zp"])
+    np.testing.assert_array_equal(out[rows], ref)
+
+
+def test_acc32_exact_at_the_chunk_bound():
+    """Adversarial magnitudes: |x - zp| = 255 and |w| = 128 make each
+    512-long chunk reach 512 * 32640 = 16,711,680 (just below 2^24) before it
+    is drained; mixed rows check that low-order bits survive next to it."""
+    M, K, N = 256, 4096 + 64, 256
+    x = np.full((M, K), 127, np.int8)
+    w = np.full((N, K), -128, np.int8)
+    # rows 64..127: alternate +255 / -255 operands; rows 128..: max then one small term
+    x[64:128, 1::2] = -128
+    x[128:, :] = synth.int8_uniform(1, "ax", (M - 128, K), -128, 127)
+    x[128:, ::512] = 127
+    w[64:, :] = synth.int8_uniform(2, "aw", (N - 64, K), -128, 127)
+    w[200:, :511] = -128
+    w[200:, 511] = 1
+    packed = q8.pack_weight(T(w))
+    got = H(q8.linear_packed_acc32(T(x), -128, packed))
+    np.testing.assert_array_equal(got, oracle.linear_acc(x, -128, w))
+    got = H(q8.linear_packed_acc32(T(x), 127, packed))
+    np.testing.assert_array_equal(got, oracle.linear_acc(x, 127, w))
+
+
+# --------------------------------------------------------------- conv_t
+
+def _conv_case(seed, N, IC, H_in, W_in, OC, K, s, p, op, izp, ozp, out_hw=None):
+    d = dict(N=N, IC=IC, H_in=H_in, W_in=W_in, OC=OC, Kh=K, Kw=K)
+    pp = dict(in_scale=0.02, ws_lo=0.002, ws_hi=0.01, b_mean=0.0, b_var=0.1)
+    x, w, ws, b = synth.conv_t_inputs(seed, d, pp)
+    Hn, Wn = synth.output_hw(H_in, W_in, K, K, s, s, p, p, op, op)
+    H_out, W_out = out_hw if out_hw else (Hn, Wn)
+    ref = oracle.conv2d_transposed(x, 0.02, izp, w, K, K, ws, b, 0.15, ozp, H_out, W_out, (s, s),
+                                   (p, p))
+    got = H(q8.conv2d_transposed(T(x), 0.02, izp, T(w), None, T(ws), T(b), 0.15, ozp, K,
+                                 stride=s, padding=p, output_padding=op,
+                                 output_size=(H_out, W_out)))
+    np.testing.assert_array_equal(got, ref)
+    acc_ref = oracle.conv2d_transposed_acc(x, izp, w, K, K, H_out, W_out, (s, s), (p, p))
+    acc = H(q8.conv2d_transposed_acc32(T(x), izp, T(w), K, (H_out, W_out), stride=s, padding=p))
+    np.testing.assert_array_equal(acc, acc_ref)
+
+
+CONV_SHAPES = [
+    # seed, N, IC, H, W, OC, K, s, p, op, izp, ozp, (H_out, W_out) or None
+    (1, 1, 3, 5, 4, 4, 3, 2, 1, 1, -7, 2, None),
+    (2, 2, 64, 7, 9, 36, 4, 2, 1, 0, 4, 0, (14, 16)),
+    (3, 1, 70, 6, 6, 132, 3, 1, 0, 0, -128, -3, (8, 8)),
+    (4, 1, 16, 5, 5, 8, 1, 3, 0, 2, 127, 1, (15, 16)),        # phases with no tap
+    (5, 3, 8, 4, 6, 12, 5, 2, 2, 1, 0, 0, (10, 12)),
+    (6, 1, 32, 40, 150, 16, 2, 2, 0, 0, 9, -9, (80, 300)),   # W' > 128: several w tiles
+    (7, 2, 128, 8, 8, 256, 3, 2, 1, 1, -1, 5, (16, 16)),
+    (8, 1, 8, 3, 3, 4, 3, 2, 0, 0, 2, 2, (9, 12)),           # output larger than natural
+    (9, 1, 40, 9, 10, 24, 4, 2, 1, 0, -3, 3, (24, 32)),      # staged rows, ragged row tiles
+    (10, 2, 64, 16, 16, 64, 3, 2, 1, 1, 11, -4, (32, 32)),   # staged, several images
+]
+
+
+@pytest.mark.parametrize("case", CONV_SHAPES)
+def test_conv_t_matches_oracle(case):
+    seed, N, IC, H_in, W_in, OC, K, s, p, op, izp, ozp, hw = case
+    _conv_case(seed, N, IC, H_in, W_in, OC, K, s, p, op, izp, ozp, hw)
+
+
+def _workload_conv(name):
+    wl = synth.CONFIGS[name]
+    d, p = wl.dims, wl.params
+    x, w, ws, b = synth.conv_t_inputs(wl.seed, d, p)
+    Ho, Wo = synth.output_hw(d["H_in"], d["W_in"], d["Kh"], d["Kw"], d["s"], d["s"], d["p"],
+                             d["p"], d["op"], d["op"])
+    got = H(q8.conv2d_transposed(T(x), p["in_scale"], p["in_zp"], T(w), None, T(ws), T(b),
+                                 p["out_scale"], p["out_zp"], (d["Kh"], d["Kw"]), stride=d["s"],
+                                 padding=d["p"], output_padding=d["op"]))
+    return wl, d, p, x, w, ws, b, Ho, Wo, got
+
+
+def test_conv_t_1x64x32x32_full():
+    wl, d, p, x, w, ws, b, Ho, Wo, got = _workload_conv("conv_t_1x64x32x32_k4s2")
+    assert (Ho, Wo) == (64, 64)
+    ref = oracle.conv2d_transposed(x, p["in_scale"], p["in_zp"], w, 4, 4, ws, b, p["out_scale"],
+                                   p["out_zp"], Ho, Wo, (2, 2), (1, 1))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_conv_t_8x256x64x64_sampled():
+    wl, d, p, x, w, ws, b, Ho, Wo, got = _workload_conv("conv_t_8x256x64x64_k3s2")
+    assert (Ho, Wo) == (128, 128)
+    ocs = [0, 1, 63, 64, 126, 127]
+    for n in (0, 7):
+        ref = oracle.conv2d_transposed(x[n:n + 1], p["in_scale"], p["in_zp"], w[ocs], 3, 3,
+                                       ws[ocs], b[ocs], p["out_scale"], p["out_zp"], Ho, Wo,
+                                       (2, 2), (1, 1))
+        np.testing.assert_array_equal(got[n:n + 1, ocs], ref)
