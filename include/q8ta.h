@@ -132,6 +132,34 @@ q8_status q8_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
                     double output_scale, int32_t output_zero_point, const char* activation,
                     int8_t* out, void* workspace, size_t workspace_bytes, q8_stream_t stream);
 
+/*
+ * q8_linear without any allocation or workspace: the pages have no
+ * counterpart; this entry point exists for callers that cannot allocate
+ * device memory where they run the layer (a plugin whose host runtime owns
+ * the device memory pool and forbids cudaMalloc, a latency-critical loop
+ * that cannot afford cudaMalloc/cudaFree, a deployment whose memory budget
+ * is fixed at start-up).  Same arguments, guards and results as q8_linear,
+ * minus the workspace.  The scratch is a library-owned device array of
+ * Q8_LINEAR_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU loading this
+ * library holds until the process exits; no call allocates or frees memory.
+ *   - Limit: 2*(M + N)*ceil64(K) bytes (each half rounded up to 256) must fit
+ *     the array, else Q8_ERR_WORKSPACE and nothing is launched.  M == 1 uses
+ *     no scratch (the gemv kernel) and has no such limit.
+ *   - The first call on each device looks up the array's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last
+ *     call's contents (nothing in it needs to start at zero).  Calls whose
+ *     work overlaps on the GPU (other streams, other host threads) race on
+ *     it: order them on one stream.
+ */
+#define Q8_LINEAR_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+q8_status q8_linear_noalloc(const int8_t* x, int64_t M, int64_t K, double input_scale,
+                            int32_t input_zero_point, const int8_t* weight, int64_t N,
+                            const int32_t* weight_sums, const float* weight_scales,
+                            const float* bias, double output_scale, int32_t output_zero_point,
+                            const char* activation, int8_t* out, q8_stream_t stream);
+
 /* The M == 1 case with the identical schema; returns Q8_ERR_SHAPE unless
  * M == 1.  Needs no workspace (pass NULL, 0). */
 q8_status q8_linear_gemv(const int8_t* x, int64_t M, int64_t K, double input_scale,

@@ -28,7 +28,7 @@ Q8_ERR_WORKSPACE, Q8_ERR_CUDA, Q8_ERR_DEVICE, Q8_ERR_ARG = 5, 6, 7, 8
 EXPORTS = (
     "q8_status_string", "q8_version", "q8_device_error",
     "q8_quantize_per_tensor", "q8_dequantize_per_tensor",
-    "q8_linear_workspace_bytes", "q8_linear", "q8_linear_gemv",
+    "q8_linear_workspace_bytes", "q8_linear", "q8_linear_noalloc", "q8_linear_gemv",
     "q8_linear_packed_weight_bytes", "q8_linear_pack_weight",
     "q8_linear_operand_bytes", "q8_linear_prepare_operand", "q8_quantize_to_linear_operand",
     "q8_linear_operand_packed", "q8_linear_packed", "q8_quantize_linear_packed",
@@ -72,6 +72,8 @@ def _load() -> ctypes.CDLL:
         "q8_linear": (ctypes.c_int, [P, I64, I64, D, I32, P, I64, P, P, P, D, I32, C, P, P, S, P]),
         "q8_linear_gemv": (ctypes.c_int, [P, I64, I64, D, I32, P, I64, P, P, P, D, I32, C, P, P, S,
                                           P]),
+        "q8_linear_noalloc": (ctypes.c_int, [P, I64, I64, D, I32, P, I64, P, P, P, D, I32, C, P,
+                                             P]),
         "q8_linear_packed_weight_bytes": (S, [I64, I64]),
         "q8_linear_pack_weight": (ctypes.c_int, [P, I64, I64, P, S, P]),
         "q8_linear_operand_bytes": (S, [I64, I64]),
