@@ -250,7 +250,15 @@ __device__ __forceinline__ uint32_t bf16x2_from_ints(int lo, int hi) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-// One thread writes 8 consecutive bf16 (16 bytes) of a destination row.
+// Destination layout of the GEMM operands ("K-blocked"): dst[kb][r][kk] with
+// kb = k / 64 and kk = k % 64, so the 128 x 64 (or BN x 64) tile the tensor
+// cores read for one k-block is a single contiguous run in memory.
+__device__ __forceinline__ int64_t kblocked_index16(int64_t r, int64_t k0, int64_t rows) {
+  // index of the 16-byte chunk holding elements k0 .. k0 + 7 of row r
+  return (((k0 >> 6) * rows + r) * 64 + (k0 & 63)) / 8;
+}
+
+// One thread converts 8 consecutive elements (16 bytes of output) of a row.
 __global__ void __launch_bounds__(256) rows_to_bf16_kernel(const int8_t* __restrict__ src,
                                                            int64_t rows, int64_t K, int64_t ld,
                                                            int32_t zp, uint4* __restrict__ dst,
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(256) rows_to_bf16_kernel(const int8_t* __restr
     o.y = bf16x2_from_ints(v[2], v[3]);
     o.z = bf16x2_from_ints(v[4], v[5]);
     o.w = bf16x2_from_ints(v[6], v[7]);
-    dst[i] = o;
+    dst[kblocked_index16(r, k0, rows)] = o;
   }
 }
 
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
     o.y = bf16x2_from_ints(v[2], v[3]);
     o.z = bf16x2_from_ints(v[4], v[5]);
     o.w = bf16x2_from_ints(v[6], v[7]);
-    dst[i] = o;
+    dst[kblocked_index16(r, k0, rows)] = o;
   }
 }
 
@@ -353,10 +361,13 @@ cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, f
   return cudaGetLastError();
 }
 
-// NCHW int8 -> NHWC bf16 (x - zp), channels zero-padded to Cp (padding
-// channels are exactly 0, not -zp).  A block transposes a 64-channel x
-// 64-column slab of one (n, h) row through shared memory: 16-byte loads
-// along w, 16-byte stores along c.
+// NCHW int8 -> channel-blocked NHWC bf16 (x - zp): dst[n][c/64][h][w][c%64],
+// channels zero-padded to Cp (padding channels are exactly 0, not -zp), so
+// the (64 channels x w x h) box of one k-block is contiguous along w.  A
+// block transposes a 64-channel x 64-column slab of one (n, h) row through
+// shared memory: 16-byte loads along w, 16-byte stores along c.
+constexpr int kRowsPerBlock = 4;  // (n, h) rows whose loads a block issues together
+
 __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __restrict__ x,
                                                                 int64_t NH, int64_t C, int64_t H,
                                                                 int64_t W, int32_t zp,
@@ -367,44 +378,62 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * 64;
   const bool vec = (W % 16 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
   const int lc = threadIdx.x >> 2, wseg = threadIdx.x & 3;
-  for (int64_t nh = blockIdx.z; nh < NH; nh += gridDim.z) {  // nh = n * H + h
-    const int64_t n = nh / H, h = nh - n * H;
-    int8_t v[16];
-    const int64_t c = c0 + lc;
-    const int64_t wb = w0 + 16 * wseg;
-    if (c < C && vec && wb + 16 <= W) {
-      const int4 raw = __ldcs(reinterpret_cast<const int4*>(x + ((n * C + c) * H + h) * W + wb));
-      const int32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
+  const int64_t c = c0 + lc;
+  const int64_t wb = w0 + 16 * wseg;
+  for (int64_t nh0 = static_cast<int64_t>(blockIdx.z) * kRowsPerBlock; nh0 < NH;
+       nh0 += static_cast<int64_t>(gridDim.z) * kRowsPerBlock) {
+    // issue every row's loads before transposing any (bytes in flight)
+    int4 raw[kRowsPerBlock];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = static_cast<int8_t>((r[i >> 2] >> (8 * (i & 3))) & 0xff);
-    } else {
+    for (int r = 0; r < kRowsPerBlock; ++r) {
+      const int64_t nh = nh0 + r;
+      raw[r] = make_int4(0, 0, 0, 0);
+      if (nh < NH && c < C) {
+        const int64_t n = nh / H, h = nh - n * H;
+        const int8_t* src = x + ((n * C + c) * H + h) * W + wb;
+        if (vec && wb + 16 <= W) {
+          raw[r] = __ldcs(reinterpret_cast<const int4*>(src));
+        } else {
+          uint32_t wd[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (wb + i < W) wd[i >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(src[i])) << (8 * (i & 3));
+          raw[r] = make_int4(static_cast<int>(wd[0]), static_cast<int>(wd[1]), static_cast<int>(wd[2]),
+                             static_cast<int>(wd[3]));
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerBlock; ++r) {
+      const int64_t nh = nh0 + r;
+      if (nh >= NH) break;
+      const int64_t n = nh / H, h = nh - n * H;
+      __syncthreads();  // the previous row's readers are done with the tile
+      const int32_t rw[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        v[i] = (c < C && wb + i < W) ? x[((n * C + c) * H + h) * W + wb + i] : 0;
-    }
-    __syncthreads();  // the previous row's readers are done with the tile
+        tile[16 * wseg + i][lc] = static_cast<int8_t>((rw[i >> 2] >> (8 * (i & 3))) & 0xff);
+      __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 16; ++i) tile[16 * wseg + i][lc] = v[i];
-    __syncthreads();
+      for (int k = 0; k < 2; ++k) {
+        const int item = threadIdx.x + 256 * k;
+        const int w = item >> 3, cseg = item & 7;
+        const int64_t cc = c0 + 8 * cseg;
+        if (w0 + w < W && cc < Cp) {
+          const uint2 v = *reinterpret_cast<const uint2*>(&tile[w][8 * cseg]);
+          int d[8];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int item = threadIdx.x + 256 * k;
-      const int w = item >> 3, cseg = item & 7;
-      const int64_t cc = c0 + 8 * cseg;
-      if (w0 + w < W && cc < Cp) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(&tile[w][8 * cseg]);
-        int d[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          d[j] = (cc + j < C) ? static_cast<int8_t>((raw.x >> (8 * j)) & 0xff) - zp : 0;
-          d[4 + j] = (cc + 4 + j < C) ? static_cast<int8_t>((raw.y >> (8 * j)) & 0xff) - zp : 0;
+          for (int j = 0; j < 4; ++j) {
+            d[j] = (cc + j < C) ? static_cast<int8_t>((v.x >> (8 * j)) & 0xff) - zp : 0;
+            d[4 + j] = (cc + 4 + j < C) ? static_cast<int8_t>((v.y >> (8 * j)) & 0xff) - zp : 0;
+          }
+          uint4 o;
+          o.x = bf16x2_from_ints(d[0], d[1]);
+          o.y = bf16x2_from_ints(d[2], d[3]);
+          o.z = bf16x2_from_ints(d[4], d[5]);
+          o.w = bf16x2_from_ints(d[6], d[7]);
+          dst[((((n * (Cp / 64) + blockIdx.y) * H + h) * W + w0 + w) * 64 + 8 * cseg) / 8] = o;
         }
-        uint4 o;
-        o.x = bf16x2_from_ints(d[0], d[1]);
-        o.y = bf16x2_from_ints(d[2], d[3]);
-        o.z = bf16x2_from_ints(d[4], d[5]);
-        o.w = bf16x2_from_ints(d[6], d[7]);
-        dst[(((n * H + h) * W + w0 + w) * Cp + cc) / 8] = o;
       }
     }
   }
@@ -414,24 +443,32 @@ cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t C, int6
                                      int32_t zp, __nv_bfloat16* dst, int64_t Cp, cudaStream_t s) {
   if (N * H * W == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>((W + 63) / 64), static_cast<unsigned>(Cp / 64),
-            static_cast<unsigned>(std::min<int64_t>(N * H, 65535)));
+            static_cast<unsigned>(std::min<int64_t>((N * H + kRowsPerBlock - 1) / kRowsPerBlock,
+                                                    65535)));
   nchw_to_nhwc_bf16_kernel<<<grid, 256, 0, s>>>(x, N * H, C, H, W, zp,
                                                 reinterpret_cast<uint4*>(dst), Cp);
   return cudaGetLastError();
 }
 
+// Transposed-convolution weight [OC, ldw] (taps x IC used) -> bf16
+// dst[t][ic/64][oc][ic%64], input channels zero-padded to ICp: the
+// (BN output channels x 64 input channels) tile of one k-block is contiguous.
 __global__ void __launch_bounds__(256) convt_weight_bf16_kernel(const int8_t* __restrict__ w,
                                                                 int64_t OC, int64_t taps,
                                                                 int64_t IC, int64_t ldw,
                                                                 uint32_t* __restrict__ dst,
                                                                 int64_t ICp) {
-  const int64_t cols = taps * ICp;
-  const int64_t total = OC * cols / 2;
+  const int64_t icb = ICp / 64;
+  const int64_t total = taps * icb * OC * 32;  // bf16 pairs
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t oc = (2 * i) / cols;
-    const int64_t col = 2 * i - oc * cols;
-    const int64_t t = col / ICp, ic = col - t * ICp;
+    const int64_t jp = i & 31;
+    int64_t rest = i >> 5;
+    const int64_t oc = rest % OC;
+    rest /= OC;
+    const int64_t cb = rest % icb;
+    const int64_t t = rest / icb;
+    const int64_t ic = cb * 64 + 2 * jp;
     const int a = (ic < IC) ? w[oc * ldw + t * IC + ic] : 0;
     const int b = (ic + 1 < IC) ? w[oc * ldw + t * IC + ic + 1] : 0;
     dst[i] = bf16x2_from_ints(a, b);

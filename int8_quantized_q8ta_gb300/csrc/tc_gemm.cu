@@ -61,10 +61,11 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 constexpr int kBM = 128;
 constexpr int kBK = 64;             // bf16 per 128-byte row
 constexpr int kChunkKb = 8;         // 8 x 64 = 512 products per exact f32 chunk
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kMaxStages = 8;
+constexpr int kMaxPhases = 16;
+
+// Threads of a CTA with E epilogue warps: the TMA warp, the MMA warp, E more.
+__host__ __device__ constexpr int cta_threads(int epi_warps) { return 64 + 32 * epi_warps; }
 constexpr int kMaxBN = 256;
 
 struct TcParams {
@@ -78,6 +79,7 @@ struct TcParams {
   int Nimg, OC, Kh, Kw, H_out, W_out, sh, sw, pad_h, pad_w, icb, ICp;
   int BW, BH, tiles_w, tiles_h, tiles_oc;
   int staged;        // conv output goes through the shared-memory stage
+  int8_t ph_order[kMaxPhases];  // row phases, most taps first (stride_h <= kMaxPhases)
   uint32_t stage_off;  // byte offset of that stage from the aligned smem base
   // epilogue
   const float* ws;
@@ -114,7 +116,8 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int u, int j)
     ti.hb = u % p.tiles_h;
     u /= p.tiles_h;
     ti.n = u % p.Nimg;
-    ti.ph = u / p.Nimg;
+    const int phx = u / p.Nimg;
+    ti.ph = (p.sh <= kMaxPhases) ? p.ph_order[phx] : phx;
     ti.pw = j;
     ti.rh = (ti.ph + p.pad_h) % p.sh;
     ti.rw = (ti.pw + p.pad_w) % p.sw;
@@ -131,7 +134,7 @@ struct Ctl {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
-  uint64_t epi_bar;            // epilogue-warps rendezvous (count kEpiWarps)
+  uint64_t epi_bar;            // epilogue-warps rendezvous (one arrival per epilogue warp)
   uint32_t tmem_base;
   uint32_t abort_flag;
   alignas(16) float ep_ws[2][kMaxBN];  // per-tile column scales / biases, by tile parity
@@ -167,10 +170,11 @@ __device__ __forceinline__ void wait_bar_final(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Rendezvous of the 8 epilogue warps on an mbarrier (bounded, unlike
+// Rendezvous of the epilogue warps on an mbarrier (bounded, unlike
 // bar.sync, so one aborted warp cannot strand the others).  Shared-memory
 // writes made before the call are visible to every epilogue thread after it.
 __device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uint32_t* abort_flag) {
+  // every epilogue warp arrives once per rendezvous
   __syncwarp();
   bool ok = true;
   if ((threadIdx.x & 31) == 0) {
@@ -183,15 +187,21 @@ __device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uin
   return ok;
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int EPI>
+__global__ void __launch_bounds__(cta_threads(EPI), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
+  constexpr int kEpiWarps = EPI;
+  constexpr int kEpiThreads = EPI * 32;
+  constexpr int kColGroups = EPI / 4;     // epilogue warps sharing one TMEM lane quarter
   constexpr uint32_t kABytes = kBM * kBK * 2;
   constexpr uint32_t kBBytes = BN * kBK * 2;
   constexpr uint32_t kStageBytes = kABytes + kBBytes;
   constexpr uint32_t kTmemCols = 2 * BN;  // two f32 accumulator buffers
-  constexpr int kColsPerWarp = BN / 2;
+  constexpr int kColsPerWarp = BN / kColGroups;
+  // columns loaded from TMEM per wait: 32 where registers allow
+  constexpr int kDrainCols = kColsPerWarp >= 128 ? 16 : (kColsPerWarp < 32 ? kColsPerWarp : 32);
+  static_assert(kColsPerWarp % 16 == 0, "epilogue column slice must be a multiple of 16");
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   const int S = p.stages;
 
@@ -250,8 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sb = sa + kABytes;
             mbar_arrive_expect_tx(full, kStageBytes);
             if (p.mode == 0) {
-              tma_load_2d(sa, &tmA, full, kb * kBK, ti.mb * kBM);
-              tma_load_2d(sb, &tmB, full, kb * kBK, ti.nb * BN);
+              tma_load_3d(sa, &tmA, full, 0, ti.mb * kBM, kb);
+              tma_load_3d(sb, &tmB, full, 0, ti.nb * BN, kb);
             } else {
               const int icx = kb % p.icb;
               const int rest = kb / p.icb;
@@ -259,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int kh = ti.rh + th * p.sh, kw = ti.rw + tw * p.sw;
               const int dh = (ti.ph + p.pad_h - kh) / p.sh;
               const int dw = (ti.pw + p.pad_w - kw) / p.sw;
-              tma_load_4d(sa, &tmA, full, icx * kBK, ti.wb * p.BW + dw, ti.hb * p.BH + dh, ti.n);
-              tma_load_2d(sb, &tmB, full, (kh * p.Kw + kw) * p.ICp + icx * kBK, ti.ocb * BN);
+              tma_load_5d(sa, &tmA, full, 0, ti.wb * p.BW + dw, ti.hb * p.BH + dh, icx, ti.n);
+              tma_load_3d(sb, &tmB, full, 0, ti.ocb * BN, (kh * p.Kw + kw) * p.icb + icx);
             }
             ++fills;
             if (++stage == static_cast<uint32_t>(S)) {
@@ -326,10 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int quarter = warp & 3;           // TMEM lanes this warp may read
+    const int group = (warp - 2) >> 2;      // which column slice
     const int row = quarter * 32 + lane;
-    const int col0 = half * kColsPerWarp;
+    const int col0 = group * kColsPerWarp;
     const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc_it = 0, epi_phase = 0, tile_par = 0;
@@ -354,14 +364,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Each chunk sum is an integer below 2^24 in magnitude, so the f32 ->
           // int32 conversion is exact; the int32 adds wrap like the pages' i32.
 #pragma unroll
-          for (int c = 0; c < kColsPerWarp / 16; ++c) {
-            uint32_t r[16];
-            tmem_ld_16cols(tmem_base + lane_addr + buf * BN + col0 + 16 * c, r);
+          for (int c = 0; c < kColsPerWarp / kDrainCols; ++c) {
+            uint32_t r[kDrainCols];
+#pragma unroll
+            for (int h = 0; h < kDrainCols / 16; ++h)
+              tmem_ld_16cols(tmem_base + lane_addr + buf * BN + col0 + kDrainCols * c + 16 * h,
+                             *reinterpret_cast<uint32_t(*)[16]>(&r[16 * h]));
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              sum[16 * c + i] = static_cast<int32_t>(
-                  static_cast<uint32_t>(sum[16 * c + i]) +
+            for (int i = 0; i < kDrainCols; ++i)
+              sum[kDrainCols * c + i] = static_cast<int32_t>(
+                  static_cast<uint32_t>(sum[kDrainCols * c + i]) +
                   static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i]))));
           }
           tc_fence_before();
@@ -550,7 +563,8 @@ static bool encode_bf16(CUtensorMap* map, const void* base, int rank, const uint
                         const uint64_t* strides_bytes, const uint32_t* box) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
-  uint32_t estr[4] = {1, 1, 1, 1};
+  uint32_t estr[5] = {1, 1, 1, 1, 1};
+  if (rank < 1 || rank > 5) return false;
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
                    strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -560,7 +574,7 @@ static bool encode_bf16(CUtensorMap* map, const void* base, int rank, const uint
 
 constexpr size_t kSmemBudget = 225 * 1024;   // of the 227 KB a CTA may use
 
-template <int BN>
+template <int BN, int EPI>
 static cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b, TcParams p,
                              size_t out_stage_bytes, cudaStream_t s) {
   constexpr size_t kStage = static_cast<size_t>(kBM) * kBK * 2 + static_cast<size_t>(BN) * kBK * 2;
@@ -576,12 +590,13 @@ static cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b, TcParam
   cudaGetDevice(&dev);
   cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev & 63], [&] {
-    attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmemBudget + 1024));
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int grid = std::max(1, std::min(p.total_units, device_sm_count()));
-  tc_gemm_kernel<BN><<<grid, kThreads, smem, s>>>(a, b, p);
+  tc_gemm_kernel<BN, EPI><<<grid, cta_threads(EPI), smem, s>>>(a, b, p);
   return cudaGetLastError();
 }
 
@@ -591,26 +606,29 @@ static cudaError_t dispatch(int bn, const CUtensorMap& a, const CUtensorMap& b, 
                             size_t out_stage_bytes, cudaStream_t s) {
   if (p.total_units == 0) return cudaSuccess;
   switch (bn) {
-    case 64: return launch_bn<64>(a, b, p, out_stage_bytes, s);
-    case 128: return launch_bn<128>(a, b, p, out_stage_bytes, s);
-    default: return launch_bn<256>(a, b, p, out_stage_bytes, s);
+    // 16 epilogue warps where their register share fits the column slice
+    case 64: return launch_bn<64, 16>(a, b, p, out_stage_bytes, s);
+    case 128: return launch_bn<128, 16>(a, b, p, out_stage_bytes, s);
+    default: return launch_bn<256, 8>(a, b, p, out_stage_bytes, s);
   }
 }
 
 cudaError_t launch_tc_linear(const TcLinear& L, cudaStream_t s) {
   const int bn = pick_bn(L.N);
+  const uint64_t kblocks = static_cast<uint64_t>(L.Kp / kBK);
   CUtensorMap ma, mb;
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(L.Kp), static_cast<uint64_t>(L.M)};
-    const uint64_t str[1] = {static_cast<uint64_t>(L.Kp) * 2};
-    const uint32_t box[2] = {kBK, kBM};
-    if (!encode_bf16(&ma, L.a, 2, dims, str, box)) return cudaErrorInvalidValue;
+    // K-blocked operand: [Kp/64][M][64] bf16
+    const uint64_t dims[3] = {kBK, static_cast<uint64_t>(L.M), kblocks};
+    const uint64_t str[2] = {kBK * 2, static_cast<uint64_t>(L.M) * kBK * 2};
+    const uint32_t box[3] = {kBK, kBM, 1};
+    if (!encode_bf16(&ma, L.a, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(L.Kp), static_cast<uint64_t>(L.N)};
-    const uint64_t str[1] = {static_cast<uint64_t>(L.Kp) * 2};
-    const uint32_t box[2] = {kBK, static_cast<uint32_t>(bn)};
-    if (!encode_bf16(&mb, L.b, 2, dims, str, box)) return cudaErrorInvalidValue;
+    const uint64_t dims[3] = {kBK, static_cast<uint64_t>(L.N), kblocks};
+    const uint64_t str[2] = {kBK * 2, static_cast<uint64_t>(L.N) * kBK * 2};
+    const uint32_t box[3] = {kBK, static_cast<uint32_t>(bn), 1};
+    if (!encode_bf16(&mb, L.b, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   TcParams p{};
   p.mode = 0;
@@ -639,21 +657,24 @@ cudaError_t launch_tc_conv_t(const TcConvT& C, cudaStream_t s) {
   while (bw < Wq && bw < kBM) bw *= 2;
   const int bh = kBM / bw;
   CUtensorMap ma, mb;
+  const uint64_t icb = static_cast<uint64_t>(C.ICp / kBK);
   {
-    const uint64_t dims[4] = {static_cast<uint64_t>(C.ICp), static_cast<uint64_t>(C.W_in),
-                              static_cast<uint64_t>(C.H_in), static_cast<uint64_t>(C.N)};
-    const uint64_t str[3] = {static_cast<uint64_t>(C.ICp) * 2,
-                             static_cast<uint64_t>(C.W_in * C.ICp) * 2,
-                             static_cast<uint64_t>(C.H_in * C.W_in * C.ICp) * 2};
-    const uint32_t box[4] = {kBK, static_cast<uint32_t>(bw), static_cast<uint32_t>(bh), 1};
-    if (!encode_bf16(&ma, C.a, 4, dims, str, box)) return cudaErrorInvalidValue;
+    // channel-blocked NHWC input: [N][ICp/64][H_in][W_in][64] bf16
+    const uint64_t dims[5] = {kBK, static_cast<uint64_t>(C.W_in), static_cast<uint64_t>(C.H_in),
+                              icb, static_cast<uint64_t>(C.N)};
+    const uint64_t row = kBK * 2;
+    const uint64_t str[4] = {row, row * C.W_in, row * C.W_in * C.H_in,
+                             row * C.W_in * C.H_in * icb};
+    const uint32_t box[5] = {kBK, static_cast<uint32_t>(bw), static_cast<uint32_t>(bh), 1, 1};
+    if (!encode_bf16(&ma, C.a, 5, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
-    const int64_t cols = C.Kh * C.Kw * C.ICp;
-    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(C.OC)};
-    const uint64_t str[1] = {static_cast<uint64_t>(cols) * 2};
-    const uint32_t box[2] = {kBK, static_cast<uint32_t>(bn)};
-    if (!encode_bf16(&mb, C.b, 2, dims, str, box)) return cudaErrorInvalidValue;
+    // weight [taps][ICp/64][OC][64] bf16
+    const uint64_t dims[3] = {kBK, static_cast<uint64_t>(C.OC),
+                              static_cast<uint64_t>(C.Kh * C.Kw) * icb};
+    const uint64_t str[2] = {kBK * 2, static_cast<uint64_t>(C.OC) * kBK * 2};
+    const uint32_t box[3] = {kBK, static_cast<uint32_t>(bn), 1};
+    if (!encode_bf16(&mb, C.b, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   TcParams p{};
   p.mode = 1;
@@ -678,6 +699,17 @@ cudaError_t launch_tc_conv_t(const TcConvT& C, cudaStream_t s) {
   if (units > (1ll << 30)) return cudaErrorInvalidValue;
   p.total_units = static_cast<int>(units);
   p.subtiles = static_cast<int>(C.stride_w);
+  if (C.stride_h <= kMaxPhases) {
+    // row phases with more taps first, so the heaviest units start earliest
+    int order[kMaxPhases], taps[kMaxPhases];
+    for (int ph = 0; ph < C.stride_h; ++ph) {
+      const int64_t rh = (ph + C.pad_h) % C.stride_h;
+      taps[ph] = rh < C.Kh ? static_cast<int>((C.Kh - rh + C.stride_h - 1) / C.stride_h) : 0;
+      order[ph] = ph;
+    }
+    std::stable_sort(order, order + C.stride_h, [&](int x, int y) { return taps[x] > taps[y]; });
+    for (int i = 0; i < C.stride_h; ++i) p.ph_order[i] = static_cast<int8_t>(order[i]);
+  }
   p.ws = C.ws;
   p.bias = C.bias;
   p.rq = C.rq;
