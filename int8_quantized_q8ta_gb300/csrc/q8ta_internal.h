@@ -2,6 +2,7 @@
 // translation units (kernel launchers and the tensor-core GEMM plan).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstddef>
@@ -69,7 +70,13 @@ struct TcConvT {
 };
 cudaError_t launch_tc_conv_t(const TcConvT& p, cudaStream_t s);
 
-// Device error word (written by kernels whose pipeline waits time out).
+// Device error word (written by kernels whose pipeline waits time out):
+// its device address for the current device, and a synchronizing read.
+uint32_t* device_error_word();
 cudaError_t read_device_error(uint32_t* code, bool clear);
+
+// TMA tensor map of a bf16 tensor with 128-byte swizzle (tc_gemm_host.cu).
+bool encode_bf16_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box);
 
 }  // namespace q8

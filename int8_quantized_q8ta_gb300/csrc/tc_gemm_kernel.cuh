@@ -1,4 +1,4 @@
-// tc_gemm.cu -- exact int8 contraction on the sm_103a tcgen05 tensor cores.
+// tc_gemm_kernel.cuh -- exact int8 contraction on the sm_103a tcgen05 tensor cores.
 //
 // What it computes: the int32 accumulator of "Add q8ta_linear op" (Solution
 // paragraph), acc[m,n] = sum_k (x[m,k] - input_zero_point) * w[n,k], and of
@@ -32,10 +32,11 @@
 // Every mbarrier wait has a time limit (about 1 s); on expiry the CTA records
 // a code in g_q8_error, stops issuing work, waits (again bounded) for its own
 // copies and MMAs in flight, frees TMEM and returns.
+#pragma once
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstdint>
@@ -45,8 +46,6 @@
 #include "q8ta_internal.h"
 
 namespace q8 {
-
-__device__ uint32_t g_q8_error = 0;
 
 enum : uint32_t {
   kErrWaitFull = 0x101,
@@ -63,14 +62,18 @@ constexpr int kBK = 64;             // bf16 per 128-byte row
 constexpr int kChunkKb = 8;         // 8 x 64 = 512 products per exact f32 chunk
 constexpr int kMaxStages = 8;
 constexpr int kMaxPhases = 16;
+constexpr int kMaxEpiWarps = 16;
+constexpr int kMaxColsPerWarp = 128;
 
 // Threads of a CTA with E epilogue warps: the TMA warp, the MMA warp, E more.
 __host__ __device__ constexpr int cta_threads(int epi_warps) { return 64 + 32 * epi_warps; }
 constexpr int kMaxBN = 256;
+constexpr int kEpFloats = 8 * kMaxBN;  // scale/bias staging (see Ctl::ep)
 
 struct TcParams {
   int mode;          // 0 = linear, 1 = transposed convolution
   int stages;        // smem ring depth
+  int kd;            // k-blocks per ring stage (1 or 2): one TMA box holds kd k-blocks
   int total_units;   // work units; a unit is `subtiles` consecutive tiles
   int subtiles;      // 1 (linear) or stride_w (transposed convolution)
   // linear
@@ -88,6 +91,7 @@ struct TcParams {
   int8_t* out;
   int32_t* acc_out;
   int store_mode;    // linear int8 stores: 2 = 16 B, 1 = 4 B, 0 = bytes
+  uint32_t* err;     // the library's device error word
 };
 
 struct TileInfo {
@@ -102,9 +106,10 @@ struct TileInfo {
 // (row phase ph, image n, row block hb, column block wb, channel block ocb);
 // their sub-tiles are the stride_w column phases pw, so one CTA produces
 // every output column of its rows and can write whole rows.
+template <int MODE>
 __device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int u, int j) {
   TileInfo ti{};
-  if (p.mode == 0) {
+  if constexpr (MODE == 0) {
     ti.mb = u % p.tiles_m;
     ti.nb = u / p.tiles_m;
     ti.num_kb = p.kb_total;
@@ -137,14 +142,17 @@ struct Ctl {
   uint64_t epi_bar;            // epilogue-warps rendezvous (one arrival per epilogue warp)
   uint32_t tmem_base;
   uint32_t abort_flag;
-  alignas(16) float ep_ws[2][kMaxBN];  // per-tile column scales / biases, by tile parity
-  alignas(16) float ep_b[2][kMaxBN];
+  // each epilogue warp's column scales and biases for its current tile
+  // column scales and biases of the current tile:
+  //   linear: shared by all epilogue warps, two buffers by tile parity, [2][2][BN]
+  //   conv:   one slice per epilogue warp, [warp][2][BN / (warps / 4)] = 8 * BN
+  alignas(16) float ep[kEpFloats];
 };
 
 // Bounded wait.  Returns false when this CTA is aborting (this wait timed
 // out, or another role's did).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                         uint32_t code) {
+                                         uint32_t code, uint32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -152,19 +160,19 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1u;
-      atomicCAS(&g_q8_error, 0u, code);
+      atomicCAS(err, 0u, code);
       return false;
     }
   }
 }
 
 // Bounded wait used while shutting down: ignores the abort flag.
-__device__ __forceinline__ void wait_bar_final(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void wait_bar_final(uint32_t bar, uint32_t parity, uint32_t* err) {
   if (mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicCAS(&g_q8_error, 0u, kErrWaitDrain);
+      atomicCAS(err, 0u, kErrWaitDrain);
       return;
     }
   }
@@ -173,13 +181,14 @@ __device__ __forceinline__ void wait_bar_final(uint32_t bar, uint32_t parity) {
 // Rendezvous of the epilogue warps on an mbarrier (bounded, unlike
 // bar.sync, so one aborted warp cannot strand the others).  Shared-memory
 // writes made before the call are visible to every epilogue thread after it.
-__device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uint32_t* abort_flag) {
+__device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uint32_t* abort_flag,
+                                         uint32_t* err) {
   // every epilogue warp arrives once per rendezvous
   __syncwarp();
   bool ok = true;
   if ((threadIdx.x & 31) == 0) {
     mbar_arrive(smem_u32(&ctl->epi_bar));
-    ok = wait_bar(smem_u32(&ctl->epi_bar), phase, abort_flag, kErrWaitEpi);
+    ok = wait_bar(smem_u32(&ctl->epi_bar), phase, abort_flag, kErrWaitEpi, err);
   }
   phase ^= 1u;
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -187,22 +196,28 @@ __device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uin
   return ok;
 }
 
-template <int BN, int EPI>
+// MODE 0: q8ta_linear tiles; MODE 1: transposed-convolution units.
+// KD: k-blocks per ring stage (one TMA box spans KD k-blocks).
+template <int BN, int EPI, int MODE, int KD>
 __global__ void __launch_bounds__(cta_threads(EPI), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
   constexpr int kEpiWarps = EPI;
   constexpr int kEpiThreads = EPI * 32;
   constexpr int kColGroups = EPI / 4;     // epilogue warps sharing one TMEM lane quarter
-  constexpr uint32_t kABytes = kBM * kBK * 2;
-  constexpr uint32_t kBBytes = BN * kBK * 2;
-  constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  constexpr uint32_t kABytes = kBM * kBK * 2;   // one k-block of A
+  constexpr uint32_t kBBytes = BN * kBK * 2;    // one k-block of B
   constexpr uint32_t kTmemCols = 2 * BN;  // two f32 accumulator buffers
   constexpr int kColsPerWarp = BN / kColGroups;
   // columns loaded from TMEM per wait: 32 where registers allow
   constexpr int kDrainCols = kColsPerWarp >= 128 ? 16 : (kColsPerWarp < 32 ? kColsPerWarp : 32);
   static_assert(kColsPerWarp % 16 == 0, "epilogue column slice must be a multiple of 16");
+  static_assert(EPI <= kMaxEpiWarps && kColsPerWarp <= kMaxColsPerWarp, "epilogue smem slices");
+  static_assert(MODE != 0 || 4 * BN <= kEpFloats, "linear scale/bias buffers exceed Ctl::ep");
+  static_assert(MODE != 1 || EPI * 2 * kColsPerWarp <= kEpFloats,
+                "per-warp scale/bias slices exceed Ctl::ep");
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+  constexpr uint32_t kStageBytes = static_cast<uint32_t>(KD) * (kABytes + kBBytes);
   const int S = p.stages;
 
   extern __shared__ uint8_t smem_raw[];
@@ -249,33 +264,43 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
         for (int j = 0; j < p.subtiles && ok; ++j) {
-          const TileInfo ti = decode_tile(p, u, j);
-          for (int kb = 0; kb < ti.num_kb; ++kb) {
-            if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, kErrWaitEmpty)) {
-              ok = false;
-              break;
-            }
-            const uint32_t full = smem_u32(&ctl->full[stage]);
-            const uint32_t sa = base + stage * kStageBytes;
-            const uint32_t sb = sa + kABytes;
-            mbar_arrive_expect_tx(full, kStageBytes);
-            if (p.mode == 0) {
-              tma_load_3d(sa, &tmA, full, 0, ti.mb * kBM, kb);
-              tma_load_3d(sb, &tmB, full, 0, ti.nb * BN, kb);
-            } else {
-              const int icx = kb % p.icb;
-              const int rest = kb / p.icb;
-              const int tw = rest % ti.ntw, th = rest / ti.ntw;
-              const int kh = ti.rh + th * p.sh, kw = ti.rw + tw * p.sw;
-              const int dh = (ti.ph + p.pad_h - kh) / p.sh;
-              const int dw = (ti.pw + p.pad_w - kw) / p.sw;
-              tma_load_5d(sa, &tmA, full, 0, ti.wb * p.BW + dw, ti.hb * p.BH + dh, icx, ti.n);
-              tma_load_3d(sb, &tmB, full, 0, ti.ocb * BN, (kh * p.Kw + kw) * p.icb + icx);
-            }
-            ++fills;
-            if (++stage == static_cast<uint32_t>(S)) {
-              stage = 0;
-              phase ^= 1u;
+          const TileInfo ti = decode_tile<MODE>(p, u, j);
+          // k-blocks in (row tap, column tap, channel block) order, with the
+          // input offsets stepped incrementally: no division in this loop.
+          // Linear tiles are one "tap" of kb_total channel blocks.
+          const int ntaps_h = (MODE == 0) ? 1 : (ti.num_kb > 0 ? ti.num_kb / (ti.ntw * p.icb) : 0);
+          const int ntaps_w = (MODE == 0) ? 1 : ti.ntw;
+          const int nblk = (MODE == 0) ? ti.num_kb : p.icb;   // a multiple of KD
+          const int dh0 = (MODE == 0) ? 0 : (ti.ph + p.pad_h - ti.rh) / p.sh;
+          const int dw0 = (MODE == 0) ? 0 : (ti.pw + p.pad_w - ti.rw) / p.sw;
+          const int a_w = ti.wb * p.BW, a_h = ti.hb * p.BH;
+          for (int th = 0; th < ntaps_h && ok; ++th) {
+            for (int tw = 0; tw < ntaps_w && ok; ++tw) {
+              // tap (kh, kw) = (rh + th*sh, rw + tw*sw) reads input (oh' + dh, ow' + dw)
+              const int b_blk = ((ti.rh + th * p.sh) * p.Kw + ti.rw + tw * p.sw) * p.icb;
+              for (int blk = 0; blk < nblk; blk += KD) {
+                if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag,
+                              kErrWaitEmpty, p.err)) {
+                  ok = false;
+                  break;
+                }
+                const uint32_t full = smem_u32(&ctl->full[stage]);
+                const uint32_t sa = base + stage * kStageBytes;
+                const uint32_t sb = sa + KD * kABytes;
+                mbar_arrive_expect_tx(full, kStageBytes);
+                if constexpr (MODE == 0) {
+                  tma_load_3d(sa, &tmA, full, 0, ti.mb * kBM, blk);
+                  tma_load_3d(sb, &tmB, full, 0, ti.nb * BN, blk);
+                } else {
+                  tma_load_5d(sa, &tmA, full, 0, a_w + dw0 - tw, a_h + dh0 - th, blk, ti.n);
+                  tma_load_3d(sb, &tmB, full, 0, ti.ocb * BN, b_blk + blk);
+                }
+                ++fills;
+                if (++stage == static_cast<uint32_t>(S)) {
+                  stage = 0;
+                  phase ^= 1u;
+                }
+              }
             }
           }
         }
@@ -283,7 +308,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       // Let every copy this thread issued land before the CTA can exit.
       for (int s = 0; s < S; ++s) {
         const uint32_t f = (fills > static_cast<uint32_t>(s)) ? (fills - s + S - 1) / S : 0;
-        if (f > 0) wait_bar_final(smem_u32(&ctl->full[s]), (f - 1) & 1u);
+        if (f > 0) wait_bar_final(smem_u32(&ctl->full[s]), (f - 1) & 1u, p.err);
       }
     }
   } else if (warp == 1) {
@@ -293,30 +318,35 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
         for (int j = 0; j < p.subtiles && ok; ++j) {
-          const TileInfo ti = decode_tile(p, u, j);
+          const TileInfo ti = decode_tile<MODE>(p, u, j);
           for (int kb0 = 0; kb0 < ti.num_kb && ok; kb0 += kChunkKb) {
             const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
             if (!wait_bar(smem_u32(&ctl->acc_empty[buf]), (use & 1u) ^ 1u, abort_flag,
-                          kErrWaitAccEmpty)) {
+                          kErrWaitAccEmpty, p.err)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t d = tmem_base + buf * BN;
             const int kend = min(kb0 + kChunkKb, ti.num_kb);
-            for (int kb = kb0; kb < kend; ++kb) {
-              if (!wait_bar(smem_u32(&ctl->full[stage]), phase, abort_flag, kErrWaitFull)) {
+            for (int kb = kb0; kb < kend; kb += KD) {
+              if (!wait_bar(smem_u32(&ctl->full[stage]), phase, abort_flag, kErrWaitFull, p.err)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
               const uint32_t sa = base + stage * kStageBytes;
-              const uint64_t da = sw128_kmajor_desc(sa);
-              const uint64_t db = sw128_kmajor_desc(sa + kABytes);
+              const uint32_t sb = sa + KD * kABytes;
 #pragma unroll
-              for (int k = 0; k < kBK / 16; ++k) {
-                // +32 bytes along K inside the 128-byte swizzled row
-                umma_bf16(d, da + 2u * k, db + 2u * k, kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              for (int k2 = 0; k2 < KD; ++k2) {
+                const uint64_t da = sw128_kmajor_desc(sa + k2 * kABytes);
+                const uint64_t db = sw128_kmajor_desc(sb + k2 * kBBytes);
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k) {
+                  // +32 bytes along K inside the 128-byte swizzled row
+                  umma_bf16(d, da + 2u * k, db + 2u * k, kIdesc,
+                            (kb > kb0 || k2 > 0 || k > 0) ? 1u : 0u);
+                }
               }
               umma_commit(smem_u32(&ctl->empty[stage]));
               if (++stage == static_cast<uint32_t>(S)) {
@@ -332,7 +362,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       }
       // Every MMA issued so far must finish before TMEM is freed.
       umma_commit(smem_u32(&ctl->drain));
-      wait_bar_final(smem_u32(&ctl->drain), 0u);
+      wait_bar_final(smem_u32(&ctl->drain), 0u, p.err);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -342,11 +372,50 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     const int col0 = group * kColsPerWarp;
     const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t acc_it = 0, epi_phase = 0, tile_par = 0;
+    uint32_t acc_it = 0, epi_phase = 0, unit_par = 0, tile_par = 0;
+    int cur_ocb = -1;
+    const int ew = warp - 2;  // epilogue warp index
     bool ok = true;
     for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
       for (int j = 0; j < p.subtiles && ok; ++j) {
-        const TileInfo ti = decode_tile(p, u, j);
+        const TileInfo ti = decode_tile<MODE>(p, u, j);
+        const int gcolbase = (MODE == 0) ? ti.nb * BN : ti.ocb * BN;
+        const int ncols = (MODE == 0) ? p.N : p.OC;
+        // The tile's column scales and biases into shared memory, loaded
+        // before the accumulator waits so their latency hides there.
+        //   linear: one copy per tile for all warps (et < BN loads it), two
+        //     buffers by tile parity, published by the rendezvous below;
+        //   conv: each warp keeps its own columns, reloaded only when the
+        //     output-channel block changes (for OC <= BN: once per CTA).
+        const float* sws;
+        const float* sbs;
+        if constexpr (MODE == 0) {
+          float* ws_buf = ctl->ep + tile_par * (2 * kMaxBN);
+          if (p.acc_out == nullptr && et < BN) {
+            const int gc = gcolbase + et;
+            ws_buf[et] = (gc < ncols) ? __ldg(p.ws + gc) : 0.0f;
+            ws_buf[kMaxBN + et] = (gc < ncols && p.bias) ? __ldg(p.bias + gc) : 0.0f;
+          }
+          sws = ws_buf + col0;
+          sbs = ws_buf + kMaxBN + col0;
+        } else {
+          float* slice = ctl->ep + ew * (2 * kColsPerWarp);
+          if (p.acc_out == nullptr && ti.ocb != cur_ocb) {
+            __syncwarp();
+#pragma unroll
+            for (int c0 = 0; c0 < kColsPerWarp; c0 += 32) {
+              const int c = c0 + lane;
+              if (c < kColsPerWarp) {
+                const int gc = gcolbase + col0 + c;
+                slice[c] = (gc < ncols) ? __ldg(p.ws + gc) : 0.0f;
+                slice[kColsPerWarp + c] = (gc < ncols && p.bias) ? __ldg(p.bias + gc) : 0.0f;
+              }
+            }
+            cur_ocb = ti.ocb;
+          }
+          sws = slice;
+          sbs = slice + kColsPerWarp;
+        }
         int32_t sum[kColsPerWarp];
 #pragma unroll
         for (int c = 0; c < kColsPerWarp; ++c) sum[c] = 0;
@@ -354,7 +423,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
           bool got = true;
           if (lane == 0)
-            got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull);
+            got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull, p.err);
           got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
           if (!got) {
             ok = false;
@@ -385,25 +454,16 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
         if (!ok) break;
 
         // ---- fused epilogue
-        const int gcolbase = (p.mode == 0) ? ti.nb * BN : ti.ocb * BN;
-        const int ncols = (p.mode == 0) ? p.N : p.OC;
-        if (p.acc_out == nullptr) {
-          // this tile's column scales and biases, once, into shared memory
-          if (et < BN) {
-            const int gc = gcolbase + et;
-            ctl->ep_ws[tile_par][et] = (gc < ncols) ? __ldg(p.ws + gc) : 0.0f;
-            ctl->ep_b[tile_par][et] = (gc < ncols && p.bias) ? __ldg(p.bias + gc) : 0.0f;
-          }
-          if (!epi_sync(ctl, epi_phase, abort_flag)) {
+        if constexpr (MODE == 0) {
+          if (p.acc_out == nullptr && !epi_sync(ctl, epi_phase, abort_flag, p.err)) {
             ok = false;
             break;
           }
+          tile_par ^= 1u;
+        } else {
+          __syncwarp();  // this warp's scale/bias slice is visible to all its lanes
         }
-        const float* sws = ctl->ep_ws[tile_par] + col0;
-        const float* sbs = ctl->ep_b[tile_par] + col0;
-        tile_par ^= 1u;
-
-        if (p.mode == 0) {
+        if constexpr (MODE == 0) {
           const int grow = ti.mb * kBM + row;
           const int gcol0 = gcolbase + col0;
           if (grow < p.M) {
@@ -449,9 +509,11 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           const int oc0 = gcolbase + col0;
           const bool inside = (oh < p.H_out && ow < p.W_out);
           if (p.staged && p.acc_out == nullptr) {
-            // stage[oc][hh][wl], wl = ww * sw + pw: one unit's rows, all columns
+            // stage[oc][hh][wl], wl = ww * sw + pw: one unit's rows, all columns;
+            // two stages alternate by unit, so one rendezvous per unit suffices
             const int wt = p.BW * p.sw;
-            uint8_t* st = ostage + hh * wt + ww * p.sw + ti.pw;
+            uint8_t* stage_base = ostage + unit_par * (BN * p.BH * wt);
+            uint8_t* st = stage_base + hh * wt + ww * p.sw + ti.pw;
 #pragma unroll
             for (int g = 0; g < kColsPerWarp / 16; ++g) {
 #pragma unroll
@@ -472,7 +534,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
             }
             if (ti.pw == p.sw - 1) {
               // every column phase of this unit is staged: write whole rows
-              if (!epi_sync(ctl, epi_phase, abort_flag)) {
+              if (!epi_sync(ctl, epi_phase, abort_flag, p.err)) {
                 ok = false;
                 break;
               }
@@ -487,16 +549,13 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 const int ohh = (ti.hb * p.BH + rh) * p.sh + ti.ph;
                 const int oww = ow0 + 16 * ch;
                 if (oc < p.OC && ohh < p.H_out && oww < p.W_out) {
-                  const uint4 v = *reinterpret_cast<const uint4*>(ostage + r * wt + 16 * ch);
+                  const uint4 v = *reinterpret_cast<const uint4*>(stage_base + r * wt + 16 * ch);
                   int8_t* dst = p.out + (static_cast<int64_t>(ti.n) * p.OC + oc) * plane +
                                 static_cast<int64_t>(ohh) * p.W_out + oww;
                   *reinterpret_cast<uint4*>(dst) = v;   // W_out % 16 == 0 when staged
                 }
               }
-              if (!epi_sync(ctl, epi_phase, abort_flag)) {
-                ok = false;
-                break;
-              }
+              unit_par ^= 1u;
             }
           } else if (inside) {
             const int64_t plane = static_cast<int64_t>(p.H_out) * p.W_out;
@@ -542,45 +601,24 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
   }
 }
 
-// ---------------------------------------------------------------------------
-// Host side
-// ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
 
-static bool encode_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                        const uint64_t* strides_bytes, const uint32_t* box) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  uint32_t estr[5] = {1, 1, 1, 1, 1};
-  if (rank < 1 || rank > 5) return false;
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
-                   strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
+// ---------------------------------------------------------------------------
+// Host launch of one instantiation (smem ring sized from the budget)
+// ---------------------------------------------------------------------------
 constexpr size_t kSmemBudget = 225 * 1024;   // of the 227 KB a CTA may use
 
-template <int BN, int EPI>
-static cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b, TcParams p,
+inline int pick_bn(int64_t n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
+
+template <int BN, int EPI, int MODE, int KD>
+inline cudaError_t launch_tc_kernel(const CUtensorMap& a, const CUtensorMap& b, TcParams p,
                              size_t out_stage_bytes, cudaStream_t s) {
-  constexpr size_t kStage = static_cast<size_t>(kBM) * kBK * 2 + static_cast<size_t>(BN) * kBK * 2;
+  const size_t kStage = static_cast<size_t>(KD) *
+                        (static_cast<size_t>(kBM) * kBK * 2 + static_cast<size_t>(BN) * kBK * 2);
   const size_t fixed = sizeof(Ctl) + 1024 + out_stage_bytes;
   const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemBudget - fixed) / kStage));
   if (stages < 2) return cudaErrorInvalidValue;
+  p.err = device_error_word();
+  if (p.err == nullptr) return cudaErrorInvalidValue;
   p.stages = stages;
   const size_t ctl_end = static_cast<size_t>(stages) * kStage + sizeof(Ctl);
   p.stage_off = static_cast<uint32_t>((ctl_end + 127) / 128 * 128);
@@ -590,153 +628,14 @@ static cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b, TcParam
   cudaGetDevice(&dev);
   cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev & 63], [&] {
-    attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>,
+    attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, MODE, KD>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmemBudget + 1024));
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int grid = std::max(1, std::min(p.total_units, device_sm_count()));
-  tc_gemm_kernel<BN, EPI><<<grid, cta_threads(EPI), smem, s>>>(a, b, p);
+  tc_gemm_kernel<BN, EPI, MODE, KD><<<grid, cta_threads(EPI), smem, s>>>(a, b, p);
   return cudaGetLastError();
-}
-
-static int pick_bn(int64_t n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
-
-static cudaError_t dispatch(int bn, const CUtensorMap& a, const CUtensorMap& b, const TcParams& p,
-                            size_t out_stage_bytes, cudaStream_t s) {
-  if (p.total_units == 0) return cudaSuccess;
-  switch (bn) {
-    // 16 epilogue warps where their register share fits the column slice
-    case 64: return launch_bn<64, 16>(a, b, p, out_stage_bytes, s);
-    case 128: return launch_bn<128, 16>(a, b, p, out_stage_bytes, s);
-    default: return launch_bn<256, 8>(a, b, p, out_stage_bytes, s);
-  }
-}
-
-cudaError_t launch_tc_linear(const TcLinear& L, cudaStream_t s) {
-  const int bn = pick_bn(L.N);
-  const uint64_t kblocks = static_cast<uint64_t>(L.Kp / kBK);
-  CUtensorMap ma, mb;
-  {
-    // K-blocked operand: [Kp/64][M][64] bf16
-    const uint64_t dims[3] = {kBK, static_cast<uint64_t>(L.M), kblocks};
-    const uint64_t str[2] = {kBK * 2, static_cast<uint64_t>(L.M) * kBK * 2};
-    const uint32_t box[3] = {kBK, kBM, 1};
-    if (!encode_bf16(&ma, L.a, 3, dims, str, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[3] = {kBK, static_cast<uint64_t>(L.N), kblocks};
-    const uint64_t str[2] = {kBK * 2, static_cast<uint64_t>(L.N) * kBK * 2};
-    const uint32_t box[3] = {kBK, static_cast<uint32_t>(bn), 1};
-    if (!encode_bf16(&mb, L.b, 3, dims, str, box)) return cudaErrorInvalidValue;
-  }
-  TcParams p{};
-  p.mode = 0;
-  p.M = static_cast<int>(L.M);
-  p.N = static_cast<int>(L.N);
-  p.kb_total = static_cast<int>(L.Kp / kBK);
-  p.tiles_m = static_cast<int>((L.M + kBM - 1) / kBM);
-  const int tiles_n = static_cast<int>((L.N + bn - 1) / bn);
-  p.total_units = p.tiles_m * tiles_n;
-  p.subtiles = 1;
-  p.ws = L.ws;
-  p.bias = L.bias;
-  p.rq = L.rq;
-  p.out = L.out;
-  p.acc_out = L.acc_out;
-  const uintptr_t oa = reinterpret_cast<uintptr_t>(L.out);
-  p.store_mode = (L.N % 16 == 0 && oa % 16 == 0) ? 2 : (oa % 4 == 0 ? 1 : 0);
-  return dispatch(bn, ma, mb, p, 0, s);
-}
-
-cudaError_t launch_tc_conv_t(const TcConvT& C, cudaStream_t s) {
-  const int bn = pick_bn(C.OC);
-  const int64_t Hq = (C.H_out + C.stride_h - 1) / C.stride_h;
-  const int64_t Wq = (C.W_out + C.stride_w - 1) / C.stride_w;
-  int bw = 1;
-  while (bw < Wq && bw < kBM) bw *= 2;
-  const int bh = kBM / bw;
-  CUtensorMap ma, mb;
-  const uint64_t icb = static_cast<uint64_t>(C.ICp / kBK);
-  {
-    // channel-blocked NHWC input: [N][ICp/64][H_in][W_in][64] bf16
-    const uint64_t dims[5] = {kBK, static_cast<uint64_t>(C.W_in), static_cast<uint64_t>(C.H_in),
-                              icb, static_cast<uint64_t>(C.N)};
-    const uint64_t row = kBK * 2;
-    const uint64_t str[4] = {row, row * C.W_in, row * C.W_in * C.H_in,
-                             row * C.W_in * C.H_in * icb};
-    const uint32_t box[5] = {kBK, static_cast<uint32_t>(bw), static_cast<uint32_t>(bh), 1, 1};
-    if (!encode_bf16(&ma, C.a, 5, dims, str, box)) return cudaErrorInvalidValue;
-  }
-  {
-    // weight [taps][ICp/64][OC][64] bf16
-    const uint64_t dims[3] = {kBK, static_cast<uint64_t>(C.OC),
-                              static_cast<uint64_t>(C.Kh * C.Kw) * icb};
-    const uint64_t str[2] = {kBK * 2, static_cast<uint64_t>(C.OC) * kBK * 2};
-    const uint32_t box[3] = {kBK, static_cast<uint32_t>(bn), 1};
-    if (!encode_bf16(&mb, C.b, 3, dims, str, box)) return cudaErrorInvalidValue;
-  }
-  TcParams p{};
-  p.mode = 1;
-  p.Nimg = static_cast<int>(C.N);
-  p.OC = static_cast<int>(C.OC);
-  p.Kh = static_cast<int>(C.Kh);
-  p.Kw = static_cast<int>(C.Kw);
-  p.H_out = static_cast<int>(C.H_out);
-  p.W_out = static_cast<int>(C.W_out);
-  p.sh = static_cast<int>(C.stride_h);
-  p.sw = static_cast<int>(C.stride_w);
-  p.pad_h = static_cast<int>(C.pad_h);
-  p.pad_w = static_cast<int>(C.pad_w);
-  p.ICp = static_cast<int>(C.ICp);
-  p.icb = static_cast<int>(C.ICp / kBK);
-  p.BW = bw;
-  p.BH = bh;
-  p.tiles_w = static_cast<int>((Wq + bw - 1) / bw);
-  p.tiles_h = static_cast<int>((Hq + bh - 1) / bh);
-  p.tiles_oc = static_cast<int>((C.OC + bn - 1) / bn);
-  const int64_t units = C.stride_h * C.N * p.tiles_h * p.tiles_w * p.tiles_oc;
-  if (units > (1ll << 30)) return cudaErrorInvalidValue;
-  p.total_units = static_cast<int>(units);
-  p.subtiles = static_cast<int>(C.stride_w);
-  if (C.stride_h <= kMaxPhases) {
-    // row phases with more taps first, so the heaviest units start earliest
-    int order[kMaxPhases], taps[kMaxPhases];
-    for (int ph = 0; ph < C.stride_h; ++ph) {
-      const int64_t rh = (ph + C.pad_h) % C.stride_h;
-      taps[ph] = rh < C.Kh ? static_cast<int>((C.Kh - rh + C.stride_h - 1) / C.stride_h) : 0;
-      order[ph] = ph;
-    }
-    std::stable_sort(order, order + C.stride_h, [&](int x, int y) { return taps[x] > taps[y]; });
-    for (int i = 0; i < C.stride_h; ++i) p.ph_order[i] = static_cast<int8_t>(order[i]);
-  }
-  p.ws = C.ws;
-  p.bias = C.bias;
-  p.rq = C.rq;
-  p.out = C.out;
-  p.acc_out = C.acc_out;
-  p.store_mode = 0;
-  // Whole output rows go through shared memory when a unit's rows fit the
-  // stage and split into aligned 16-byte pieces.
-  const int64_t wt = static_cast<int64_t>(bw) * C.stride_w;
-  const size_t stage_bytes = static_cast<size_t>(bn) * kBM * C.stride_w;
-  const bool staged = C.out != nullptr && C.acc_out == nullptr && bn <= 128 &&
-                      C.stride_w <= 2 && wt % 16 == 0 && C.W_out % 16 == 0 &&
-                      reinterpret_cast<uintptr_t>(C.out) % 16 == 0;
-  p.staged = staged ? 1 : 0;
-  return dispatch(bn, ma, mb, p, staged ? stage_bytes : 0, s);
-}
-
-cudaError_t read_device_error(uint32_t* code, bool clear) {
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return e;
-  e = cudaMemcpyFromSymbol(code, g_q8_error, sizeof(uint32_t));
-  if (e != cudaSuccess) return e;
-  if (clear) {
-    const uint32_t zero = 0;
-    e = cudaMemcpyToSymbol(g_q8_error, &zero, sizeof(uint32_t));
-  }
-  return e;
 }
 
 }  // namespace q8
