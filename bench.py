@@ -315,19 +315,22 @@ def cpu_oracle_step_estimate(h, budget_s=12.0):
                                       conv_t=t_c)
 
 
-def traffic_from_profile():
-    """dram read+write bytes per GEMM launch from the committed ncu summary,
-    valid only while the GEMM source is unchanged since the capture."""
+def traffic_from_profile(key="tc_gemm_linear_2048x4096x11008"):
+    """DRAM read+write bytes per launch of a GEMM from the committed ncu
+    summary (profiles/traffic.json), valid only while the kernel's source
+    files are unchanged since the capture; otherwise None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "int8_quantized_q8ta_gb300", "csrc", "tc_gemm.cu")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f)
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
-    e = d.get("tc_gemm_linear_2048x4096x11008")
-    if not e or e.get("source_sha256_16") != digest:
+        e = json.load(f).get(key)
+    if not e:
+        return None
+    digest = hashlib.sha256()
+    for rel in e.get("source_files", []):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            digest.update(f.read())
+    if digest.hexdigest()[:16] != e.get("source_sha256_16"):
         return None
     return e.get("dram_bytes_per_launch")
 
