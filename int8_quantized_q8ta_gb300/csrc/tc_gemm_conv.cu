@@ -94,13 +94,15 @@ cudaError_t launch_tc_conv_t(const TcConvT& C, cudaStream_t s) {
   p.staged = staged ? 1 : 0;
   if (p.total_units == 0) return cudaSuccess;
   const size_t ostage = staged ? stage_bytes : 0;
+  // one CTA per 128-row tile: on this workload the 2-SM MMA measured no
+  // faster (its stages fit, but the conv's k-blocks are short and many)
   switch (bn * 4 + kd) {
-    case 64 * 4 + 1: return launch_tc_kernel<64, 16, 1, 1>(ma, mb, p, ostage, s);
-    case 64 * 4 + 2: return launch_tc_kernel<64, 16, 1, 2>(ma, mb, p, ostage, s);
-    case 128 * 4 + 1: return launch_tc_kernel<128, 16, 1, 1>(ma, mb, p, ostage, s);
-    case 128 * 4 + 2: return launch_tc_kernel<128, 16, 1, 2>(ma, mb, p, ostage, s);
-    case 256 * 4 + 1: return launch_tc_kernel<256, 8, 1, 1>(ma, mb, p, ostage, s);
-    default: return launch_tc_kernel<256, 8, 1, 2>(ma, mb, p, ostage, s);
+    case 64 * 4 + 1: return launch_tc_kernel<64, 16, 1, 1, 1>(ma, mb, p, ostage, s);
+    case 64 * 4 + 2: return launch_tc_kernel<64, 16, 1, 2, 1>(ma, mb, p, ostage, s);
+    case 128 * 4 + 1: return launch_tc_kernel<128, 16, 1, 1, 1>(ma, mb, p, ostage, s);
+    case 128 * 4 + 2: return launch_tc_kernel<128, 16, 1, 2, 1>(ma, mb, p, ostage, s);
+    case 256 * 4 + 1: return launch_tc_kernel<256, 8, 1, 1, 1>(ma, mb, p, ostage, s);
+    default: return launch_tc_kernel<256, 8, 1, 2, 1>(ma, mb, p, ostage, s);
   }
 }
 

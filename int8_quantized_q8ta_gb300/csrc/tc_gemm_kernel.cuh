@@ -24,11 +24,17 @@
 // filled with zeros by the TMA unit, which is exactly "taps outside the input
 // contribute nothing" because the stored values are x - input_zero_point.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
+// Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one thread)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4)..+31, half of the
-//               tile's columns each, keeps the int32 running sums in registers
+//   warps 2..   E epilogue warps (8, 12 or 16): warp w reads TMEM lanes
+//               32*(w%4)..+31 and BN / (E/4) of the tile's columns, keeping
+//               the int32 running sums in registers
+// With CTA pairs (CG = 2, a cluster of two CTAs on neighbouring SMs) one
+// 256 x BN tile is computed by the 2-SM MMA: each CTA loads its own 128 rows
+// of A and half of the BN rows of B, the leader CTA's MMA thread issues the
+// MMAs for both, and each CTA's epilogue drains its own TMEM rows.  Per SM
+// that is 16 KB of B per k-block instead of 32 KB at BN = 256.
 // Every mbarrier wait has a time limit (about 1 s); on expiry the CTA records
 // a code in g_q8_error, stops issuing work, waits (again bounded) for its own
 // copies and MMAs in flight, frees TMEM and returns.
@@ -95,7 +101,9 @@ struct TcParams {
 };
 
 struct TileInfo {
-  int num_kb;
+  int num_kb;   // k-blocks of the tile
+  int nstages;  // ring stages that carry them (KD k-blocks each; a stage
+                // past a tap's last channel block holds zeros of A)
   // linear
   int mb, nb;
   // conv
@@ -106,19 +114,23 @@ struct TileInfo {
 // (row phase ph, image n, row block hb, column block wb, channel block ocb);
 // their sub-tiles are the stride_w column phases pw, so one CTA produces
 // every output column of its rows and can write whole rows.
-template <int MODE>
-__device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int u, int j) {
+// With CTA pairs (CG == 2) a unit spans CG row blocks of 128: the CTA of
+// rank r takes row block (u % tiles) * CG + r, and p.tiles_m / p.tiles_h
+// count pairs of row blocks.
+template <int MODE, int CG, int KD>
+__device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int u, int j, int rank) {
   TileInfo ti{};
   if constexpr (MODE == 0) {
-    ti.mb = u % p.tiles_m;
+    ti.mb = (u % p.tiles_m) * CG + rank;
     ti.nb = u / p.tiles_m;
     ti.num_kb = p.kb_total;
+    ti.nstages = (p.kb_total + KD - 1) / KD;
   } else {
     ti.ocb = u % p.tiles_oc;
     u /= p.tiles_oc;
     ti.wb = u % p.tiles_w;
     u /= p.tiles_w;
-    ti.hb = u % p.tiles_h;
+    ti.hb = (u % p.tiles_h) * CG + rank;
     u /= p.tiles_h;
     ti.n = u % p.Nimg;
     const int phx = u / p.Nimg;
@@ -129,6 +141,7 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int u, int j)
     const int nth = ti.rh < p.Kh ? (p.Kh - ti.rh + p.sh - 1) / p.sh : 0;
     ti.ntw = ti.rw < p.Kw ? (p.Kw - ti.rw + p.sw - 1) / p.sw : 0;
     ti.num_kb = nth * ti.ntw * p.icb;
+    ti.nstages = nth * ti.ntw * ((p.icb + KD - 1) / KD);
   }
   return ti;
 }
@@ -198,7 +211,11 @@ __device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uin
 
 // MODE 0: q8ta_linear tiles; MODE 1: transposed-convolution units.
 // KD: k-blocks per ring stage (one TMA box spans KD k-blocks).
-template <int BN, int EPI, int MODE, int KD>
+// CG: 1 = one CTA per 128-row tile (cta_group::1); 2 = a cluster of two CTAs
+// shares one 256-row tile through the 2-SM MMA (cta_group::2): each CTA
+// loads its 128 rows of A and half of B's BN rows, the leader CTA issues
+// the MMAs, and each CTA's TMEM holds the accumulators of its own rows.
+template <int BN, int EPI, int MODE, int KD, int CG>
 __global__ void __launch_bounds__(cta_threads(EPI), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
@@ -206,17 +223,26 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
   constexpr int kEpiThreads = EPI * 32;
   constexpr int kColGroups = EPI / 4;     // epilogue warps sharing one TMEM lane quarter
   constexpr uint32_t kABytes = kBM * kBK * 2;   // one k-block of A
-  constexpr uint32_t kBBytes = BN * kBK * 2;    // one k-block of B
-  constexpr uint32_t kTmemCols = 2 * BN;  // two f32 accumulator buffers
+  constexpr uint32_t kBBytes = (BN / CG) * kBK * 2;  // this CTA's part of one k-block of B
+  // two f32 accumulator buffers, 32-column aligned; the allocation is a power of two
+  constexpr uint32_t kAccStride = (BN + 31) / 32 * 32;
+  constexpr uint32_t kTmemCols = 2 * kAccStride <= 64 ? 64 : (2 * kAccStride <= 128 ? 128
+                                 : (2 * kAccStride <= 256 ? 256 : 512));
+  static_assert(2 * kAccStride <= 512, "two accumulator buffers fit TMEM");
   constexpr int kColsPerWarp = BN / kColGroups;
   // columns loaded from TMEM per wait: 32 where registers allow
-  constexpr int kDrainCols = kColsPerWarp >= 128 ? 16 : (kColsPerWarp < 32 ? kColsPerWarp : 32);
+  constexpr int kDrainCols = (kColsPerWarp >= 128 || kColsPerWarp % 32 != 0) ? 16 : 32;
   static_assert(kColsPerWarp % 16 == 0, "epilogue column slice must be a multiple of 16");
+  static_assert(BN % 16 == 0 && BN >= 16 * CG && BN <= 256, "MMA N: a multiple of 16 up to 256");
+  static_assert((BN / CG) % 8 == 0, "B tiles keep the 1024-byte swizzle-atom alignment");
   static_assert(EPI <= kMaxEpiWarps && kColsPerWarp <= kMaxColsPerWarp, "epilogue smem slices");
   static_assert(MODE != 0 || 4 * BN <= kEpFloats, "linear scale/bias buffers exceed Ctl::ep");
   static_assert(MODE != 1 || EPI * 2 * kColsPerWarp <= kEpFloats,
                 "per-warp scale/bias slices exceed Ctl::ep");
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM * CG, BN);
+  constexpr bool kPair = (CG == 2);
+  constexpr int kChunkStages = kChunkKb / KD;   // exact-f32 chunk, in ring stages
+  static_assert(kChunkKb % KD == 0, "a chunk holds whole stages");
   constexpr uint32_t kStageBytes = static_cast<uint32_t>(KD) * (kABytes + kBBytes);
   const int S = p.stages;
 
@@ -230,6 +256,11 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = (rank == 0);
+  // persistent loop over units: a CTA pair walks the units together
+  const int unit0 = static_cast<int>(blockIdx.x) / CG;
+  const int unit_step = static_cast<int>(gridDim.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -238,7 +269,8 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->acc_full[b]), 1);
-      mbar_init(smem_u32(&ctl->acc_empty[b]), kEpiWarps);
+      // the leader's MMA reuses a buffer once both CTAs' epilogues drained it
+      mbar_init(smem_u32(&ctl->acc_empty[b]), kEpiWarps * CG);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     mbar_init(smem_u32(&ctl->epi_bar), kEpiWarps);
@@ -248,11 +280,17 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
@@ -262,15 +300,16 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       uint32_t stage = 0, phase = 0;
       uint32_t fills = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+      for (int u = unit0; u < p.total_units && ok; u += unit_step) {
         for (int j = 0; j < p.subtiles && ok; ++j) {
-          const TileInfo ti = decode_tile<MODE>(p, u, j);
+          const TileInfo ti = decode_tile<MODE, CG, KD>(p, u, j, rank);
           // k-blocks in (row tap, column tap, channel block) order, with the
           // input offsets stepped incrementally: no division in this loop.
           // Linear tiles are one "tap" of kb_total channel blocks.
           const int ntaps_h = (MODE == 0) ? 1 : (ti.num_kb > 0 ? ti.num_kb / (ti.ntw * p.icb) : 0);
           const int ntaps_w = (MODE == 0) ? 1 : ti.ntw;
-          const int nblk = (MODE == 0) ? ti.num_kb : p.icb;   // a multiple of KD
+          // channel blocks per tap, KD per stage (a last stage may run past them)
+          const int nblk = (MODE == 0) ? ti.num_kb : p.icb;
           const int dh0 = (MODE == 0) ? 0 : (ti.ph + p.pad_h - ti.rh) / p.sh;
           const int dw0 = (MODE == 0) ? 0 : (ti.pw + p.pad_w - ti.rw) / p.sw;
           const int a_w = ti.wb * p.BW, a_h = ti.hb * p.BH;
@@ -284,16 +323,30 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                   ok = false;
                   break;
                 }
-                const uint32_t full = smem_u32(&ctl->full[stage]);
                 const uint32_t sa = base + stage * kStageBytes;
                 const uint32_t sb = sa + KD * kABytes;
-                mbar_arrive_expect_tx(full, kStageBytes);
-                if constexpr (MODE == 0) {
-                  tma_load_3d(sa, &tmA, full, 0, ti.mb * kBM, blk);
-                  tma_load_3d(sb, &tmB, full, 0, ti.nb * BN, blk);
+                const int b_row = (MODE == 0 ? ti.nb : ti.ocb) * BN + rank * (BN / CG);
+                if constexpr (kPair) {
+                  // both CTAs' copies complete on the leader's full barrier
+                  const uint32_t full = map_to_cta(smem_u32(&ctl->full[stage]), 0);
+                  if (leader) mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), CG * kStageBytes);
+                  if constexpr (MODE == 0) {
+                    tma_load_3d_pair(sa, &tmA, full, 0, ti.mb * kBM, blk);
+                    tma_load_3d_pair(sb, &tmB, full, 0, b_row, blk);
+                  } else {
+                    tma_load_5d_pair(sa, &tmA, full, 0, a_w + dw0 - tw, a_h + dh0 - th, blk, ti.n);
+                    tma_load_3d_pair(sb, &tmB, full, 0, b_row, b_blk + blk);
+                  }
                 } else {
-                  tma_load_5d(sa, &tmA, full, 0, a_w + dw0 - tw, a_h + dh0 - th, blk, ti.n);
-                  tma_load_3d(sb, &tmB, full, 0, ti.ocb * BN, b_blk + blk);
+                  const uint32_t full = smem_u32(&ctl->full[stage]);
+                  mbar_arrive_expect_tx(full, kStageBytes);
+                  if constexpr (MODE == 0) {
+                    tma_load_3d(sa, &tmA, full, 0, ti.mb * kBM, blk);
+                    tma_load_3d(sb, &tmB, full, 0, b_row, blk);
+                  } else {
+                    tma_load_5d(sa, &tmA, full, 0, a_w + dw0 - tw, a_h + dh0 - th, blk, ti.n);
+                    tma_load_3d(sb, &tmB, full, 0, b_row, b_blk + blk);
+                  }
                 }
                 ++fills;
                 if (++stage == static_cast<uint32_t>(S)) {
@@ -305,21 +358,24 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           }
         }
       }
-      // Let every copy this thread issued land before the CTA can exit.
-      for (int s = 0; s < S; ++s) {
+      // Let every copy this thread issued land before the CTA can exit (a
+      // peer's copies complete on the leader's barriers; the leader waits
+      // for both, and the closing cluster barrier holds the peer until then).
+      for (int s = 0; s < S && leader; ++s) {
         const uint32_t f = (fills > static_cast<uint32_t>(s)) ? (fills - s + S - 1) / S : 0;
         if (f > 0) wait_bar_final(smem_u32(&ctl->full[s]), (f - 1) & 1u, p.err);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, acc_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+      for (int u = unit0; u < p.total_units && ok; u += unit_step) {
         for (int j = 0; j < p.subtiles && ok; ++j) {
-          const TileInfo ti = decode_tile<MODE>(p, u, j);
-          for (int kb0 = 0; kb0 < ti.num_kb && ok; kb0 += kChunkKb) {
+          const TileInfo ti = decode_tile<MODE, CG, KD>(p, u, j, rank);
+          // chunks of kChunkStages stages: at most kChunkKb k-blocks each
+          for (int st0 = 0; st0 < ti.nstages && ok; st0 += kChunkStages) {
             const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
             if (!wait_bar(smem_u32(&ctl->acc_empty[buf]), (use & 1u) ^ 1u, abort_flag,
                           kErrWaitAccEmpty, p.err)) {
@@ -327,9 +383,9 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               break;
             }
             tc_fence_after();
-            const uint32_t d = tmem_base + buf * BN;
-            const int kend = min(kb0 + kChunkKb, ti.num_kb);
-            for (int kb = kb0; kb < kend; kb += KD) {
+            const uint32_t d = tmem_base + buf * kAccStride;
+            const int st_end = min(st0 + kChunkStages, ti.nstages);
+            for (int st = st0; st < st_end; ++st) {
               if (!wait_bar(smem_u32(&ctl->full[stage]), phase, abort_flag, kErrWaitFull, p.err)) {
                 ok = false;
                 break;
@@ -344,24 +400,37 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k) {
                   // +32 bytes along K inside the 128-byte swizzled row
-                  umma_bf16(d, da + 2u * k, db + 2u * k, kIdesc,
-                            (kb > kb0 || k2 > 0 || k > 0) ? 1u : 0u);
+                  const uint32_t acc = (st > st0 || k2 > 0 || k > 0) ? 1u : 0u;
+                  if constexpr (kPair)
+                    umma_bf16_pair(d, da + 2u * k, db + 2u * k, kIdesc, acc);
+                  else
+                    umma_bf16(d, da + 2u * k, db + 2u * k, kIdesc, acc);
                 }
               }
-              umma_commit(smem_u32(&ctl->empty[stage]));
+              // the stage is free in every CTA that supplied it
+              if constexpr (kPair)
+                umma_commit_pair(smem_u32(&ctl->empty[stage]), 0x3);
+              else
+                umma_commit(smem_u32(&ctl->empty[stage]));
               if (++stage == static_cast<uint32_t>(S)) {
                 stage = 0;
                 phase ^= 1u;
               }
             }
             if (!ok) break;
-            umma_commit(smem_u32(&ctl->acc_full[buf]));
+            if constexpr (kPair)
+              umma_commit_pair(smem_u32(&ctl->acc_full[buf]), 0x3);
+            else
+              umma_commit(smem_u32(&ctl->acc_full[buf]));
             ++acc_it;
           }
         }
       }
       // Every MMA issued so far must finish before TMEM is freed.
-      umma_commit(smem_u32(&ctl->drain));
+      if constexpr (kPair)
+        umma_commit_pair(smem_u32(&ctl->drain), 0x1);
+      else
+        umma_commit(smem_u32(&ctl->drain));
       wait_bar_final(smem_u32(&ctl->drain), 0u, p.err);
     }
   } else {
@@ -376,9 +445,9 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     int cur_ocb = -1;
     const int ew = warp - 2;  // epilogue warp index
     bool ok = true;
-    for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+    for (int u = unit0; u < p.total_units && ok; u += unit_step) {
       for (int j = 0; j < p.subtiles && ok; ++j) {
-        const TileInfo ti = decode_tile<MODE>(p, u, j);
+        const TileInfo ti = decode_tile<MODE, CG, KD>(p, u, j, rank);
         const int gcolbase = (MODE == 0) ? ti.nb * BN : ti.ocb * BN;
         const int ncols = (MODE == 0) ? p.N : p.OC;
         // The tile's column scales and biases into shared memory, loaded
@@ -419,7 +488,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
         int32_t sum[kColsPerWarp];
 #pragma unroll
         for (int c = 0; c < kColsPerWarp; ++c) sum[c] = 0;
-        for (int kb0 = 0; kb0 < ti.num_kb; kb0 += kChunkKb) {
+        for (int st0 = 0; st0 < ti.nstages; st0 += kChunkStages) {
           const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
           bool got = true;
           if (lane == 0)
@@ -437,7 +506,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
             uint32_t r[kDrainCols];
 #pragma unroll
             for (int h = 0; h < kDrainCols / 16; ++h)
-              tmem_ld_16cols(tmem_base + lane_addr + buf * BN + col0 + kDrainCols * c + 16 * h,
+              tmem_ld_16cols(tmem_base + lane_addr + buf * kAccStride + col0 + kDrainCols * c + 16 * h,
                              *reinterpret_cast<uint32_t(*)[16]>(&r[16 * h]));
             tmem_ld_wait();
 #pragma unroll
@@ -448,7 +517,13 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+          if (lane == 0) {
+            // the MMA issuer (the leader CTA's) may reuse this buffer
+            if (kPair && !leader)
+              mbar_arrive_cluster(map_to_cta(smem_u32(&ctl->acc_empty[buf]), 0));
+            else
+              mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+          }
           ++acc_it;
         }
         if (!ok) break;
@@ -595,9 +670,15 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair leaves while the leader's MMAs may still read the
+  // peer's shared memory or signal its barriers
+  if constexpr (kPair) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -609,32 +690,63 @@ constexpr size_t kSmemBudget = 225 * 1024;   // of the 227 KB a CTA may use
 
 inline int pick_bn(int64_t n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
 
-template <int BN, int EPI, int MODE, int KD>
+template <int BN, int EPI, int MODE, int KD, int CG>
 inline cudaError_t launch_tc_kernel(const CUtensorMap& a, const CUtensorMap& b, TcParams p,
-                             size_t out_stage_bytes, cudaStream_t s) {
-  const size_t kStage = static_cast<size_t>(KD) *
-                        (static_cast<size_t>(kBM) * kBK * 2 + static_cast<size_t>(BN) * kBK * 2);
+                                    size_t out_stage_bytes, cudaStream_t s) {
+  const size_t kStage = static_cast<size_t>(KD) * (static_cast<size_t>(kBM) * kBK * 2 +
+                                                   static_cast<size_t>(BN / CG) * kBK * 2);
   const size_t fixed = sizeof(Ctl) + 1024 + out_stage_bytes;
   const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemBudget - fixed) / kStage));
   if (stages < 2) return cudaErrorInvalidValue;
   p.err = device_error_word();
   if (p.err == nullptr) return cudaErrorInvalidValue;
   p.stages = stages;
+  p.kd = KD;
   const size_t ctl_end = static_cast<size_t>(stages) * kStage + sizeof(Ctl);
   p.stage_off = static_cast<uint32_t>((ctl_end + 127) / 128 * 128);
   const size_t smem = p.stage_off + out_stage_bytes + 1024;
+  auto kernel = tc_gemm_kernel<BN, EPI, MODE, KD, CG>;
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev & 63], [&] {
-    attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, MODE, KD>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmemBudget + 1024));
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const int grid = std::max(1, std::min(p.total_units, device_sm_count()));
-  tc_gemm_kernel<BN, EPI, MODE, KD><<<grid, cta_threads(EPI), smem, s>>>(a, b, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(static_cast<unsigned>(cta_threads(EPI)), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent: one CTA per SM, or one CTA pair per co-resident SM pair (a
+  // pair must share a GPC, so fewer than SMs / 2 pairs may fit at once)
+  int resident = device_sm_count() / CG;
+  if (CG > 1) {
+    static int pairs_cache[64] = {};
+    int& cached = pairs_cache[dev & 63];
+    if (cached == 0) {
+      cfg.gridDim = dim3(static_cast<unsigned>(resident * CG), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = resident;
+      }
+      cached = n;
+    }
+    resident = std::min(resident, cached);
+  }
+  const int groups = std::max(1, std::min(p.total_units, resident));
+  cfg.gridDim = dim3(static_cast<unsigned>(groups * CG), 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, b, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -103,8 +103,13 @@ def test_gemv_ragged(K, N, izp):
 
 # --------------------------------------------------------------- linear
 
+# The last three rows pick the 224-, 240- and 256-column pair tiles on a
+# 152-SM GPU (the widths that fill the last wave best); the others use the
+# 192-column pair tile or one CTA per tile.  Odd k-block counts leave a
+# zero-filled half stage.
 LINEAR_SHAPES = [(2, 4, 4, 0), (8, 64, 32, 3), (130, 200, 36, -128), (257, 520, 260, 127),
-                 (129, 1040, 516, -5), (300, 4096, 136, 1), (64, 1536, 64, -100)]
+                 (129, 1040, 516, -5), (300, 4096, 136, 1), (64, 1536, 64, -100),
+                 (257, 192, 7300, 77), (257, 136, 8516, -3), (257, 520, 9124, 0)]
 
 
 @pytest.mark.parametrize("M,K,N,izp", LINEAR_SHAPES)
