@@ -4,6 +4,7 @@
 // enqueued (the "fail-loud" guards of the three q8ta pages' Implementation
 // paragraphs), forms the f32 reciprocals in double, lays out the caller's
 // workspace and enqueues the kernels on the caller's stream.
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,6 +41,7 @@ q8::Requant make_rq(double input_scale, double output_scale, int32_t ozp) {
   r.s_in = static_cast<float>(input_scale);
   r.inv_out = recip_f32(output_scale);
   r.ozp = static_cast<float>(ozp);
+  r.ozp_i = ozp;
   return r;
 }
 
@@ -63,6 +65,15 @@ q8_status check_linear(const int8_t* x, int64_t M, int64_t K, double input_scale
 
 size_t bf16_rows_bytes(int64_t rows, int64_t K) {
   return align_ws(static_cast<size_t>(rows) * static_cast<size_t>(round_up(K, kTileK)) * 2);
+}
+
+// Largest |x - zp| over int8 x.
+inline int a_bound_of(int32_t zp) { return std::max(128 + zp, 127 - zp); }
+
+// A prepared operand is the bf16 data followed by one 256-byte trailer whose
+// first int32 holds a_bound_of(zp) of the zero point it was prepared with.
+int32_t* operand_bound_word(void* operand, int64_t M, int64_t K) {
+  return reinterpret_cast<int32_t*>(static_cast<char*>(operand) + bf16_rows_bytes(M, K));
 }
 
 }  // namespace
@@ -124,7 +135,7 @@ size_t q8_linear_packed_weight_bytes(int64_t N, int64_t K) {
 
 size_t q8_linear_operand_bytes(int64_t M, int64_t K) {
   if (M < 1 || K < 1) return 0;
-  return bf16_rows_bytes(M, K);
+  return bf16_rows_bytes(M, K) + q8::kWorkspaceAlign;
 }
 
 q8_status q8_linear_gemv(const int8_t* x, int64_t M, int64_t K, double input_scale,
@@ -176,6 +187,7 @@ q8_status q8_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
   L.bias = bias;
   L.rq = make_rq(input_scale, output_scale, output_zero_point);
   L.out = out;
+  L.a_bound_host = a_bound_of(input_zero_point);
   return cuda_status(q8::launch_tc_linear(L, cs(stream)));
 }
 
@@ -208,7 +220,8 @@ q8_status q8_linear_prepare_operand(const int8_t* x, int64_t M, int64_t K,
   if (st != Q8_OK) return st;
   return cuda_status(q8::launch_rows_to_bf16(x, M, K, K, input_zero_point,
                                              static_cast<__nv_bfloat16*>(operand),
-                                             round_up(K, kTileK), cs(stream)));
+                                             round_up(K, kTileK), cs(stream),
+                                             operand_bound_word(operand, M, K)));
 }
 
 q8_status q8_quantize_to_linear_operand(const float* x_f32, int64_t M, int64_t K,
@@ -223,7 +236,8 @@ q8_status q8_quantize_to_linear_operand(const float* x_f32, int64_t M, int64_t K
   if (st != Q8_OK) return st;
   return cuda_status(q8::launch_quantize_rows_bf16(
       x_f32, M, K, recip_f32(input_scale), input_zero_point, x_q,
-      static_cast<__nv_bfloat16*>(operand), round_up(K, kTileK), cs(stream)));
+      static_cast<__nv_bfloat16*>(operand), round_up(K, kTileK), cs(stream),
+      operand_bound_word(operand, M, K)));
 }
 
 static q8_status run_operand_packed(const void* operand, int64_t M, int64_t K, double input_scale,
@@ -244,6 +258,8 @@ static q8_status run_operand_packed(const void* operand, int64_t M, int64_t K, d
   L.rq = make_rq(input_scale, output_scale, ozp);
   L.out = out;
   L.acc_out = acc_out;
+  L.a_bound_dev = operand_bound_word(const_cast<void*>(operand), M, K);
+  L.a_bound_host = 255;
   return cuda_status(q8::launch_tc_linear(L, cs(stream)));
 }
 
@@ -382,6 +398,7 @@ static q8_status conv_t_common(const int8_t* x, const q8_conv2d_transposed_shape
   C.rq = make_rq(input_scale, output_scale, ozp);
   C.out = out;
   C.acc_out = acc_out;
+  C.a_bound = a_bound_of(izp);
   return cuda_status(q8::launch_tc_conv_t(C, cs(stream)));
 }
 

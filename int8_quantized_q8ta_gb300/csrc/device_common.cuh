@@ -20,6 +20,7 @@ struct Requant {
   float s_in;     // (float)input_scale
   float inv_out;  // (float)(1.0 / output_scale), formed on the host in double
   float ozp;      // output zero point, exactly representable
+  int32_t ozp_i;  // the same zero point as an integer
 };
 
 __device__ __forceinline__ int8_t round_add_clamp(float u, float zp) {
@@ -29,13 +30,43 @@ __device__ __forceinline__ int8_t round_add_clamp(float u, float zp) {
   return (int8_t)__float2int_rz(t);
 }
 
-__device__ __forceinline__ int8_t requant_one(int32_t acc, float ws, float b, const Requant& rq) {
+// clamp(rint(u) + zp, -128, 127) with rint half-to-even, as an int32, on
+// plain FP32/INT32 ALU operations (no float<->int conversion instruction):
+//  * u is first clamped to [-2^21, 2^21]; any u beyond that saturates the
+//    result anyway, and fmaxf maps NaN to -2^21, i.e. -128 -- the same value
+//    round_add_clamp gives for NaN;
+//  * adding 1.5 * 2^23 rounds to an integer (round-to-nearest-even: the sum
+//    lies in [2^23, 2^24), where the spacing of floats is exactly 1), and the
+//    integer is the low bits of the sum's encoding: bits(sum) - 0x4B400000.
+// Equal to round_add_clamp for every float u and every zp in [-128, 127].
+__device__ __forceinline__ int32_t round_add_clamp_i(float u, int32_t zp) {
+  const float c = fminf(fmaxf(u, -2097152.0f), 2097152.0f);
+  const float y = __fadd_rn(c, 12582912.0f);
+  const int32_t q = __float_as_int(y) - (0x4B400000 - zp);
+  return min(max(q, -128), 127);
+}
+
+// The fused epilogue of one accumulator, in the order of "Add q8ta_linear op"
+// (Solution paragraph): ((acc * input_scale) * weight_scale + bias) *
+// (1 / output_scale), rounded, plus the output zero point, clamped.
+__device__ __forceinline__ int32_t requant_i(int32_t acc, float ws, float b, const Requant& rq) {
   float a = __int2float_rn(acc);
   float t = __fmul_rn(a, rq.s_in);
   t = __fmul_rn(t, ws);
   float v = __fadd_rn(t, b);
   float u = __fmul_rn(v, rq.inv_out);
-  return round_add_clamp(u, rq.ozp);
+  return round_add_clamp_i(u, rq.ozp_i);
+}
+
+__device__ __forceinline__ int8_t requant_one(int32_t acc, float ws, float b, const Requant& rq) {
+  return static_cast<int8_t>(requant_i(acc, ws, b, rq));
+}
+
+// Four values in [-128, 127] as bytes 0..3 of a word.
+__device__ __forceinline__ uint32_t pack4_i(int32_t a, int32_t b, int32_t c, int32_t d) {
+  const uint32_t lo = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040);
+  const uint32_t hi = __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040);
+  return __byte_perm(lo, hi, 0x5410);
 }
 
 __device__ __forceinline__ uint32_t pack4(int8_t a, int8_t b, int8_t c, int8_t d) {

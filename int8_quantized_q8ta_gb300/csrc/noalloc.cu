@@ -13,6 +13,7 @@
 // (16 MiB), held on every GPU that loads this library until the process
 // exits.  It holds the two bf16 operand copies q8_linear's tensor-core path
 // needs (x - input_zero_point and the weight, K rounded up to 64).
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -98,6 +99,9 @@ extern "C" q8_status q8_linear_noalloc(const int8_t* x, int64_t M, int64_t K, do
   L.rq.s_in = static_cast<float>(input_scale);
   L.rq.inv_out = static_cast<float>(1.0 / output_scale);
   L.rq.ozp = static_cast<float>(output_zero_point);
+  L.rq.ozp_i = output_zero_point;
+  // largest |x - input_zero_point| over int8 x: sets the exact f32 chunk length
+  L.a_bound_host = std::max(128 + input_zero_point, 127 - input_zero_point);
   L.out = out;
   return q8::launch_tc_linear(L, s) == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }

@@ -30,13 +30,17 @@ cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w
                         const float* ws, const float* bias, Requant rq, int8_t* out,
                         cudaStream_t s);
 // dst[r, k] = bf16(src[r*ld + k] - zp) for k < K, 0 for K <= k < Kp.
+// When bound_word is non-null, one thread also stores there the largest
+// |x - zp| an int8 x can give, max(128 + zp, 127 - zp): the operand's bound
+// read by the GEMM (see TcLinear::a_bound).
 cudaError_t launch_rows_to_bf16(const int8_t* src, int64_t rows, int64_t K, int64_t ld, int32_t zp,
-                                __nv_bfloat16* dst, int64_t Kp, cudaStream_t s);
+                                __nv_bfloat16* dst, int64_t Kp, cudaStream_t s,
+                                int32_t* bound_word = nullptr);
 // Fused quantize of fp32 rows: q = quantize(x) (written to xq when non-null)
 // and dst[r, k] = bf16(q - zp), zero-padded to Kp.
 cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, float inv_scale,
                                       int32_t zp, int8_t* xq, __nv_bfloat16* dst, int64_t Kp,
-                                      cudaStream_t s);
+                                      cudaStream_t s, int32_t* bound_word = nullptr);
 // dst[n, h, w, c] = bf16(x[n, c, h, w] - zp) for c < C, 0 for C <= c < Cp.
 cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t C, int64_t H, int64_t W,
                                      int32_t zp, __nv_bfloat16* dst, int64_t Cp, cudaStream_t s);
@@ -54,6 +58,12 @@ struct TcLinear {
   Requant rq;
   int8_t* out;       // [M, N] (or null when acc_out is set)
   int32_t* acc_out;  // [M, N] int32 debug output, or null
+  // Largest |x - input_zero_point| of the operand: read on the device from
+  // a_bound_dev when that is non-null (an operand prepared by an earlier
+  // launch), else a_bound_host.  It sets how many k-blocks one exact f32
+  // chunk may hold (255, the int8 worst case, gives 8).
+  const int32_t* a_bound_dev;
+  int a_bound_host;
 };
 cudaError_t launch_tc_linear(const TcLinear& p, cudaStream_t s);
 
@@ -67,6 +77,7 @@ struct TcConvT {
   Requant rq;
   int8_t* out;       // [N, OC, H_out, W_out]
   int32_t* acc_out;  // int32 debug output, or null
+  int a_bound;       // largest |x - input_zero_point| (see TcLinear)
 };
 cudaError_t launch_tc_conv_t(const TcConvT& p, cudaStream_t s);
 

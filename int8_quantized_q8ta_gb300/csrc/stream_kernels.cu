@@ -262,7 +262,9 @@ __device__ __forceinline__ int64_t kblocked_index16(int64_t r, int64_t k0, int64
 __global__ void __launch_bounds__(256) rows_to_bf16_kernel(const int8_t* __restrict__ src,
                                                            int64_t rows, int64_t K, int64_t ld,
                                                            int32_t zp, uint4* __restrict__ dst,
-                                                           int64_t Kp) {
+                                                           int64_t Kp, int32_t* bound_word) {
+  if (bound_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+    *bound_word = max(128 + zp, 127 - zp);
   const int64_t per_row = Kp / 8;
   const int64_t total = rows * per_row;
   const bool vec8 = (K % 8 == 0) && (ld % 8 == 0) && (reinterpret_cast<uintptr_t>(src) % 8 == 0);
@@ -293,18 +295,21 @@ __global__ void __launch_bounds__(256) rows_to_bf16_kernel(const int8_t* __restr
 }
 
 cudaError_t launch_rows_to_bf16(const int8_t* src, int64_t rows, int64_t K, int64_t ld, int32_t zp,
-                                __nv_bfloat16* dst, int64_t Kp, cudaStream_t s) {
+                                __nv_bfloat16* dst, int64_t Kp, cudaStream_t s,
+                                int32_t* bound_word) {
   if (rows == 0) return cudaSuccess;
   const int64_t items = rows * (Kp / 8);
   rows_to_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
-      src, rows, K, ld, zp, reinterpret_cast<uint4*>(dst), Kp);
+      src, rows, K, ld, zp, reinterpret_cast<uint4*>(dst), Kp, bound_word);
   return cudaGetLastError();
 }
 
 // Fused quantize of fp32 rows into the GEMM operand (and the int8 op output).
 __global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
     const float* __restrict__ x, int64_t rows, int64_t K, float inv, int32_t zp,
-    int8_t* __restrict__ xq, uint4* __restrict__ dst, int64_t Kp) {
+    int8_t* __restrict__ xq, uint4* __restrict__ dst, int64_t Kp, int32_t* bound_word) {
+  if (bound_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+    *bound_word = max(128 + zp, 127 - zp);
   const int64_t per_row = Kp / 8;
   const int64_t total = rows * per_row;
   const float zpf = static_cast<float>(zp);
@@ -353,11 +358,12 @@ __global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
 }
 
 cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, float inv, int32_t zp,
-                                      int8_t* xq, __nv_bfloat16* dst, int64_t Kp, cudaStream_t s) {
+                                      int8_t* xq, __nv_bfloat16* dst, int64_t Kp, cudaStream_t s,
+                                      int32_t* bound_word) {
   if (rows == 0) return cudaSuccess;
   const int64_t items = rows * (Kp / 8);
   quantize_rows_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
-      x, rows, K, inv, zp, xq, reinterpret_cast<uint4*>(dst), Kp);
+      x, rows, K, inv, zp, xq, reinterpret_cast<uint4*>(dst), Kp, bound_word);
   return cudaGetLastError();
 }
 

@@ -83,6 +83,8 @@ cudaError_t launch_tc_conv_t(const TcConvT& C, cudaStream_t s) {
   p.rq = C.rq;
   p.out = C.out;
   p.acc_out = C.acc_out;
+  p.a_bound_dev = nullptr;
+  p.a_bound_host = C.a_bound;
   p.store_mode = 0;
   // Whole output rows go through shared memory when a unit's rows fit the
   // stage and split into aligned 16-byte pieces.

@@ -8,12 +8,14 @@
 // How, on GB300: tcgen05 has no integer MMA on sm_103a, so the operands are
 // bf16 copies of the integers: x - input_zero_point lies in [-255, 255] and
 // w in [-128, 127], both exact in bf16, and every product (|p| <= 32640) is
-// exact in the f32 accumulator.  The K loop is cut into chunks of 512 so the
-// f32 partial sum of a chunk stays below 2^24 in magnitude (512 * 32640 <
-// 2^24) and is therefore an exact integer; each chunk's TMEM accumulator is
-// drained by the epilogue warps into int32 registers (exact conversion) while
-// the MMA warp already fills the other TMEM buffer.  Integer addition of the
-// chunk sums is exact (modulo 2^32, like the pages' i32 accumulator).
+// exact in the f32 accumulator.  The K loop is cut into chunks whose f32
+// partial sums stay within 2^24 in magnitude and are therefore exact
+// integers: at most 2048 / b k-blocks of 64, b = max(128 + zp, 127 - zp)
+// being the largest |x - zp| (8 k-blocks = 512 products for b = 255, 16 for
+// zp = 0).  Each chunk's TMEM accumulator is drained by the epilogue warps
+// into int32 registers (exact conversion) while the MMA warp already fills
+// the other TMEM buffer.  Integer addition of the chunk sums is exact
+// (modulo 2^32, like the pages' i32 accumulator).
 //
 // Transposed convolution is an implicit GEMM per stride phase: outputs with
 // oh % stride_h == ph and ow % stride_w == pw all use the same taps
@@ -65,7 +67,12 @@ enum : uint32_t {
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 constexpr int kBM = 128;
 constexpr int kBK = 64;             // bf16 per 128-byte row
-constexpr int kChunkKb = 8;         // 8 x 64 = 512 products per exact f32 chunk
+// Exact f32 chunks: a chunk of c k-blocks sums c * 64 products of magnitude
+// at most a_bound * 128 (|x - zp| <= a_bound, |w| <= 128), which stays an
+// exact integer in f32 while c * 64 * a_bound * 128 <= 2^24, i.e.
+// c <= 2048 / a_bound: 8 k-blocks for the int8 worst case a_bound = 255,
+// 16 for a zero point of 0 (a_bound = 128).
+constexpr int kMaxChunkKb = 16;
 constexpr int kMaxStages = 8;
 constexpr int kMaxPhases = 16;
 constexpr int kMaxEpiWarps = 16;
@@ -98,7 +105,17 @@ struct TcParams {
   int32_t* acc_out;
   int store_mode;    // linear int8 stores: 2 = 16 B, 1 = 4 B, 0 = bytes
   uint32_t* err;     // the library's device error word
+  const int32_t* a_bound_dev;  // largest |x - zp| of A, on the device (or null)
+  int a_bound_host;            // the same, when a_bound_dev is null
 };
+
+// Ring stages per exact f32 chunk (see kMaxChunkKb), from A's bound.
+__device__ __forceinline__ int chunk_stages(const TcParams& p, int kd) {
+  int bound = p.a_bound_dev != nullptr ? __ldg(p.a_bound_dev) : p.a_bound_host;
+  if (bound < 1 || bound > 255) bound = 255;  // anything else: the int8 worst case
+  const int kb = min(kMaxChunkKb, 2048 / bound);
+  return max(1, kb / kd);
+}
 
 struct TileInfo {
   int num_kb;   // k-blocks of the tile
@@ -241,8 +258,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 "per-warp scale/bias slices exceed Ctl::ep");
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM * CG, BN);
   constexpr bool kPair = (CG == 2);
-  constexpr int kChunkStages = kChunkKb / KD;   // exact-f32 chunk, in ring stages
-  static_assert(kChunkKb % KD == 0, "a chunk holds whole stages");
+  static_assert(8 % KD == 0, "the worst-case chunk holds whole stages");
   constexpr uint32_t kStageBytes = static_cast<uint32_t>(KD) * (kABytes + kBBytes);
   const int S = p.stages;
 
@@ -261,6 +277,8 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
   // persistent loop over units: a CTA pair walks the units together
   const int unit0 = static_cast<int>(blockIdx.x) / CG;
   const int unit_step = static_cast<int>(gridDim.x) / CG;
+  // exact-f32 chunk length in ring stages (MMA issuer and epilogue agree)
+  const int chunk_st = chunk_stages(p, KD);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -374,8 +392,8 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       for (int u = unit0; u < p.total_units && ok; u += unit_step) {
         for (int j = 0; j < p.subtiles && ok; ++j) {
           const TileInfo ti = decode_tile<MODE, CG, KD>(p, u, j, rank);
-          // chunks of kChunkStages stages: at most kChunkKb k-blocks each
-          for (int st0 = 0; st0 < ti.nstages && ok; st0 += kChunkStages) {
+          // chunks of chunk_st stages (at most 2048 / a_bound k-blocks each)
+          for (int st0 = 0; st0 < ti.nstages && ok; st0 += chunk_st) {
             const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
             if (!wait_bar(smem_u32(&ctl->acc_empty[buf]), (use & 1u) ^ 1u, abort_flag,
                           kErrWaitAccEmpty, p.err)) {
@@ -384,7 +402,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
             }
             tc_fence_after();
             const uint32_t d = tmem_base + buf * kAccStride;
-            const int st_end = min(st0 + kChunkStages, ti.nstages);
+            const int st_end = min(st0 + chunk_st, ti.nstages);
             for (int st = st0; st < st_end; ++st) {
               if (!wait_bar(smem_u32(&ctl->full[stage]), phase, abort_flag, kErrWaitFull, p.err)) {
                 ok = false;
@@ -458,12 +476,16 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
         //     output-channel block changes (for OC <= BN: once per CTA).
         const float* sws;
         const float* sbs;
+        // linear: this thread's column scale and bias, loaded now and
+        // written to shared memory after the accumulator drains, so the
+        // load latency is spent there
+        float ld_ws = 0.0f, ld_b = 0.0f;
+        float* ws_buf = ctl->ep + tile_par * (2 * kMaxBN);
         if constexpr (MODE == 0) {
-          float* ws_buf = ctl->ep + tile_par * (2 * kMaxBN);
           if (p.acc_out == nullptr && et < BN) {
             const int gc = gcolbase + et;
-            ws_buf[et] = (gc < ncols) ? __ldg(p.ws + gc) : 0.0f;
-            ws_buf[kMaxBN + et] = (gc < ncols && p.bias) ? __ldg(p.bias + gc) : 0.0f;
+            ld_ws = (gc < ncols) ? __ldg(p.ws + gc) : 0.0f;
+            ld_b = (gc < ncols && p.bias) ? __ldg(p.bias + gc) : 0.0f;
           }
           sws = ws_buf + col0;
           sbs = ws_buf + kMaxBN + col0;
@@ -488,7 +510,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
         int32_t sum[kColsPerWarp];
 #pragma unroll
         for (int c = 0; c < kColsPerWarp; ++c) sum[c] = 0;
-        for (int st0 = 0; st0 < ti.nstages; st0 += kChunkStages) {
+        for (int st0 = 0; st0 < ti.nstages; st0 += chunk_st) {
           const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
           bool got = true;
           if (lane == 0)
@@ -530,6 +552,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
 
         // ---- fused epilogue
         if constexpr (MODE == 0) {
+          if (p.acc_out == nullptr && et < BN) {
+            ws_buf[et] = ld_ws;
+            ws_buf[kMaxBN + et] = ld_b;
+          }
           if (p.acc_out == nullptr && !epi_sync(ctl, epi_phase, abort_flag, p.err)) {
             ok = false;
             break;
@@ -559,10 +585,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                   const float4 w4 = *reinterpret_cast<const float4*>(sws + 16 * g + 4 * q);
                   const float4 b4 = *reinterpret_cast<const float4*>(sbs + 16 * g + 4 * q);
                   const int s0 = 16 * g + 4 * q;
-                  wds[q] = pack4(requant_one(sum[s0 + 0], w4.x, b4.x, p.rq),
-                                 requant_one(sum[s0 + 1], w4.y, b4.y, p.rq),
-                                 requant_one(sum[s0 + 2], w4.z, b4.z, p.rq),
-                                 requant_one(sum[s0 + 3], w4.w, b4.w, p.rq));
+                  wds[q] = pack4_i(requant_i(sum[s0 + 0], w4.x, b4.x, p.rq),
+                                   requant_i(sum[s0 + 1], w4.y, b4.y, p.rq),
+                                   requant_i(sum[s0 + 2], w4.z, b4.z, p.rq),
+                                   requant_i(sum[s0 + 3], w4.w, b4.w, p.rq));
                 }
                 if (p.store_mode == 2 && c + 16 <= p.N) {
                   *reinterpret_cast<uint4*>(dst + c) = make_uint4(wds[0], wds[1], wds[2], wds[3]);

@@ -42,6 +42,8 @@ int pick_pair_bn(int64_t M, int64_t N, int pairs) {
 cudaError_t launch_tc_linear(const TcLinear& L, cudaStream_t s) {
   const bool pair = L.M > kBM && L.N > 128;
   const int cg = pair ? 2 : 1;
+  // two k-blocks per TMA box on pairs: one k-block per box measured slower
+  // (the per-box cost of the TMA unit, not bytes, sets the feed rate)
   const int kd = pair ? 2 : 1;
   const int bn = pair ? pick_pair_bn(L.M, L.N, device_sm_count() / 2) : pick_bn(L.N);
   const uint64_t kblocks = static_cast<uint64_t>(L.Kp / kBK);
@@ -76,6 +78,8 @@ cudaError_t launch_tc_linear(const TcLinear& L, cudaStream_t s) {
   p.rq = L.rq;
   p.out = L.out;
   p.acc_out = L.acc_out;
+  p.a_bound_dev = L.a_bound_dev;
+  p.a_bound_host = L.a_bound_host;
   const uintptr_t oa = reinterpret_cast<uintptr_t>(L.out);
   p.store_mode = (L.N % 16 == 0 && oa % 16 == 0) ? 2 : (oa % 4 == 0 ? 1 : 0);
   if (p.total_units == 0) return cudaSuccess;

@@ -88,7 +88,8 @@ def test_linear_workspace_and_gemv_shape_guards():
 def test_workspace_sizes():
     # bf16 copies padded to a multiple of 64 along K, 256-byte aligned
     assert lib.q8_linear_packed_weight_bytes(11008, 4096) == 11008 * 4096 * 2
-    assert lib.q8_linear_operand_bytes(2048, 4096) == 2048 * 4096 * 2
+    # operand: the bf16 data plus a 256-byte trailer holding its |x - zp| bound
+    assert lib.q8_linear_operand_bytes(2048, 4096) == 2048 * 4096 * 2 + 256
     assert lib.q8_linear_packed_weight_bytes(4, 70) == (4 * 128 * 2 + 255) // 256 * 256
     s = q8.conv_t_shape((8, 256, 64, 64), (128, 2304), 3, 3, 128, 128, 2, 1, 1)
     assert lib.q8_conv2d_transposed_workspace_bytes(ctypes.byref(s)) == \

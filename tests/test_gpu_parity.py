@@ -188,6 +188,41 @@ def test_acc32_exact_at_the_chunk_bound():
     np.testing.assert_array_equal(got, oracle.linear_acc(x, 127, w))
 
 
+@pytest.mark.parametrize("izp", [0, 1, -1, -5, 64, -100])
+def test_acc32_exact_at_the_zero_point_chunk_bound(izp):
+    """The exact f32 chunk holds floor(2048 / b) k-blocks for b = max(128 +
+    zp, 127 - zp), the largest |x - zp|: with every |x - zp| = b and w = -128
+    each chunk reaches its largest sum (2^24 exactly for zp = 0).  Rows past
+    the first 64 mix in random values so low-order bits sit next to it."""
+    M, K, N = 256, 4096 + 64, 256
+    xe = -128 if izp >= 0 else 127
+    x = np.full((M, K), xe, np.int8)
+    w = np.full((N, K), -128, np.int8)
+    x[64:, :] = synth.int8_uniform(11, "bx", (M - 64, K), -128, 127)
+    x[64:, ::97] = xe
+    w[128:, :] = synth.int8_uniform(12, "bw", (N - 128, K), -128, 127)
+    packed = q8.pack_weight(T(w))
+    ref = oracle.linear_acc(x, izp, w)
+    np.testing.assert_array_equal(H(q8.linear_packed_acc32(T(x), izp, packed)), ref)
+    operand = q8.prepare_operand(T(x), izp)
+    ws = np.full(N, 2.0 ** -12, np.float32)
+    got = H(q8.linear_operand_packed(operand, 1.0, packed, T(ws), None, 1.0, 0))
+    np.testing.assert_array_equal(got, oracle.linear(x, 1.0, izp, w, ws, None, 1.0, 0))
+
+
+def test_conv_t_acc32_exact_at_the_chunk_bound():
+    """Transposed convolution with |x - zp| = 128 (zp = 0) and w = -128 over
+    9 taps x 512 channels: every exact chunk of 1024 products sums to 2^24."""
+    N, IC, H_in, W_in, OC, K = 1, 512, 8, 8, 64, 3
+    x = np.full((N, IC, H_in, W_in), -128, np.int8)
+    w = np.full((OC, K * K * IC), -128, np.int8)
+    w[32:, :] = synth.int8_uniform(13, "cw", (OC - 32, K * K * IC), -128, 127)
+    H_out, W_out = synth.output_hw(H_in, W_in, K, K, 1, 1, 1, 1, 0, 0)
+    ref = oracle.conv2d_transposed_acc(x, 0, w, K, K, H_out, W_out, (1, 1), (1, 1))
+    got = H(q8.conv2d_transposed_acc32(T(x), 0, T(w), K, (H_out, W_out), stride=1, padding=1))
+    np.testing.assert_array_equal(got, ref)
+
+
 # --------------------------------------------------------------- conv_t
 
 def _conv_case(seed, N, IC, H_in, W_in, OC, K, s, p, op, izp, ozp, out_hw=None):

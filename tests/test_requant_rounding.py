@@ -1,0 +1,59 @@
+"""The CUDA epilogue's conversion-free rounding equals the plain one (CPU).
+
+The GEMM and gemv epilogues compute clamp(rint(u) + zp, -128, 127) without a
+float->int conversion instruction: u is clamped to [-2^21, 2^21], 1.5 * 2^23
+is added in f32 (round to nearest even), and the integer is read from the
+sum's encoding.  This test replays both forms in numpy float32 -- whose
+addition rounds to nearest even like the GPU's __fadd_rn -- over every
+rounding tie near the int8 range, their float neighbours, random bit
+patterns (NaN, infinities, subnormals included) and every zero point.
+"""
+import numpy as np
+
+F = np.float32
+
+
+def plain(u, zp):
+    """rint half-to-even, + zp in f32, clamp, truncate (NaN -> -128 through
+    fmaxf's choice of the non-NaN operand)."""
+    r = np.rint(u).astype(F)
+    t = (r + F(zp)).astype(F)
+    t = np.where(np.isnan(t), F(-128.0), t)
+    t = np.minimum(np.maximum(t, F(-128.0)), F(127.0))
+    return t.astype(np.int32)
+
+
+def alu_only(u, zp):
+    c = np.where(np.isnan(u), F(-2097152.0), u).astype(F)      # fmaxf(NaN, c) = c
+    c = np.minimum(np.maximum(c, F(-2097152.0)), F(2097152.0)).astype(F)
+    y = (c + F(12582912.0)).astype(F)
+    q = y.view(np.int32).astype(np.int64) - (0x4B400000 - zp)
+    return np.clip(q, -128, 127).astype(np.int32)
+
+
+def _samples():
+    ties = np.arange(-400, 400, dtype=np.float64) + 0.5
+    ints = np.arange(-400, 400, dtype=np.float64)
+    base = np.concatenate([ties, ints]).astype(F)
+    up = np.nextafter(base, F(np.inf))
+    down = np.nextafter(base, F(-np.inf))
+    big = np.array([2.0 ** 21, 2.0 ** 21 + 0.5, 2.0 ** 22, 2.0 ** 23, 2.0 ** 24, 3.4e38, 1e30,
+                    4194303.5, 8388607.5, 12582912.0], dtype=np.float64)
+    big = np.concatenate([big, -big]).astype(F)
+    special = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-45, -1e-45, 1e-38], dtype=F)
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 2 ** 32, size=200_000, dtype=np.uint64).astype(np.uint32).view(F)
+    scaled = (rng.standard_normal(200_000) * 150.0).astype(F)
+    return np.concatenate([base, up, down, big, special, bits, scaled])
+
+
+def test_alu_rounding_matches_rint_add_clamp_for_every_zero_point():
+    u = _samples()
+    with np.errstate(invalid="ignore", over="ignore"):
+        for zp in range(-128, 128):
+            np.testing.assert_array_equal(alu_only(u, zp), plain(u, zp), err_msg=f"zp={zp}")
+
+
+def test_ties_round_to_even():
+    u = np.array([0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5, -127.5], dtype=F)
+    assert alu_only(u, 0).tolist() == [0, 2, 2, 0, -2, -2, 126, -128]
