@@ -90,8 +90,12 @@ def test_gemv_1x4096x4096_full():
     np.testing.assert_array_equal(got2, ref)
 
 
+# K % 16 == 0 takes 16-byte loads (up to K = 16384 here, N = 36 and 1004
+# leaving partial blocks of four rows), K % 4 == 0 4-byte loads.
 @pytest.mark.parametrize("K,N,izp", [(4, 4, 0), (20, 8, -128), (64, 36, 127), (100, 12, 5),
-                                     (4096 + 16, 8, -7), (1028, 40, 3)])
+                                     (4096 + 16, 8, -7), (1028, 40, 3), (16, 4, 0),
+                                     (2048, 1004, 3), (4096 + 64, 300, 17), (8192, 20, -100),
+                                     (12288, 8, -128), (16384, 12, 127)])
 def test_gemv_ragged(K, N, izp):
     p = dict(ws_lo=0.002, ws_hi=0.01, b_mean=0.0, b_var=0.1)
     x, w, ws, b = synth.linear_inputs(K + N, 1, K, N, x_kind="int8", p=p)
