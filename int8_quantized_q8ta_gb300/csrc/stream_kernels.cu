@@ -32,6 +32,26 @@ static int stream_grid(int64_t work_items, int threads, int blocks_per_sm) {
   return static_cast<int>(std::max<int64_t>(1, std::min(want, cap)));
 }
 
+// Grid of a grid-stride kernel: no more blocks than fit on the GPU at once
+// (its occupancy at `threads`), so every block starts in the first wave and
+// no late partial wave stretches the tail.  The occupancy query is made once
+// per kernel and device (`cache` is the call site's own table).
+template <typename Kernel>
+static int resident_grid(Kernel kernel, int (&cache)[64], int64_t work_items, int threads) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 4;
+    }
+    cache[dev] = per_sm;
+  }
+  return stream_grid(work_items, threads, cache[dev]);
+}
+
 // ---------------------------------------------------------------------------
 // quantize_per_tensor ("Add quantize_per_tensor op", Solution paragraph):
 // q = clamp(rint(x * inv_scale) + zp, -128, 127).
@@ -81,7 +101,8 @@ cudaError_t launch_quantize(const float* x, int64_t numel, float inv, float zp, 
   if (vec) {
     constexpr int U = 4;
     const int64_t n4 = numel / 4;
-    const int grid = stream_grid((n4 + U - 1) / U, 256, 8);
+    static int occ[64];
+    const int grid = resident_grid(quantize_vec_kernel<U>, occ, (n4 + U - 1) / U, 256);
     quantize_vec_kernel<U><<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(x), n4, inv, zp,
                                                 reinterpret_cast<uint32_t*>(out));
   } else {
@@ -305,55 +326,77 @@ cudaError_t launch_rows_to_bf16(const int8_t* src, int64_t rows, int64_t K, int6
 }
 
 // Fused quantize of fp32 rows into the GEMM operand (and the int8 op output).
+// An item is 8 consecutive elements of a row; each thread loads U items
+// (U * 32 bytes) before converting any of them.  Idx is the index type:
+// 32-bit when the item count allows (integer division is a long sequence of
+// instructions, four times longer in 64 bits).
+template <int U, typename Idx>
 __global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
-    const float* __restrict__ x, int64_t rows, int64_t K, float inv, int32_t zp,
-    int8_t* __restrict__ xq, uint4* __restrict__ dst, int64_t Kp, int32_t* bound_word) {
+    const float* __restrict__ x, Idx rows, Idx K, float inv, int32_t zp,
+    int8_t* __restrict__ xq, uint4* __restrict__ dst, Idx Kp, int32_t* bound_word) {
   if (bound_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
     *bound_word = max(128 + zp, 127 - zp);
-  const int64_t per_row = Kp / 8;
-  const int64_t total = rows * per_row;
+  const Idx per_row = Kp / 8;
+  const Idx total = rows * per_row;
   const float zpf = static_cast<float>(zp);
   const bool vec = (K % 8 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                    (xq == nullptr || reinterpret_cast<uintptr_t>(xq) % 8 == 0);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / per_row;
-    const int64_t k0 = (i - r * per_row) * 8;
-    int8_t q[8];
-    int v[8];
-    if (vec && k0 + 8 <= K) {
-      const float4* xp = reinterpret_cast<const float4*>(x + r * K + k0);
-      const float4 a = __ldcs(xp), b = __ldcs(xp + 1);
-      q[0] = quantize_one(a.x, inv, zpf); q[1] = quantize_one(a.y, inv, zpf);
-      q[2] = quantize_one(a.z, inv, zpf); q[3] = quantize_one(a.w, inv, zpf);
-      q[4] = quantize_one(b.x, inv, zpf); q[5] = quantize_one(b.y, inv, zpf);
-      q[6] = quantize_one(b.z, inv, zpf); q[7] = quantize_one(b.w, inv, zpf);
-      if (xq) {
-        uint2 o;
-        o.x = pack4(q[0], q[1], q[2], q[3]);
-        o.y = pack4(q[4], q[5], q[6], q[7]);
-        *reinterpret_cast<uint2*>(xq + r * K + k0) = o;
-      }
+  const Idx step = static_cast<Idx>(gridDim.x) * blockDim.x * U;
+  for (Idx base = static_cast<Idx>(blockIdx.x) * blockDim.x * U + threadIdx.x; base < total;
+       base += step) {
+    float4 va[U], vb[U];
+    Idx rr[U], kk[U];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = static_cast<int>(q[j]) - zp;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (k0 + j < K) {
-          q[j] = quantize_one(x[r * K + k0 + j], inv, zpf);
-          if (xq) xq[r * K + k0 + j] = q[j];
-          v[j] = static_cast<int>(q[j]) - zp;
-        } else {
-          v[j] = 0;
-        }
+    for (int u = 0; u < U; ++u) {
+      const Idx i = base + static_cast<Idx>(u) * blockDim.x;
+      rr[u] = i / per_row;
+      kk[u] = (i - rr[u] * per_row) * 8;
+      if (vec && i < total && kk[u] + 8 <= K) {
+        const float4* xp = reinterpret_cast<const float4*>(x + static_cast<int64_t>(rr[u]) * K + kk[u]);
+        va[u] = __ldcs(xp);
+        vb[u] = __ldcs(xp + 1);
       }
     }
-    uint4 o;
-    o.x = bf16x2_from_ints(v[0], v[1]);
-    o.y = bf16x2_from_ints(v[2], v[3]);
-    o.z = bf16x2_from_ints(v[4], v[5]);
-    o.w = bf16x2_from_ints(v[6], v[7]);
-    dst[kblocked_index16(r, k0, rows)] = o;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const Idx i = base + static_cast<Idx>(u) * blockDim.x;
+      if (i >= total) break;
+      const int64_t r = rr[u];
+      const int64_t k0 = kk[u];
+      int8_t q[8];
+      int v[8];
+      if (vec && k0 + 8 <= K) {
+        q[0] = quantize_one(va[u].x, inv, zpf); q[1] = quantize_one(va[u].y, inv, zpf);
+        q[2] = quantize_one(va[u].z, inv, zpf); q[3] = quantize_one(va[u].w, inv, zpf);
+        q[4] = quantize_one(vb[u].x, inv, zpf); q[5] = quantize_one(vb[u].y, inv, zpf);
+        q[6] = quantize_one(vb[u].z, inv, zpf); q[7] = quantize_one(vb[u].w, inv, zpf);
+        if (xq) {
+          uint2 o;
+          o.x = pack4(q[0], q[1], q[2], q[3]);
+          o.y = pack4(q[4], q[5], q[6], q[7]);
+          *reinterpret_cast<uint2*>(xq + r * K + k0) = o;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = static_cast<int>(q[j]) - zp;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (k0 + j < K) {
+            q[j] = quantize_one(x[r * K + k0 + j], inv, zpf);
+            if (xq) xq[r * K + k0 + j] = q[j];
+            v[j] = static_cast<int>(q[j]) - zp;
+          } else {
+            v[j] = 0;
+          }
+        }
+      }
+      uint4 o;
+      o.x = bf16x2_from_ints(v[0], v[1]);
+      o.y = bf16x2_from_ints(v[2], v[3]);
+      o.z = bf16x2_from_ints(v[4], v[5]);
+      o.w = bf16x2_from_ints(v[6], v[7]);
+      dst[kblocked_index16(r, k0, static_cast<int64_t>(rows))] = o;
+    }
   }
 }
 
@@ -362,85 +405,79 @@ cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, f
                                       int32_t* bound_word) {
   if (rows == 0) return cudaSuccess;
   const int64_t items = rows * (Kp / 8);
-  quantize_rows_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
-      x, rows, K, inv, zp, xq, reinterpret_cast<uint4*>(dst), Kp, bound_word);
+  constexpr int U = 4;
+  if (items + 256 * U < (int64_t(1) << 31)) {
+    static int occ[64];
+    const int grid = resident_grid(quantize_rows_bf16_kernel<U, uint32_t>, occ, (items + U - 1) / U, 256);
+    quantize_rows_bf16_kernel<U, uint32_t><<<grid, 256, 0, s>>>(
+        x, static_cast<uint32_t>(rows), static_cast<uint32_t>(K), inv, zp, xq,
+        reinterpret_cast<uint4*>(dst), static_cast<uint32_t>(Kp), bound_word);
+  } else {
+    static int occ[64];
+    const int grid = resident_grid(quantize_rows_bf16_kernel<U, int64_t>, occ, (items + U - 1) / U, 256);
+    quantize_rows_bf16_kernel<U, int64_t><<<grid, 256, 0, s>>>(
+        x, rows, K, inv, zp, xq, reinterpret_cast<uint4*>(dst), Kp, bound_word);
+  }
   return cudaGetLastError();
 }
 
 // NCHW int8 -> channel-blocked NHWC bf16 (x - zp): dst[n][c/64][h][w][c%64],
 // channels zero-padded to Cp (padding channels are exactly 0, not -zp), so
-// the (64 channels x w x h) box of one k-block is contiguous along w.  A
-// block transposes a 64-channel x 64-column slab of one (n, h) row through
-// shared memory: 16-byte loads along w, 16-byte stores along c.
-constexpr int kRowsPerBlock = 4;  // (n, h) rows whose loads a block issues together
-
+// the (64 channels x w x h) box of one k-block is contiguous along w.
+// A thread takes 8 channels x 4 columns of one (n, h) row: 8 loads of 4
+// bytes (consecutive threads take consecutive column quads of one channel,
+// so a warp reads whole 32-byte sectors) and 4 stores of 16 bytes (the
+// 8-channel pieces of 4 columns).  No shared memory, no block barrier.
+template <typename Idx>
 __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __restrict__ x,
-                                                                int64_t NH, int64_t C, int64_t H,
+                                                                Idx NH, int64_t C, Idx H,
                                                                 int64_t W, int32_t zp,
                                                                 uint4* __restrict__ dst,
                                                                 int64_t Cp) {
-  __shared__ __align__(16) int8_t tile[64][72];  // [w][c]
-  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 64;
-  const int64_t w0 = static_cast<int64_t>(blockIdx.x) * 64;
-  const bool vec = (W % 16 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
-  const int lc = threadIdx.x >> 2, wseg = threadIdx.x & 3;
-  const int64_t c = c0 + lc;
-  const int64_t wb = w0 + 16 * wseg;
-  for (int64_t nh0 = static_cast<int64_t>(blockIdx.z) * kRowsPerBlock; nh0 < NH;
-       nh0 += static_cast<int64_t>(gridDim.z) * kRowsPerBlock) {
-    // issue every row's loads before transposing any (bytes in flight)
-    int4 raw[kRowsPerBlock];
+  const Idx W4 = static_cast<Idx>((W + 3) / 4);
+  const Idx CB = static_cast<Idx>(Cp / 64);
+  const Idx total = NH * CB * 8 * W4;
+  const bool vec = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 4 == 0);
+  for (Idx i = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<Idx>(gridDim.x) * blockDim.x) {
+    const int64_t w4 = i % W4;
+    Idx rest = i / W4;
+    const int cseg = static_cast<int>(rest % 8);
+    rest /= 8;
+    const int64_t cb = rest % CB;
+    const Idx nhi = rest / CB;
+    const int64_t n = nhi / H, h = nhi - (nhi / H) * H;
+    const int64_t c0 = cb * 64 + 8 * cseg;
+    const int64_t wb = 4 * w4;
+    uint32_t raw[8];
 #pragma unroll
-    for (int r = 0; r < kRowsPerBlock; ++r) {
-      const int64_t nh = nh0 + r;
-      raw[r] = make_int4(0, 0, 0, 0);
-      if (nh < NH && c < C) {
-        const int64_t n = nh / H, h = nh - n * H;
-        const int8_t* src = x + ((n * C + c) * H + h) * W + wb;
-        if (vec && wb + 16 <= W) {
-          raw[r] = __ldcs(reinterpret_cast<const int4*>(src));
+    for (int j = 0; j < 8; ++j) {
+      raw[j] = 0u;
+      if (c0 + j < C) {
+        const int8_t* src = x + ((n * C + c0 + j) * H + h) * W + wb;
+        if (vec) {
+          raw[j] = __ldcs(reinterpret_cast<const unsigned int*>(src));
         } else {
-          uint32_t wd[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (wb + i < W) wd[i >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(src[i])) << (8 * (i & 3));
-          raw[r] = make_int4(static_cast<int>(wd[0]), static_cast<int>(wd[1]), static_cast<int>(wd[2]),
-                             static_cast<int>(wd[3]));
+          for (int q = 0; q < 4; ++q)
+            if (wb + q < W) raw[j] |= static_cast<uint32_t>(static_cast<uint8_t>(src[q])) << (8 * q);
         }
       }
     }
+    uint4* out = dst + (((n * CB + cb) * H + h) * W + wb) * 8 + cseg;
 #pragma unroll
-    for (int r = 0; r < kRowsPerBlock; ++r) {
-      const int64_t nh = nh0 + r;
-      if (nh >= NH) break;
-      const int64_t n = nh / H, h = nh - n * H;
-      __syncthreads();  // the previous row's readers are done with the tile
-      const int32_t rw[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+    for (int q = 0; q < 4; ++q) {
+      if (wb + q >= W) break;
+      int d[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        tile[16 * wseg + i][lc] = static_cast<int8_t>((rw[i >> 2] >> (8 * (i & 3))) & 0xff);
-      __syncthreads();
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int item = threadIdx.x + 256 * k;
-        const int w = item >> 3, cseg = item & 7;
-        const int64_t cc = c0 + 8 * cseg;
-        if (w0 + w < W && cc < Cp) {
-          const uint2 v = *reinterpret_cast<const uint2*>(&tile[w][8 * cseg]);
-          int d[8];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            d[j] = (cc + j < C) ? static_cast<int8_t>((v.x >> (8 * j)) & 0xff) - zp : 0;
-            d[4 + j] = (cc + 4 + j < C) ? static_cast<int8_t>((v.y >> (8 * j)) & 0xff) - zp : 0;
-          }
-          uint4 o;
-          o.x = bf16x2_from_ints(d[0], d[1]);
-          o.y = bf16x2_from_ints(d[2], d[3]);
-          o.z = bf16x2_from_ints(d[4], d[5]);
-          o.w = bf16x2_from_ints(d[6], d[7]);
-          dst[((((n * (Cp / 64) + blockIdx.y) * H + h) * W + w0 + w) * 64 + 8 * cseg) / 8] = o;
-        }
-      }
+      for (int j = 0; j < 8; ++j)
+        d[j] = (c0 + j < C) ? static_cast<int>(static_cast<int8_t>((raw[j] >> (8 * q)) & 0xff)) - zp : 0;
+      uint4 o;
+      o.x = bf16x2_from_ints(d[0], d[1]);
+      o.y = bf16x2_from_ints(d[2], d[3]);
+      o.z = bf16x2_from_ints(d[4], d[5]);
+      o.w = bf16x2_from_ints(d[6], d[7]);
+      out[q * 8] = o;
     }
   }
 }
@@ -448,11 +485,19 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __
 cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t C, int64_t H, int64_t W,
                                      int32_t zp, __nv_bfloat16* dst, int64_t Cp, cudaStream_t s) {
   if (N * H * W == 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>((W + 63) / 64), static_cast<unsigned>(Cp / 64),
-            static_cast<unsigned>(std::min<int64_t>((N * H + kRowsPerBlock - 1) / kRowsPerBlock,
-                                                    65535)));
-  nchw_to_nhwc_bf16_kernel<<<grid, 256, 0, s>>>(x, N * H, C, H, W, zp,
-                                                reinterpret_cast<uint4*>(dst), Cp);
+  const int64_t items = N * H * (Cp / 64) * 8 * ((W + 3) / 4);
+  if (items + 256 < (int64_t(1) << 31)) {
+    static int occ[64];
+    const int grid = resident_grid(nchw_to_nhwc_bf16_kernel<uint32_t>, occ, items, 256);
+    nchw_to_nhwc_bf16_kernel<uint32_t><<<grid, 256, 0, s>>>(
+        x, static_cast<uint32_t>(N * H), C, static_cast<uint32_t>(H), W, zp,
+        reinterpret_cast<uint4*>(dst), Cp);
+  } else {
+    static int occ[64];
+    const int grid = resident_grid(nchw_to_nhwc_bf16_kernel<int64_t>, occ, items, 256);
+    nchw_to_nhwc_bf16_kernel<int64_t><<<grid, 256, 0, s>>>(x, N * H, C, H, W, zp,
+                                                           reinterpret_cast<uint4*>(dst), Cp);
+  }
   return cudaGetLastError();
 }
 
