@@ -41,7 +41,7 @@ def build(force: bool = False) -> str:
 class ConvTShape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "N", "IC", "H_in", "W_in", "OC", "Kh", "Kw", "ldw", "H_out", "W_out",
-        "stride_h", "stride_w", "pad_h", "pad_w", "dil_h", "dil_w")]
+        "stride_h", "stride_w", "pad_h", "pad_w", "dil_h", "dil_w", "groups")]
 
 
 def _load():
@@ -52,18 +52,23 @@ def _load():
             P = ctypes.c_void_p
             I64, I32, D = ctypes.c_int64, ctypes.c_int32, ctypes.c_double
             lib.oracle_quantize_per_tensor.argtypes = [P, I64, D, I32, P]
-            lib.oracle_requantize.argtypes = [P, I64, I64, D, P, P, D, I32, P]
+            lib.oracle_requantize.argtypes = [P, I64, I64, D, P, P, D, I32, ctypes.c_int, P]
             lib.oracle_linear_acc.argtypes = [P, I64, I64, I32, P, I64, I64, P]
-            lib.oracle_linear.argtypes = [P, I64, I64, D, I32, P, I64, I64, P, P, D, I32, P]
+            lib.oracle_linear.argtypes = [P, I64, I64, D, I32, P, I64, I64, P, P, D, I32,
+                                          ctypes.c_int, P]
             SP = ctypes.POINTER(ConvTShape)
             lib.oracle_conv2d_transposed_acc_gather.argtypes = [P, I32, P, SP, P]
             lib.oracle_conv2d_transposed_acc_scatter.argtypes = [P, I32, P, SP, P]
             lib.oracle_conv2d_transposed_acc_scatter.restype = ctypes.c_int
-            lib.oracle_conv2d_transposed.argtypes = [P, D, I32, P, SP, P, P, D, I32, P]
+            lib.oracle_conv2d_transposed.argtypes = [P, D, I32, P, SP, P, P, D, I32, ctypes.c_int,
+                                                     P]
+            lib.oracle_conv2d_acc.argtypes = [P, I32, P, SP, P]
+            lib.oracle_conv2d.argtypes = [P, D, I32, P, SP, P, P, D, I32, ctypes.c_int, P]
             lib.oracle_dequantize_per_tensor.argtypes = [P, I64, D, I32, P]
             for f in ("oracle_quantize_per_tensor", "oracle_requantize", "oracle_linear_acc",
                       "oracle_linear", "oracle_conv2d_transposed_acc_gather",
-                      "oracle_conv2d_transposed", "oracle_dequantize_per_tensor"):
+                      "oracle_conv2d_transposed", "oracle_dequantize_per_tensor",
+                      "oracle_conv2d_acc", "oracle_conv2d"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -95,7 +100,14 @@ def dequantize_per_tensor(q, scale: float, zero_point: int) -> np.ndarray:
     return out
 
 
-def requantize(acc, input_scale, weight_scales, bias, output_scale, output_zero_point):
+def _relu_flag(activation) -> int:
+    if activation not in ("none", "relu"):
+        raise ValueError(f"activation {activation!r}")
+    return 1 if activation == "relu" else 0
+
+
+def requantize(acc, input_scale, weight_scales, bias, output_scale, output_zero_point,
+               activation="none"):
     """The dequant/requant epilogue on an int32 [rows, N] accumulator array."""
     acc = _c(acc, np.int32)
     rows, N = acc.shape
@@ -104,7 +116,7 @@ def requantize(acc, input_scale, weight_scales, bias, output_scale, output_zero_
     out = np.empty((rows, N), np.int8)
     _load().oracle_requantize(_ptr(acc), rows, N, float(input_scale), _ptr(ws),
                               None if b is None else _ptr(b), float(output_scale),
-                              int(output_zero_point), _ptr(out))
+                              int(output_zero_point), _relu_flag(activation), _ptr(out))
     return out
 
 
@@ -121,7 +133,7 @@ def linear_acc(x, input_zero_point, w) -> np.ndarray:
 
 
 def linear(x, input_scale, input_zero_point, w, weight_scales, bias, output_scale,
-           output_zero_point, K=None) -> np.ndarray:
+           output_zero_point, K=None, activation="none") -> np.ndarray:
     """q8ta_linear: int8 [M,K] x int8 [N,K] (row stride may exceed K) -> int8 [M,N]."""
     x = _c(x, np.int8)
     w = _c(w, np.int8)
@@ -134,24 +146,25 @@ def linear(x, input_scale, input_zero_point, w, weight_scales, bias, output_scal
     out = np.empty((M, N), np.int8)
     _load().oracle_linear(_ptr(x), M, K, float(input_scale), int(input_zero_point), _ptr(w), N,
                           ldw, _ptr(ws), None if b is None else _ptr(b), float(output_scale),
-                          int(output_zero_point), _ptr(out))
+                          int(output_zero_point), _relu_flag(activation), _ptr(out))
     return out
 
 
-def _conv_shape(x, w, Kh, Kw, H_out, W_out, stride, pad, dil):
+def _conv_shape(x, w, Kh, Kw, H_out, W_out, stride, pad, dil, groups=1):
     N, IC, H_in, W_in = x.shape
     OC, ldw = w.shape
-    assert ldw >= Kh * Kw * IC
+    assert groups >= 1 and IC % groups == 0 and OC % groups == 0
+    assert ldw >= Kh * Kw * (IC // groups)
     return ConvTShape(N, IC, H_in, W_in, OC, Kh, Kw, ldw, H_out, W_out,
-                      stride[0], stride[1], pad[0], pad[1], dil[0], dil[1])
+                      stride[0], stride[1], pad[0], pad[1], dil[0], dil[1], groups)
 
 
 def conv2d_transposed_acc(x, input_zero_point, w, Kh, Kw, H_out, W_out, stride, pad,
-                          dil=(1, 1), form="gather") -> np.ndarray:
+                          dil=(1, 1), form="gather", groups=1) -> np.ndarray:
     """int32 [N, OC, H_out, W_out] accumulators of the transposed convolution."""
     x = _c(x, np.int8)
     w = _c(w, np.int8)
-    s = _conv_shape(x, w, Kh, Kw, H_out, W_out, stride, pad, dil)
+    s = _conv_shape(x, w, Kh, Kw, H_out, W_out, stride, pad, dil, groups)
     acc = np.empty((s.N, s.OC, H_out, W_out), np.int32)
     lib = _load()
     if form == "gather":
@@ -169,16 +182,44 @@ def conv2d_transposed_acc(x, input_zero_point, w, Kh, Kw, H_out, W_out, stride, 
 
 def conv2d_transposed(x, input_scale, input_zero_point, w, Kh, Kw, weight_scales, bias,
                       output_scale, output_zero_point, H_out, W_out, stride, pad,
-                      dil=(1, 1)) -> np.ndarray:
-    """q8ta_conv2d_transposed: int8 NCHW x, int8 [OC, Kh*Kw*IC] w -> int8 NCHW."""
+                      dil=(1, 1), groups=1, activation="none") -> np.ndarray:
+    """q8ta_conv2d_transposed: int8 NCHW x, int8 [OC, Kh*Kw*IC/groups] w -> int8 NCHW."""
     x = _c(x, np.int8)
     w = _c(w, np.int8)
-    s = _conv_shape(x, w, Kh, Kw, H_out, W_out, stride, pad, dil)
+    s = _conv_shape(x, w, Kh, Kw, H_out, W_out, stride, pad, dil, groups)
     ws = _c(weight_scales, np.float32)
     b = None if bias is None else _c(bias, np.float32)
     out = np.empty((s.N, s.OC, H_out, W_out), np.int8)
     _load().oracle_conv2d_transposed(_ptr(x), float(input_scale), int(input_zero_point),
                                      _ptr(w), ctypes.byref(s), _ptr(ws),
                                      None if b is None else _ptr(b), float(output_scale),
-                                     int(output_zero_point), _ptr(out))
+                                     int(output_zero_point), _relu_flag(activation), _ptr(out))
+    return out
+
+
+def conv2d_acc(x, input_zero_point, w, Kh, Kw, H_out, W_out, stride, pad, dil=(1, 1),
+               groups=1) -> np.ndarray:
+    """int32 [N, OC, H_out, W_out] accumulators of the direct convolution (q8ta_conv2d)."""
+    x = _c(x, np.int8)
+    w = _c(w, np.int8)
+    s = _conv_shape(x, w, Kh, Kw, H_out, W_out, stride, pad, dil, groups)
+    acc = np.empty((s.N, s.OC, H_out, W_out), np.int32)
+    _load().oracle_conv2d_acc(_ptr(x), int(input_zero_point), _ptr(w), ctypes.byref(s), _ptr(acc))
+    return acc
+
+
+def conv2d(x, input_scale, input_zero_point, w, Kh, Kw, weight_scales, bias, output_scale,
+           output_zero_point, H_out, W_out, stride, pad, dil=(1, 1), groups=1,
+           activation="none") -> np.ndarray:
+    """q8ta_conv2d: int8 NCHW x, int8 [OC, Kh*Kw*IC/groups] w -> int8 NCHW."""
+    x = _c(x, np.int8)
+    w = _c(w, np.int8)
+    s = _conv_shape(x, w, Kh, Kw, H_out, W_out, stride, pad, dil, groups)
+    ws = _c(weight_scales, np.float32)
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.empty((s.N, s.OC, H_out, W_out), np.int8)
+    _load().oracle_conv2d(_ptr(x), float(input_scale), int(input_zero_point), _ptr(w),
+                          ctypes.byref(s), _ptr(ws), None if b is None else _ptr(b),
+                          float(output_scale), int(output_zero_point), _relu_flag(activation),
+                          _ptr(out))
     return out
