@@ -57,7 +57,8 @@ typedef enum q8_status {
   Q8_ERR_NULL = 1,        /* a required pointer is NULL */
   Q8_ERR_SHAPE = 2,       /* a size or shape guard failed */
   Q8_ERR_ALIGN = 3,       /* a pointer misses a documented alignment */
-  Q8_ERR_UNSUPPORTED = 4, /* activation != "none", groups != 1, dilation != 1 */
+  Q8_ERR_UNSUPPORTED = 4, /* activation other than "none"/"relu", dilation or
+                             groups < 1, conv2d stride > 8 */
   Q8_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required */
   Q8_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
   Q8_ERR_DEVICE = 7,      /* a kernel raised the library's device error word */
@@ -114,7 +115,10 @@ q8_status q8_dequantize_per_tensor(const int8_t* q, int64_t numel, double scale,
  *                 element instead of using precomputed sums); may be NULL
  *   weight_scales float [>= N]; only [0, N) is read
  *   bias          float [>= N] or NULL (= zero bias)
- *   activation    host C string; must be "none" (Q8_ERR_UNSUPPORTED else)
+ *   activation    host C string: "none", or "relu" (the page's follow-up:
+ *                 the dequantized value is raised to 0 before the
+ *                 requantization, i.e. out = max(out, output_zero_point));
+ *                 anything else gives Q8_ERR_UNSUPPORTED
  *   out           int8 [M, N] row-major
  * Guards (as on the page): N % 4 == 0, (M*K) % 4 == 0, (N*K) % 4 == 0,
  * M, N, K >= 1.
@@ -233,30 +237,37 @@ q8_status q8_linear_packed_acc32(const int8_t* x, int64_t M, int64_t K, int32_t 
 typedef struct q8_conv2d_transposed_shape {
   int64_t N, IC, H_in, W_in;          /* x      int8 [N, IC, H_in, W_in] (NCHW) */
   int64_t OC, Kh, Kw;                 /* weight int8 [OC, weight_row_stride]    */
-  int64_t weight_row_stride;          /* >= Kh*Kw*IC (tolerates row padding)    */
+  int64_t weight_row_stride;          /* >= Kh*Kw*IC/groups (tolerates padding) */
   int64_t H_out, W_out;               /* out    int8 [N, OC, H_out, W_out]      */
   int64_t stride_h, stride_w;         /* >= 1                                   */
   int64_t pad_h, pad_w;               /* >= 0                                   */
   int64_t output_padding_h, output_padding_w; /* accepted, unused: the output
                                          size is H_out/W_out as given           */
-  int64_t dilation_h, dilation_w;     /* must be 1 (Q8_ERR_UNSUPPORTED else)    */
-  int64_t groups;                     /* must be 1 (Q8_ERR_UNSUPPORTED else)    */
+  int64_t dilation_h, dilation_w;     /* >= 1                                   */
+  int64_t groups;                     /* >= 1, divides IC and OC                */
 } q8_conv2d_transposed_shape;
 
 /*
- * For every output (n, oc, oh, ow):
- *   acc = sum over ic, kh, kw of (x[n,ic,ih,iw] - input_zero_point) *
- *         weight[oc, (kh*Kw + kw)*IC + ic]
- * where ih = (oh + pad_h - kh) / stride_h is used only when the numerator is
- * >= 0, divisible by stride_h and ih < H_in (iw likewise); taps that fail
- * contribute nothing.  Then the epilogue above with weight_scales[oc] and
- * bias[oc] (arrays of length >= OC; only [0, OC) is read).
- * Guards (as on the page): groups == 1, dilation == 1, stride >= 1,
- * activation == "none", W_out % 4 == 0, weight_row_stride >= Kh*Kw*IC;
- * plus every size >= 1 and pad >= 0.  weight_sums is accepted and ignored.
+ * For every output (n, oc, oh, ow), with group j = oc / (OC/groups) and
+ * ICg = IC/groups:
+ *   acc = sum over icl < ICg, kh, kw of
+ *         (x[n, j*ICg + icl, ih, iw] - input_zero_point) *
+ *         weight[oc, (kh*Kw + kw)*ICg + icl]
+ * where ih = (oh + pad_h - kh*dilation_h) / stride_h is used only when the
+ * numerator is >= 0, divisible by stride_h and ih < H_in (iw likewise); taps
+ * that fail contribute nothing.  Then the epilogue above with
+ * weight_scales[oc] and bias[oc] (arrays of length >= OC; only [0, OC) is
+ * read).  For groups == 1 the weight layout is the page's reshape
+ * weight[oc, (kh*Kw+kw)*IC + ic] = original[ic, oc, kh, kw]; group j of a
+ * grouped weight holds original[j*ICg + icl, oc - j*OC/groups, kh, kw].
+ * Guards: the page's stride >= 1, W_out % 4 == 0 and weight_row_stride >=
+ * Kh*Kw*IC/groups; activation "none" or "relu"; groups dividing IC and OC,
+ * dilation >= 1 (the page's fail-loud follow-ups, supported here); every
+ * size >= 1 and pad >= 0.  weight_sums is accepted and ignored.
  * workspace: q8_conv2d_transposed_workspace_bytes(shape) bytes, 256-byte
- * aligned (an NHWC bf16 copy of x - input_zero_point and a bf16 copy of the
- * weight).
+ * aligned (an NHWC bf16 copy of x - input_zero_point, channels padded per
+ * group to a multiple of 64, then the packed weight); the size functions
+ * return 0 when a shape guard fails.
  */
 size_t q8_conv2d_transposed_workspace_bytes(const q8_conv2d_transposed_shape* shape);
 q8_status q8_conv2d_transposed(const int8_t* x, const q8_conv2d_transposed_shape* shape,
@@ -273,6 +284,80 @@ q8_status q8_conv2d_transposed_acc32(const int8_t* x, const q8_conv2d_transposed
                                      int32_t input_zero_point, const int8_t* weight,
                                      int32_t* acc, void* workspace, size_t workspace_bytes,
                                      q8_stream_t stream);
+
+/* Packed-weight form, for weights that are fixed across calls (the page's
+ * weight arrives ahead of time, reshaped):
+ *   q8_conv2d_transposed_pack_weight writes the weight's tensor-core layout
+ *     (bf16, per group [taps][IC/64][OC/groups][64]) into `packed`
+ *     (q8_conv2d_transposed_packed_weight_bytes(shape) bytes, 256-byte
+ *     aligned, owned by the caller);
+ *   q8_conv2d_transposed_packed runs the op from it; its workspace holds only
+ *     the input copy (q8_conv2d_transposed_packed_workspace_bytes(shape)).
+ * Guards: those of q8_conv2d_transposed. */
+size_t q8_conv2d_transposed_packed_weight_bytes(const q8_conv2d_transposed_shape* shape);
+size_t q8_conv2d_transposed_packed_workspace_bytes(const q8_conv2d_transposed_shape* shape);
+q8_status q8_conv2d_transposed_pack_weight(const int8_t* weight,
+                                           const q8_conv2d_transposed_shape* shape, void* packed,
+                                           size_t packed_bytes, q8_stream_t stream);
+q8_status q8_conv2d_transposed_packed(const int8_t* x, const q8_conv2d_transposed_shape* shape,
+                                      double input_scale, int32_t input_zero_point,
+                                      const void* packed_weight, const float* weight_scales,
+                                      const float* bias, double output_scale,
+                                      int32_t output_zero_point, const char* activation,
+                                      int8_t* out, void* workspace, size_t workspace_bytes,
+                                      q8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* q8ta_conv2d (direct convolution)                                   [conv] */
+/* ------------------------------------------------------------------------ */
+/* The general int8 convolution whose scaffold and [OC, Kh*Kw*IC] weight
+ * layout the transposed convolution reuses ("Add q8ta_conv2d_transposed op",
+ * Problem and Solution paragraphs). */
+typedef struct q8_conv2d_shape {
+  int64_t N, IC, H_in, W_in;          /* x      int8 [N, IC, H_in, W_in] (NCHW) */
+  int64_t OC, Kh, Kw;                 /* weight int8 [OC, weight_row_stride]    */
+  int64_t weight_row_stride;          /* >= Kh*Kw*IC/groups                     */
+  int64_t H_out, W_out;               /* out    int8 [N, OC, H_out, W_out]      */
+  int64_t stride_h, stride_w;         /* 1 .. 8                                 */
+  int64_t pad_h, pad_w;               /* >= 0                                   */
+  int64_t dilation_h, dilation_w;     /* >= 1                                   */
+  int64_t groups;                     /* >= 1, divides IC and OC                */
+} q8_conv2d_shape;
+
+/*
+ * For every output (n, oc, oh, ow), with group j = oc / (OC/groups) and
+ * ICg = IC/groups:
+ *   acc = sum over icl < ICg, kh, kw of
+ *         (x[n, j*ICg + icl, ih, iw] - input_zero_point) *
+ *         weight[oc, (kh*Kw + kw)*ICg + icl]
+ * with ih = oh*stride_h - pad_h + kh*dilation_h, the tap used only when
+ * 0 <= ih < H_in (iw likewise); weight[oc, (kh*Kw+kw)*ICg + icl] =
+ * original[oc, icl, kh, kw].  Then the shared epilogue with per-oc scales.
+ * H_out and W_out are the caller's (normally (H_in + 2*pad_h -
+ * dilation_h*(Kh-1) - 1) / stride_h + 1); outputs whose window lies wholly
+ * in the padding hold the requantized bias.
+ * Guards: as q8_conv2d_transposed, with stride_h, stride_w <= 8
+ * (Q8_ERR_UNSUPPORTED above: the input is read through TMA boxes with
+ * element strides).  Workspace and packed forms as for the transposed op.
+ */
+size_t q8_conv2d_workspace_bytes(const q8_conv2d_shape* shape);
+q8_status q8_conv2d(const int8_t* x, const q8_conv2d_shape* shape, double input_scale,
+                    int32_t input_zero_point, const int8_t* weight, const float* weight_scales,
+                    const float* bias, double output_scale, int32_t output_zero_point,
+                    const char* activation, int8_t* out, void* workspace, size_t workspace_bytes,
+                    q8_stream_t stream);
+q8_status q8_conv2d_acc32(const int8_t* x, const q8_conv2d_shape* shape, int32_t input_zero_point,
+                          const int8_t* weight, int32_t* acc, void* workspace,
+                          size_t workspace_bytes, q8_stream_t stream);
+size_t q8_conv2d_packed_weight_bytes(const q8_conv2d_shape* shape);
+size_t q8_conv2d_packed_workspace_bytes(const q8_conv2d_shape* shape);
+q8_status q8_conv2d_pack_weight(const int8_t* weight, const q8_conv2d_shape* shape, void* packed,
+                                size_t packed_bytes, q8_stream_t stream);
+q8_status q8_conv2d_packed(const int8_t* x, const q8_conv2d_shape* shape, double input_scale,
+                           int32_t input_zero_point, const void* packed_weight,
+                           const float* weight_scales, const float* bias, double output_scale,
+                           int32_t output_zero_point, const char* activation, int8_t* out,
+                           void* workspace, size_t workspace_bytes, q8_stream_t stream);
 
 #ifdef __cplusplus
 }

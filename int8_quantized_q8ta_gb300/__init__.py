@@ -34,7 +34,11 @@ EXPORTS = (
     "q8_linear_operand_packed", "q8_linear_packed", "q8_quantize_linear_packed",
     "q8_linear_packed_acc32",
     "q8_conv2d_transposed_workspace_bytes", "q8_conv2d_transposed",
-    "q8_conv2d_transposed_acc32",
+    "q8_conv2d_transposed_acc32", "q8_conv2d_transposed_packed_weight_bytes",
+    "q8_conv2d_transposed_packed_workspace_bytes", "q8_conv2d_transposed_pack_weight",
+    "q8_conv2d_transposed_packed",
+    "q8_conv2d_workspace_bytes", "q8_conv2d", "q8_conv2d_acc32", "q8_conv2d_packed_weight_bytes",
+    "q8_conv2d_packed_workspace_bytes", "q8_conv2d_pack_weight", "q8_conv2d_packed",
 )
 
 
@@ -52,6 +56,13 @@ class ConvTShape(ctypes.Structure):
         "dilation_h", "dilation_w", "groups")]
 
 
+class ConvShape(ctypes.Structure):
+    """Mirror of q8_conv2d_shape."""
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "N", "IC", "H_in", "W_in", "OC", "Kh", "Kw", "weight_row_stride", "H_out", "W_out",
+        "stride_h", "stride_w", "pad_h", "pad_w", "dilation_h", "dilation_w", "groups")]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -62,6 +73,7 @@ def _load() -> ctypes.CDLL:
                          ctypes.c_size_t)
     C = ctypes.c_char_p
     SP = ctypes.POINTER(ConvTShape)
+    DP = ctypes.POINTER(ConvShape)
     sig = {
         "q8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "q8_version": (ctypes.c_int, []),
@@ -89,6 +101,18 @@ def _load() -> ctypes.CDLL:
         "q8_conv2d_transposed_workspace_bytes": (S, [SP]),
         "q8_conv2d_transposed": (ctypes.c_int, [P, SP, D, I32, P, P, P, P, D, I32, C, P, P, S, P]),
         "q8_conv2d_transposed_acc32": (ctypes.c_int, [P, SP, I32, P, P, P, S, P]),
+        "q8_conv2d_transposed_packed_weight_bytes": (S, [SP]),
+        "q8_conv2d_transposed_packed_workspace_bytes": (S, [SP]),
+        "q8_conv2d_transposed_pack_weight": (ctypes.c_int, [P, SP, P, S, P]),
+        "q8_conv2d_transposed_packed": (ctypes.c_int, [P, SP, D, I32, P, P, P, D, I32, C, P, P, S,
+                                                       P]),
+        "q8_conv2d_workspace_bytes": (S, [DP]),
+        "q8_conv2d": (ctypes.c_int, [P, DP, D, I32, P, P, P, D, I32, C, P, P, S, P]),
+        "q8_conv2d_acc32": (ctypes.c_int, [P, DP, I32, P, P, P, S, P]),
+        "q8_conv2d_packed_weight_bytes": (S, [DP]),
+        "q8_conv2d_packed_workspace_bytes": (S, [DP]),
+        "q8_conv2d_pack_weight": (ctypes.c_int, [P, DP, P, S, P]),
+        "q8_conv2d_packed": (ctypes.c_int, [P, DP, D, I32, P, P, P, D, I32, C, P, P, S, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -427,14 +451,14 @@ def conv2d_transposed(x, input_scale, input_zero_point, weight, weight_sums, wei
 
 
 def conv2d_transposed_acc32(x, input_zero_point, weight, kernel_size, output_size, stride=1,
-                            padding=0, out=None, workspace=None):
+                            padding=0, dilation=1, groups=1, out=None, workspace=None):
     """Exact int32 accumulators of q8ta_conv2d_transposed."""
     _need(x, torch.int8, "x")
     _need(weight, torch.int8, "weight")
     Kh, Kw = _pair(kernel_size)
     H_out, W_out = output_size
     shape = conv_t_shape(tuple(x.shape), tuple(weight.shape), Kh, Kw, H_out, W_out, stride,
-                         padding)
+                         padding, 0, dilation, groups)
     if out is None:
         out = torch.empty((x.shape[0], weight.shape[0], H_out, W_out), dtype=torch.int32,
                           device=x.device)
@@ -444,4 +468,197 @@ def conv2d_transposed_acc32(x, input_zero_point, weight, kernel_size, output_siz
     _check(_lib.q8_conv2d_transposed_acc32(_ptr(x), ctypes.byref(shape), int(input_zero_point),
                                            _ptr(weight), _ptr(out), _ptr(ws), nbytes, _stream(x)),
            "q8_conv2d_transposed_acc32")
+    return out
+
+
+@dataclasses.dataclass
+class PackedConvWeight:
+    """A convolution weight in the tensor cores' bf16 layout (see
+    q8_conv2d_transposed_pack_weight / q8_conv2d_pack_weight)."""
+    data: torch.Tensor
+    transposed: bool
+    OC: int
+    IC: int
+    Kh: int
+    Kw: int
+    groups: int
+
+
+def _pack_shape(transposed, weight, in_channels, Kh, Kw, groups):
+    # the packed layout depends on the weight only; a minimal valid problem
+    # around it satisfies the shape guards
+    OC, ldw = weight.shape
+    if transposed:
+        return ConvTShape(1, in_channels, 1, 1, OC, Kh, Kw, ldw, 1, 4, 1, 1, 0, 0, 0, 0, 1, 1,
+                          int(groups))
+    return ConvShape(1, in_channels, 1, 1, OC, Kh, Kw, ldw, 1, 4, 1, 1, 0, 0, 1, 1, int(groups))
+
+
+def _pack_conv(transposed, weight, in_channels, kernel_size, groups):
+    _need(weight, torch.int8, "weight")
+    Kh, Kw = _pair(kernel_size)
+    shape = _pack_shape(transposed, weight, in_channels, Kh, Kw, groups)
+    pre = "q8_conv2d_transposed" if transposed else "q8_conv2d"
+    nbytes = getattr(_lib, pre + "_packed_weight_bytes")(ctypes.byref(shape))
+    if nbytes == 0:
+        raise Q8Error(Q8_ERR_SHAPE, pre + "_packed_weight_bytes")
+    data = torch.empty(nbytes, dtype=torch.uint8, device=weight.device)
+    _check(getattr(_lib, pre + "_pack_weight")(_ptr(weight), ctypes.byref(shape), _ptr(data),
+                                                nbytes, _stream(weight)), pre + "_pack_weight")
+    return PackedConvWeight(data, transposed, weight.shape[0], in_channels, Kh, Kw, int(groups))
+
+
+def pack_conv2d_transposed_weight(weight, in_channels, kernel_size, groups=1) -> PackedConvWeight:
+    """Pack a q8ta_conv2d_transposed weight [OC, Kh*Kw*IC/groups] once."""
+    return _pack_conv(True, weight, in_channels, kernel_size, groups)
+
+
+def pack_conv2d_weight(weight, in_channels, kernel_size, groups=1) -> PackedConvWeight:
+    """Pack a q8ta_conv2d weight [OC, Kh*Kw*IC/groups] once."""
+    return _pack_conv(False, weight, in_channels, kernel_size, groups)
+
+
+def conv2d_transposed_packed(x, input_scale, input_zero_point, packed: PackedConvWeight,
+                             weight_scales, bias, output_scale, output_zero_point, stride=1,
+                             padding=0, output_padding=0, dilation=1, activation="none",
+                             output_size=None, out=None, workspace=None):
+    """q8ta_conv2d_transposed from a packed weight."""
+    if not packed.transposed:
+        raise ValueError("packed weight is a q8ta_conv2d weight")
+    _need(x, torch.int8, "x")
+    _need(weight_scales, torch.float32, "weight_scales")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    if x.shape[1] != packed.IC:
+        raise ValueError(f"x has {x.shape[1]} channels, the packed weight {packed.IC}")
+    Kh, Kw = packed.Kh, packed.Kw
+    if output_size is None:
+        sh, sw = _pair(stride)
+        ph, pw = _pair(padding)
+        oph, opw = _pair(output_padding)
+        dh, dw = _pair(dilation)
+        output_size = ((x.shape[2] - 1) * sh - 2 * ph + dh * (Kh - 1) + oph + 1,
+                       (x.shape[3] - 1) * sw - 2 * pw + dw * (Kw - 1) + opw + 1)
+    H_out, W_out = output_size
+    ldw = Kh * Kw * (packed.IC // packed.groups)
+    shape = conv_t_shape(tuple(x.shape), (packed.OC, ldw), Kh, Kw, H_out, W_out, stride, padding,
+                         output_padding, dilation, packed.groups)
+    if out is None:
+        out = torch.empty((x.shape[0], packed.OC, H_out, W_out), dtype=torch.int8, device=x.device)
+    _need(out, torch.int8, "out")
+    nbytes = _lib.q8_conv2d_transposed_packed_workspace_bytes(ctypes.byref(shape))
+    ws = _workspace(nbytes, x.device, workspace)
+    _check(_lib.q8_conv2d_transposed_packed(
+        _ptr(x), ctypes.byref(shape), float(input_scale), int(input_zero_point),
+        _ptr(packed.data), _ptr(weight_scales), _ptr(bias), float(output_scale),
+        int(output_zero_point), activation.encode(), _ptr(out), _ptr(ws), nbytes, _stream(x)),
+        "q8_conv2d_transposed_packed")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# q8ta_conv2d (the direct convolution)
+# ---------------------------------------------------------------------------
+def conv2d_shape(x_shape, weight_shape, Kh, Kw, H_out, W_out, stride=1, padding=0, dilation=1,
+                 groups=1) -> ConvShape:
+    N, IC, H_in, W_in = x_shape
+    OC, ldw = weight_shape
+    sh, sw = _pair(stride)
+    ph, pw = _pair(padding)
+    dh, dw = _pair(dilation)
+    return ConvShape(N, IC, H_in, W_in, OC, Kh, Kw, ldw, H_out, W_out, sh, sw, ph, pw, dh, dw,
+                     int(groups))
+
+
+def conv2d_output_size(H_in, W_in, kernel_size, stride=1, padding=0, dilation=1):
+    Kh, Kw = _pair(kernel_size)
+    sh, sw = _pair(stride)
+    ph, pw = _pair(padding)
+    dh, dw = _pair(dilation)
+    return ((H_in + 2 * ph - dh * (Kh - 1) - 1) // sh + 1,
+            (W_in + 2 * pw - dw * (Kw - 1) - 1) // sw + 1)
+
+
+def conv2d(x, input_scale, input_zero_point, weight, weight_scales, bias, output_scale,
+           output_zero_point, kernel_size, stride=1, padding=0, dilation=1, groups=1,
+           activation="none", output_size=None, out=None, workspace=None):
+    """q8ta_conv2d: int8 NCHW x, int8 weight [OC, Kh*Kw*IC/groups] -> int8 NCHW."""
+    _need(x, torch.int8, "x")
+    _need(weight, torch.int8, "weight")
+    _need(weight_scales, torch.float32, "weight_scales")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    Kh, Kw = _pair(kernel_size)
+    if output_size is None:
+        output_size = conv2d_output_size(x.shape[2], x.shape[3], kernel_size, stride, padding,
+                                         dilation)
+    H_out, W_out = output_size
+    shape = conv2d_shape(tuple(x.shape), tuple(weight.shape), Kh, Kw, H_out, W_out, stride,
+                         padding, dilation, groups)
+    if out is None:
+        out = torch.empty((x.shape[0], weight.shape[0], H_out, W_out), dtype=torch.int8,
+                          device=x.device)
+    _need(out, torch.int8, "out")
+    nbytes = _lib.q8_conv2d_workspace_bytes(ctypes.byref(shape))
+    ws = _workspace(nbytes, x.device, workspace)
+    _check(_lib.q8_conv2d(
+        _ptr(x), ctypes.byref(shape), float(input_scale), int(input_zero_point), _ptr(weight),
+        _ptr(weight_scales), _ptr(bias), float(output_scale), int(output_zero_point),
+        activation.encode(), _ptr(out), _ptr(ws), nbytes, _stream(x)), "q8_conv2d")
+    return out
+
+
+def conv2d_acc32(x, input_zero_point, weight, kernel_size, output_size=None, stride=1, padding=0,
+                 dilation=1, groups=1, out=None, workspace=None):
+    """Exact int32 accumulators of q8ta_conv2d."""
+    _need(x, torch.int8, "x")
+    _need(weight, torch.int8, "weight")
+    Kh, Kw = _pair(kernel_size)
+    if output_size is None:
+        output_size = conv2d_output_size(x.shape[2], x.shape[3], kernel_size, stride, padding,
+                                         dilation)
+    H_out, W_out = output_size
+    shape = conv2d_shape(tuple(x.shape), tuple(weight.shape), Kh, Kw, H_out, W_out, stride,
+                         padding, dilation, groups)
+    if out is None:
+        out = torch.empty((x.shape[0], weight.shape[0], H_out, W_out), dtype=torch.int32,
+                          device=x.device)
+    _need(out, torch.int32, "out")
+    nbytes = _lib.q8_conv2d_workspace_bytes(ctypes.byref(shape))
+    ws = _workspace(nbytes, x.device, workspace)
+    _check(_lib.q8_conv2d_acc32(_ptr(x), ctypes.byref(shape), int(input_zero_point), _ptr(weight),
+                                _ptr(out), _ptr(ws), nbytes, _stream(x)), "q8_conv2d_acc32")
+    return out
+
+
+def conv2d_packed(x, input_scale, input_zero_point, packed: PackedConvWeight, weight_scales, bias,
+                  output_scale, output_zero_point, stride=1, padding=0, dilation=1,
+                  activation="none", output_size=None, out=None, workspace=None):
+    """q8ta_conv2d from a packed weight."""
+    if packed.transposed:
+        raise ValueError("packed weight is a q8ta_conv2d_transposed weight")
+    _need(x, torch.int8, "x")
+    _need(weight_scales, torch.float32, "weight_scales")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    if x.shape[1] != packed.IC:
+        raise ValueError(f"x has {x.shape[1]} channels, the packed weight {packed.IC}")
+    Kh, Kw = packed.Kh, packed.Kw
+    if output_size is None:
+        output_size = conv2d_output_size(x.shape[2], x.shape[3], (Kh, Kw), stride, padding,
+                                         dilation)
+    H_out, W_out = output_size
+    ldw = Kh * Kw * (packed.IC // packed.groups)
+    shape = conv2d_shape(tuple(x.shape), (packed.OC, ldw), Kh, Kw, H_out, W_out, stride, padding,
+                         dilation, packed.groups)
+    if out is None:
+        out = torch.empty((x.shape[0], packed.OC, H_out, W_out), dtype=torch.int8, device=x.device)
+    _need(out, torch.int8, "out")
+    nbytes = _lib.q8_conv2d_packed_workspace_bytes(ctypes.byref(shape))
+    ws = _workspace(nbytes, x.device, workspace)
+    _check(_lib.q8_conv2d_packed(
+        _ptr(x), ctypes.byref(shape), float(input_scale), int(input_zero_point),
+        _ptr(packed.data), _ptr(weight_scales), _ptr(bias), float(output_scale),
+        int(output_zero_point), activation.encode(), _ptr(out), _ptr(ws), nbytes, _stream(x)),
+        "q8_conv2d_packed")
     return out

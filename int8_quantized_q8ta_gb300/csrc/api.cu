@@ -12,52 +12,33 @@
 #include <cstdint>
 #include <cstring>
 
+#include "api_common.h"
 #include "q8ta.h"
 #include "q8ta_internal.h"
 
 namespace {
 
+using namespace q8api;
 using q8::align_ws;
 using q8::kTileK;
 using q8::round_up;
 
-inline cudaStream_t cs(q8_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
-
-inline q8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? Q8_OK : Q8_ERR_CUDA; }
-
-inline bool scale_ok(double s) { return std::isfinite(s) && s > 0.0; }
-inline bool zp_ok(int32_t z) { return z >= -128 && z <= 127; }
-
-// (float)(1.0 / scale): the reciprocal in double, then one rounding to f32
-// ("Add quantize_per_tensor op", Solution paragraph).
-inline float recip_f32(double scale) { return static_cast<float>(1.0 / scale); }
-
-inline bool activation_none(const char* a) { return a != nullptr && std::strcmp(a, "none") == 0; }
-
-inline bool mul_ok(int64_t a, int64_t b) { return a == 0 || b <= INT64_MAX / a; }
-
-q8::Requant make_rq(double input_scale, double output_scale, int32_t ozp) {
-  q8::Requant r;
-  r.s_in = static_cast<float>(input_scale);
-  r.inv_out = recip_f32(output_scale);
-  r.ozp = static_cast<float>(ozp);
-  r.ozp_i = ozp;
-  return r;
-}
-
-// Guards shared by q8_linear and q8_linear_gemv ("Add q8ta_linear op",
+// Guards shared by the q8ta_linear entry points ("Add q8ta_linear op",
 // Implementation paragraph): int8 operands (typed), N % 4 == 0,
-// (M*K) % 4 == 0, (N*K) % 4 == 0, activation == "none".
+// (M*K) % 4 == 0, (N*K) % 4 == 0, activation "none" (or the follow-up
+// "relu", whose flag goes to *relu).
 q8_status check_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
                        int32_t izp, const void* weight, int64_t N, const float* ws,
                        double output_scale, int32_t ozp, const char* activation,
-                       const void* out) {
+                       const void* out, int* relu = nullptr) {
   if (!x || !weight || !ws || !out || !activation) return Q8_ERR_NULL;
   if (M < 1 || K < 1 || N < 1) return Q8_ERR_SHAPE;
   if (!mul_ok(M, K) || !mul_ok(N, K) || !mul_ok(M, N)) return Q8_ERR_SHAPE;
   if (N % 4 != 0 || (M * K) % 4 != 0 || (N * K) % 4 != 0) return Q8_ERR_SHAPE;
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX / 2) return Q8_ERR_SHAPE;
-  if (!activation_none(activation)) return Q8_ERR_UNSUPPORTED;
+  const int act = parse_activation(activation);
+  if (act < 0) return Q8_ERR_UNSUPPORTED;
+  if (relu) *relu = act;
   if (!scale_ok(input_scale) || !scale_ok(output_scale) || !zp_ok(izp) || !zp_ok(ozp))
     return Q8_ERR_ARG;
   return Q8_OK;
@@ -66,9 +47,6 @@ q8_status check_linear(const int8_t* x, int64_t M, int64_t K, double input_scale
 size_t bf16_rows_bytes(int64_t rows, int64_t K) {
   return align_ws(static_cast<size_t>(rows) * static_cast<size_t>(round_up(K, kTileK)) * 2);
 }
-
-// Largest |x - zp| over int8 x.
-inline int a_bound_of(int32_t zp) { return std::max(128 + zp, 127 - zp); }
 
 // A prepared operand is the bf16 data followed by one 256-byte trailer whose
 // first int32 holds a_bound_of(zp) of the zero point it was prepared with.
@@ -87,7 +65,7 @@ const char* q8_status_string(int status) {
     case Q8_ERR_SHAPE: return "Q8_ERR_SHAPE: a size or shape guard failed";
     case Q8_ERR_ALIGN: return "Q8_ERR_ALIGN: a pointer misses a documented alignment";
     case Q8_ERR_UNSUPPORTED:
-      return "Q8_ERR_UNSUPPORTED: activation, groups or dilation not supported";
+      return "Q8_ERR_UNSUPPORTED: activation, dilation, groups or stride not supported";
     case Q8_ERR_WORKSPACE: return "Q8_ERR_WORKSPACE: workspace missing or too small";
     case Q8_ERR_CUDA: return "Q8_ERR_CUDA: a CUDA call or kernel launch failed";
     case Q8_ERR_DEVICE: return "Q8_ERR_DEVICE: a kernel raised the device error word";
@@ -147,13 +125,14 @@ q8_status q8_linear_gemv(const int8_t* x, int64_t M, int64_t K, double input_sca
   (void)weight_sums;
   (void)workspace;
   (void)workspace_bytes;
+  int relu = 0;
   q8_status st = check_linear(x, M, K, input_scale, input_zero_point, weight, N, weight_scales,
-                              output_scale, output_zero_point, activation, out);
+                              output_scale, output_zero_point, activation, out, &relu);
   if (st != Q8_OK) return st;
   if (M != 1) return Q8_ERR_SHAPE;
   return cuda_status(q8::launch_gemv(x, K, input_zero_point, weight, N, weight_scales, bias,
-                                     make_rq(input_scale, output_scale, output_zero_point), out,
-                                     cs(stream)));
+                                     make_rq(input_scale, output_scale, output_zero_point, relu),
+                                     out, cs(stream)));
 }
 
 q8_status q8_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
@@ -161,8 +140,9 @@ q8_status q8_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
                     const int32_t* weight_sums, const float* weight_scales, const float* bias,
                     double output_scale, int32_t output_zero_point, const char* activation,
                     int8_t* out, void* workspace, size_t workspace_bytes, q8_stream_t stream) {
+  int relu = 0;
   q8_status st = check_linear(x, M, K, input_scale, input_zero_point, weight, N, weight_scales,
-                              output_scale, output_zero_point, activation, out);
+                              output_scale, output_zero_point, activation, out, &relu);
   if (st != Q8_OK) return st;
   if (M == 1)
     return q8_linear_gemv(x, M, K, input_scale, input_zero_point, weight, N, weight_sums,
@@ -185,7 +165,7 @@ q8_status q8_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
   L.Kp = Kp;
   L.ws = weight_scales;
   L.bias = bias;
-  L.rq = make_rq(input_scale, output_scale, output_zero_point);
+  L.rq = make_rq(input_scale, output_scale, output_zero_point, relu);
   L.out = out;
   L.a_bound_host = a_bound_of(input_zero_point);
   return cuda_status(q8::launch_tc_linear(L, cs(stream)));
@@ -243,7 +223,7 @@ q8_status q8_quantize_to_linear_operand(const float* x_f32, int64_t M, int64_t K
 static q8_status run_operand_packed(const void* operand, int64_t M, int64_t K, double input_scale,
                                     const void* packed, int64_t N, const float* ws,
                                     const float* bias, double output_scale, int32_t ozp,
-                                    int8_t* out, int32_t* acc_out, q8_stream_t stream) {
+                                    int relu, int8_t* out, int32_t* acc_out, q8_stream_t stream) {
   if (reinterpret_cast<uintptr_t>(packed) % q8::kWorkspaceAlign != 0 ||
       reinterpret_cast<uintptr_t>(operand) % q8::kWorkspaceAlign != 0)
     return Q8_ERR_ALIGN;
@@ -255,7 +235,7 @@ static q8_status run_operand_packed(const void* operand, int64_t M, int64_t K, d
   L.Kp = round_up(K, kTileK);
   L.ws = ws;
   L.bias = bias;
-  L.rq = make_rq(input_scale, output_scale, ozp);
+  L.rq = make_rq(input_scale, output_scale, ozp, relu);
   L.out = out;
   L.acc_out = acc_out;
   L.a_bound_dev = operand_bound_word(const_cast<void*>(operand), M, K);
@@ -270,12 +250,13 @@ q8_status q8_linear_operand_packed(const void* operand, int64_t M, int64_t K, do
                                    const char* activation, int8_t* out, q8_stream_t stream) {
   if (!operand) return Q8_ERR_NULL;
   // input_zero_point is already applied inside the operand; 0 passes its guard
+  int relu = 0;
   q8_status st = check_linear(static_cast<const int8_t*>(operand), M, K, input_scale, 0,
                               packed_weight, N, weight_scales, output_scale, output_zero_point,
-                              activation, out);
+                              activation, out, &relu);
   if (st != Q8_OK) return st;
   return run_operand_packed(operand, M, K, input_scale, packed_weight, N, weight_scales, bias,
-                            output_scale, output_zero_point, out, nullptr, stream);
+                            output_scale, output_zero_point, relu, out, nullptr, stream);
 }
 
 q8_status q8_linear_packed(const int8_t* x, int64_t M, int64_t K, double input_scale,
@@ -283,13 +264,15 @@ q8_status q8_linear_packed(const int8_t* x, int64_t M, int64_t K, double input_s
                            const float* weight_scales, const float* bias, double output_scale,
                            int32_t output_zero_point, const char* activation, int8_t* out,
                            void* workspace, size_t workspace_bytes, q8_stream_t stream) {
+  int relu = 0;
   q8_status st = check_linear(x, M, K, input_scale, input_zero_point, packed_weight, N,
-                              weight_scales, output_scale, output_zero_point, activation, out);
+                              weight_scales, output_scale, output_zero_point, activation, out,
+                              &relu);
   if (st != Q8_OK) return st;
   st = q8_linear_prepare_operand(x, M, K, input_zero_point, workspace, workspace_bytes, stream);
   if (st != Q8_OK) return st;
   return run_operand_packed(workspace, M, K, input_scale, packed_weight, N, weight_scales, bias,
-                            output_scale, output_zero_point, out, nullptr, stream);
+                            output_scale, output_zero_point, relu, out, nullptr, stream);
 }
 
 q8_status q8_quantize_linear_packed(const float* x_f32, int64_t M, int64_t K, double input_scale,
@@ -300,15 +283,16 @@ q8_status q8_quantize_linear_packed(const float* x_f32, int64_t M, int64_t K, do
                                     void* workspace, size_t workspace_bytes, q8_stream_t stream) {
   if (!x_f32) return Q8_ERR_NULL;
   // the quantize op's guard (numel % 4) is implied by (M*K) % 4 == 0 below
+  int relu = 0;
   q8_status st = check_linear(reinterpret_cast<const int8_t*>(x_f32), M, K, input_scale,
                               input_zero_point, packed_weight, N, weight_scales, output_scale,
-                              output_zero_point, activation, out);
+                              output_zero_point, activation, out, &relu);
   if (st != Q8_OK) return st;
   st = q8_quantize_to_linear_operand(x_f32, M, K, input_scale, input_zero_point, x_q, workspace,
                                      workspace_bytes, stream);
   if (st != Q8_OK) return st;
   return run_operand_packed(workspace, M, K, input_scale, packed_weight, N, weight_scales, bias,
-                            output_scale, output_zero_point, out, nullptr, stream);
+                            output_scale, output_zero_point, relu, out, nullptr, stream);
 }
 
 q8_status q8_linear_packed_acc32(const int8_t* x, int64_t M, int64_t K, int32_t input_zero_point,
@@ -320,117 +304,8 @@ q8_status q8_linear_packed_acc32(const int8_t* x, int64_t M, int64_t K, int32_t 
   if (st != Q8_OK) return st;
   st = q8_linear_prepare_operand(x, M, K, input_zero_point, workspace, workspace_bytes, stream);
   if (st != Q8_OK) return st;
-  return run_operand_packed(workspace, M, K, 1.0, packed_weight, N, nullptr, nullptr, 1.0, 0,
+  return run_operand_packed(workspace, M, K, 1.0, packed_weight, N, nullptr, nullptr, 1.0, 0, 0,
                             nullptr, acc, stream);
-}
-
-// ---------------------------------------------------------------- conv_t
-static q8_status check_conv_t(const int8_t* x, const q8_conv2d_transposed_shape* sh,
-                              const int8_t* weight, const void* out) {
-  if (!x || !sh || !weight || !out) return Q8_ERR_NULL;
-  const q8_conv2d_transposed_shape& s = *sh;
-  if (s.groups != 1 || s.dilation_h != 1 || s.dilation_w != 1) return Q8_ERR_UNSUPPORTED;
-  if (s.stride_h < 1 || s.stride_w < 1) return Q8_ERR_SHAPE;
-  if (s.N < 1 || s.IC < 1 || s.H_in < 1 || s.W_in < 1 || s.OC < 1 || s.Kh < 1 || s.Kw < 1 ||
-      s.H_out < 1 || s.W_out < 1)
-    return Q8_ERR_SHAPE;
-  if (s.pad_h < 0 || s.pad_w < 0 || s.output_padding_h < 0 || s.output_padding_w < 0)
-    return Q8_ERR_SHAPE;
-  if (s.W_out % 4 != 0) return Q8_ERR_SHAPE;
-  if (!mul_ok(s.Kh, s.Kw) || !mul_ok(s.Kh * s.Kw, s.IC)) return Q8_ERR_SHAPE;
-  if (s.weight_row_stride < s.Kh * s.Kw * s.IC) return Q8_ERR_SHAPE;
-  // sizes the kernels index with 32-bit tile coordinates
-  const int64_t lim = INT32_MAX / 4;
-  if (s.N > lim || s.IC > lim || s.H_in > lim || s.W_in > lim || s.OC > lim || s.H_out > lim ||
-      s.W_out > lim || s.Kh > 4096 || s.Kw > 4096 || s.stride_h > 4096 || s.stride_w > 4096 ||
-      s.pad_h > lim || s.pad_w > lim)
-    return Q8_ERR_SHAPE;
-  if (!mul_ok(s.N * s.H_in, s.W_in) || !mul_ok(s.N * s.H_in * s.W_in, round_up(s.IC, kTileK)))
-    return Q8_ERR_SHAPE;
-  return Q8_OK;
-}
-
-size_t q8_conv2d_transposed_workspace_bytes(const q8_conv2d_transposed_shape* sh) {
-  if (!sh || sh->N < 1 || sh->IC < 1 || sh->H_in < 1 || sh->W_in < 1 || sh->OC < 1 ||
-      sh->Kh < 1 || sh->Kw < 1)
-    return 0;
-  const int64_t ICp = round_up(sh->IC, kTileK);
-  return align_ws(static_cast<size_t>(sh->N * sh->H_in * sh->W_in) * ICp * 2) +
-         align_ws(static_cast<size_t>(sh->OC * sh->Kh * sh->Kw) * ICp * 2);
-}
-
-static q8_status conv_t_common(const int8_t* x, const q8_conv2d_transposed_shape* sh,
-                               double input_scale, int32_t izp, const int8_t* weight,
-                               const float* ws, const float* bias, double output_scale,
-                               int32_t ozp, int8_t* out, int32_t* acc_out, void* workspace,
-                               size_t workspace_bytes, q8_stream_t stream) {
-  const q8_conv2d_transposed_shape& s = *sh;
-  const size_t need = q8_conv2d_transposed_workspace_bytes(sh);
-  if (!workspace || workspace_bytes < need) return Q8_ERR_WORKSPACE;
-  if (reinterpret_cast<uintptr_t>(workspace) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
-  const int64_t ICp = round_up(s.IC, kTileK);
-  auto* a = static_cast<__nv_bfloat16*>(workspace);
-  auto* b = reinterpret_cast<__nv_bfloat16*>(
-      static_cast<char*>(workspace) + align_ws(static_cast<size_t>(s.N * s.H_in * s.W_in) * ICp * 2));
-  cudaError_t e = q8::launch_nchw_to_nhwc_bf16(x, s.N, s.IC, s.H_in, s.W_in, izp, a, ICp, cs(stream));
-  if (e == cudaSuccess)
-    e = q8::launch_convt_weight_bf16(weight, s.OC, s.Kh * s.Kw, s.IC, s.weight_row_stride, b, ICp,
-                                     cs(stream));
-  if (e != cudaSuccess) return Q8_ERR_CUDA;
-  q8::TcConvT C{};
-  C.a = a;
-  C.b = b;
-  C.N = s.N;
-  C.ICp = ICp;
-  C.H_in = s.H_in;
-  C.W_in = s.W_in;
-  C.OC = s.OC;
-  C.Kh = s.Kh;
-  C.Kw = s.Kw;
-  C.H_out = s.H_out;
-  C.W_out = s.W_out;
-  C.stride_h = s.stride_h;
-  C.stride_w = s.stride_w;
-  C.pad_h = s.pad_h;
-  C.pad_w = s.pad_w;
-  C.ws = ws;
-  C.bias = bias;
-  C.rq = make_rq(input_scale, output_scale, ozp);
-  C.out = out;
-  C.acc_out = acc_out;
-  C.a_bound = a_bound_of(izp);
-  return cuda_status(q8::launch_tc_conv_t(C, cs(stream)));
-}
-
-q8_status q8_conv2d_transposed(const int8_t* x, const q8_conv2d_transposed_shape* shape,
-                               double input_scale, int32_t input_zero_point,
-                               const int8_t* weight, const int32_t* weight_sums,
-                               const float* weight_scales, const float* bias,
-                               double output_scale, int32_t output_zero_point,
-                               const char* activation, int8_t* out, void* workspace,
-                               size_t workspace_bytes, q8_stream_t stream) {
-  (void)weight_sums;
-  q8_status st = check_conv_t(x, shape, weight, out);
-  if (st != Q8_OK) return st;
-  if (!weight_scales || !activation) return Q8_ERR_NULL;
-  if (!activation_none(activation)) return Q8_ERR_UNSUPPORTED;
-  if (!scale_ok(input_scale) || !scale_ok(output_scale) || !zp_ok(input_zero_point) ||
-      !zp_ok(output_zero_point))
-    return Q8_ERR_ARG;
-  return conv_t_common(x, shape, input_scale, input_zero_point, weight, weight_scales, bias,
-                       output_scale, output_zero_point, out, nullptr, workspace, workspace_bytes,
-                       stream);
-}
-
-q8_status q8_conv2d_transposed_acc32(const int8_t* x, const q8_conv2d_transposed_shape* shape,
-                                     int32_t input_zero_point, const int8_t* weight, int32_t* acc,
-                                     void* workspace, size_t workspace_bytes,
-                                     q8_stream_t stream) {
-  q8_status st = check_conv_t(x, shape, weight, acc);
-  if (st != Q8_OK) return st;
-  if (!zp_ok(input_zero_point)) return Q8_ERR_ARG;
-  return conv_t_common(x, shape, 1.0, input_zero_point, weight, nullptr, nullptr, 1.0, 0, nullptr,
-                       acc, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -21,6 +21,7 @@ struct Requant {
   float inv_out;  // (float)(1.0 / output_scale), formed on the host in double
   float ozp;      // output zero point, exactly representable
   int32_t ozp_i;  // the same zero point as an integer
+  int32_t lo;     // output floor: -128, or ozp_i for activation "relu"
 };
 
 __device__ __forceinline__ int8_t round_add_clamp(float u, float zp) {
@@ -38,24 +39,28 @@ __device__ __forceinline__ int8_t round_add_clamp(float u, float zp) {
 //  * adding 1.5 * 2^23 rounds to an integer (round-to-nearest-even: the sum
 //    lies in [2^23, 2^24), where the spacing of floats is exactly 1), and the
 //    integer is the low bits of the sum's encoding: bits(sum) - 0x4B400000.
-// Equal to round_add_clamp for every float u and every zp in [-128, 127].
-__device__ __forceinline__ int32_t round_add_clamp_i(float u, int32_t zp) {
+// Equal to round_add_clamp for every float u and every zp in [-128, 127]
+// when lo = -128.  lo = zp gives the relu form: max(v, 0) before the
+// requantization is max(q, zp) after it, v * inv_out being monotone and
+// rint(0) = 0.
+__device__ __forceinline__ int32_t round_add_clamp_i(float u, int32_t zp, int32_t lo) {
   const float c = fminf(fmaxf(u, -2097152.0f), 2097152.0f);
   const float y = __fadd_rn(c, 12582912.0f);
   const int32_t q = __float_as_int(y) - (0x4B400000 - zp);
-  return min(max(q, -128), 127);
+  return min(max(q, lo), 127);
 }
 
 // The fused epilogue of one accumulator, in the order of "Add q8ta_linear op"
 // (Solution paragraph): ((acc * input_scale) * weight_scale + bias) *
-// (1 / output_scale), rounded, plus the output zero point, clamped.
+// (1 / output_scale), rounded, plus the output zero point, clamped (from
+// below at the zero point under the relu activation).
 __device__ __forceinline__ int32_t requant_i(int32_t acc, float ws, float b, const Requant& rq) {
   float a = __int2float_rn(acc);
   float t = __fmul_rn(a, rq.s_in);
   t = __fmul_rn(t, ws);
   float v = __fadd_rn(t, b);
   float u = __fmul_rn(v, rq.inv_out);
-  return round_add_clamp_i(u, rq.ozp_i);
+  return round_add_clamp_i(u, rq.ozp_i, rq.lo);
 }
 
 __device__ __forceinline__ int8_t requant_one(int32_t acc, float ws, float b, const Requant& rq) {

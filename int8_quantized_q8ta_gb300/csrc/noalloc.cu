@@ -20,6 +20,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "api_common.h"
 #include "q8ta.h"
 #include "q8ta_internal.h"
 
@@ -96,12 +97,11 @@ extern "C" q8_status q8_linear_noalloc(const int8_t* x, int64_t M, int64_t K, do
   L.Kp = Kp;
   L.ws = weight_scales;
   L.bias = bias;
-  L.rq.s_in = static_cast<float>(input_scale);
-  L.rq.inv_out = static_cast<float>(1.0 / output_scale);
-  L.rq.ozp = static_cast<float>(output_zero_point);
-  L.rq.ozp_i = output_zero_point;
+  // the guards above passed, so the activation is "none" or "relu"
+  L.rq = q8api::make_rq(input_scale, output_scale, output_zero_point,
+                        q8api::parse_activation(activation) == 1 ? 1 : 0);
   // largest |x - input_zero_point| over int8 x: sets the exact f32 chunk length
-  L.a_bound_host = std::max(128 + input_zero_point, 127 - input_zero_point);
+  L.a_bound_host = q8api::a_bound_of(input_zero_point);
   L.out = out;
   return q8::launch_tc_linear(L, s) == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }

@@ -41,12 +41,17 @@ cudaError_t launch_rows_to_bf16(const int8_t* src, int64_t rows, int64_t K, int6
 cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, float inv_scale,
                                       int32_t zp, int8_t* xq, __nv_bfloat16* dst, int64_t Kp,
                                       cudaStream_t s, int32_t* bound_word = nullptr);
-// dst[n, h, w, c] = bf16(x[n, c, h, w] - zp) for c < C, 0 for C <= c < Cp.
-cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t C, int64_t H, int64_t W,
-                                     int32_t zp, __nv_bfloat16* dst, int64_t Cp, cudaStream_t s);
-// dst[oc, t*ICp + ic] = bf16(w[oc*ldw + t*IC + ic]) for ic < IC, else 0.
-cudaError_t launch_convt_weight_bf16(const int8_t* w, int64_t OC, int64_t taps, int64_t IC,
-                                     int64_t ldw, __nv_bfloat16* dst, int64_t ICp, cudaStream_t s);
+// Channel-blocked NHWC copy for the convolutions, per group:
+// dst[n][j*ICgp/64 + c/64][h][w][c%64] = bf16(x[n, j*ICg + c, h, w] - zp) for
+// c < ICg in group j, 0 for ICg <= c < ICgp (ICgp = ICg rounded up to 64).
+cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t groups, int64_t ICg,
+                                     int64_t H, int64_t W, int32_t zp, __nv_bfloat16* dst,
+                                     int64_t ICgp, cudaStream_t s);
+// Packed convolution weight, per group j (rows oc = j*OCg + ocl):
+// dst[j][t][ic/64][ocl][ic%64] = bf16(w[oc*ldw + t*ICg + ic]) for ic < ICg, else 0.
+cudaError_t launch_conv_weight_bf16(const int8_t* w, int64_t groups, int64_t OCg, int64_t taps,
+                                    int64_t ICg, int64_t ldw, __nv_bfloat16* dst, int64_t ICgp,
+                                    cudaStream_t s);
 
 // ---- tensor-core GEMM (tc_gemm.cu) -----------------------------------------
 struct TcLinear {
@@ -68,15 +73,22 @@ struct TcLinear {
 cudaError_t launch_tc_linear(const TcLinear& p, cudaStream_t s);
 
 struct TcConvT {
-  const __nv_bfloat16* a;  // [N, H_in, W_in, ICp] bf16, values x - input_zero_point
-  const __nv_bfloat16* b;  // [OC, Kh*Kw*ICp] bf16
-  int64_t N, ICp, H_in, W_in, OC, Kh, Kw, H_out, W_out;
-  int64_t stride_h, stride_w, pad_h, pad_w;
+  // One group's implicit GEMM of a transposed (direct == false) or direct
+  // (direct == true) convolution.
+  // a: the group's first channel block in the channel-blocked NHWC copy of
+  //    x - input_zero_point, [N][cb_total][H_in][W_in][64] bf16;
+  // b: the group's packed weight [taps][ICp/64][OC][64] bf16.
+  const __nv_bfloat16* a;
+  const __nv_bfloat16* b;
+  int64_t N, ICp, cb_total, H_in, W_in, OC, Kh, Kw, H_out, W_out;
+  int64_t stride_h, stride_w, pad_h, pad_w, dil_h, dil_w;
+  int64_t out_ch;    // channels of the output tensor (the group's OC columns start at out)
+  bool direct;
   const float* ws;
   const float* bias;
   Requant rq;
-  int8_t* out;       // [N, OC, H_out, W_out]
-  int32_t* acc_out;  // int32 debug output, or null
+  int8_t* out;       // the group's first output channel of [N, out_ch, H_out, W_out]
+  int32_t* acc_out;  // int32 debug output laid out like out, or null
   int a_bound;       // largest |x - input_zero_point| (see TcLinear)
 };
 cudaError_t launch_tc_conv_t(const TcConvT& p, cudaStream_t s);
@@ -87,7 +99,11 @@ uint32_t* device_error_word();
 cudaError_t read_device_error(uint32_t* code, bool clear);
 
 // TMA tensor map of a bf16 tensor with 128-byte swizzle (tc_gemm_host.cu).
+// element_strides (optional, rank entries, 1..8): the box reads every
+// element_strides[i]-th element along dimension i, box[i] / element_strides[i]
+// of them, packed densely in shared memory.
 bool encode_bf16_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides_bytes, const uint32_t* box);
+                      const uint64_t* strides_bytes, const uint32_t* box,
+                      const uint32_t* element_strides = nullptr);
 
 }  // namespace q8

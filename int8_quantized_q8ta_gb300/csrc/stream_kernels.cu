@@ -421,21 +421,24 @@ cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, f
   return cudaGetLastError();
 }
 
-// NCHW int8 -> channel-blocked NHWC bf16 (x - zp): dst[n][c/64][h][w][c%64],
-// channels zero-padded to Cp (padding channels are exactly 0, not -zp), so
-// the (64 channels x w x h) box of one k-block is contiguous along w.
+// NCHW int8 -> channel-blocked NHWC bf16 (x - zp), per group:
+// dst[n][j*CBg + c/64][h][w][c%64] for channel c of group j (CBg = ICgp/64
+// blocks per group); the padding channels ICg <= c < ICgp hold exactly 0, not
+// -zp, so the (64 channels x w x h) box of one k-block is contiguous along w.
 // A thread takes 8 channels x 4 columns of one (n, h) row: 8 loads of 4
 // bytes (consecutive threads take consecutive column quads of one channel,
 // so a warp reads whole 32-byte sectors) and 4 stores of 16 bytes (the
 // 8-channel pieces of 4 columns).  No shared memory, no block barrier.
 template <typename Idx>
 __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __restrict__ x,
-                                                                Idx NH, int64_t C, Idx H,
-                                                                int64_t W, int32_t zp,
+                                                                Idx NH, int64_t groups, int64_t ICg,
+                                                                Idx H, int64_t W, int32_t zp,
                                                                 uint4* __restrict__ dst,
-                                                                int64_t Cp) {
+                                                                int64_t ICgp) {
   const Idx W4 = static_cast<Idx>((W + 3) / 4);
-  const Idx CB = static_cast<Idx>(Cp / 64);
+  const Idx CBg = static_cast<Idx>(ICgp / 64);
+  const Idx CB = CBg * static_cast<Idx>(groups);
+  const int64_t C = groups * ICg;
   const Idx total = NH * CB * 8 * W4;
   const bool vec = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 4 == 0);
   for (Idx i = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -447,14 +450,15 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __
     const int64_t cb = rest % CB;
     const Idx nhi = rest / CB;
     const int64_t n = nhi / H, h = nhi - (nhi / H) * H;
-    const int64_t c0 = cb * 64 + 8 * cseg;
+    const int64_t g = cb / CBg;
+    const int64_t cl0 = (cb - g * CBg) * 64 + 8 * cseg;   // channel within the group
     const int64_t wb = 4 * w4;
     uint32_t raw[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       raw[j] = 0u;
-      if (c0 + j < C) {
-        const int8_t* src = x + ((n * C + c0 + j) * H + h) * W + wb;
+      if (cl0 + j < ICg) {
+        const int8_t* src = x + ((n * C + g * ICg + cl0 + j) * H + h) * W + wb;
         if (vec) {
           raw[j] = __ldcs(reinterpret_cast<const unsigned int*>(src));
         } else {
@@ -471,7 +475,8 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __
       int d[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        d[j] = (c0 + j < C) ? static_cast<int>(static_cast<int8_t>((raw[j] >> (8 * q)) & 0xff)) - zp : 0;
+        d[j] = (cl0 + j < ICg) ? static_cast<int>(static_cast<int8_t>((raw[j] >> (8 * q)) & 0xff)) - zp
+                               : 0;
       uint4 o;
       o.x = bf16x2_from_ints(d[0], d[1]);
       o.y = bf16x2_from_ints(d[2], d[3]);
@@ -482,56 +487,63 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __
   }
 }
 
-cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t C, int64_t H, int64_t W,
-                                     int32_t zp, __nv_bfloat16* dst, int64_t Cp, cudaStream_t s) {
+cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t groups, int64_t ICg,
+                                     int64_t H, int64_t W, int32_t zp, __nv_bfloat16* dst,
+                                     int64_t ICgp, cudaStream_t s) {
   if (N * H * W == 0) return cudaSuccess;
-  const int64_t items = N * H * (Cp / 64) * 8 * ((W + 3) / 4);
+  const int64_t items = N * H * groups * (ICgp / 64) * 8 * ((W + 3) / 4);
   if (items + 256 < (int64_t(1) << 31)) {
     static int occ[64];
     const int grid = resident_grid(nchw_to_nhwc_bf16_kernel<uint32_t>, occ, items, 256);
     nchw_to_nhwc_bf16_kernel<uint32_t><<<grid, 256, 0, s>>>(
-        x, static_cast<uint32_t>(N * H), C, static_cast<uint32_t>(H), W, zp,
-        reinterpret_cast<uint4*>(dst), Cp);
+        x, static_cast<uint32_t>(N * H), groups, ICg, static_cast<uint32_t>(H), W, zp,
+        reinterpret_cast<uint4*>(dst), ICgp);
   } else {
     static int occ[64];
     const int grid = resident_grid(nchw_to_nhwc_bf16_kernel<int64_t>, occ, items, 256);
-    nchw_to_nhwc_bf16_kernel<int64_t><<<grid, 256, 0, s>>>(x, N * H, C, H, W, zp,
-                                                           reinterpret_cast<uint4*>(dst), Cp);
+    nchw_to_nhwc_bf16_kernel<int64_t><<<grid, 256, 0, s>>>(
+        x, N * H, groups, ICg, H, W, zp, reinterpret_cast<uint4*>(dst), ICgp);
   }
   return cudaGetLastError();
 }
 
-// Transposed-convolution weight [OC, ldw] (taps x IC used) -> bf16
-// dst[t][ic/64][oc][ic%64], input channels zero-padded to ICp: the
-// (BN output channels x 64 input channels) tile of one k-block is contiguous.
-__global__ void __launch_bounds__(256) convt_weight_bf16_kernel(const int8_t* __restrict__ w,
-                                                                int64_t OC, int64_t taps,
-                                                                int64_t IC, int64_t ldw,
-                                                                uint32_t* __restrict__ dst,
-                                                                int64_t ICp) {
-  const int64_t icb = ICp / 64;
-  const int64_t total = taps * icb * OC * 32;  // bf16 pairs
+// Convolution weight [OC, ldw] (per row: taps x ICg used) -> bf16, per group j:
+// dst[j][t][ic/64][ocl][ic%64] for oc = j*OCg + ocl, input channels
+// zero-padded to ICgp: the (BN output channels x 64 input channels) tile of
+// one k-block is contiguous.
+__global__ void __launch_bounds__(256) conv_weight_bf16_kernel(const int8_t* __restrict__ w,
+                                                               int64_t groups, int64_t OCg,
+                                                               int64_t taps, int64_t ICg,
+                                                               int64_t ldw,
+                                                               uint32_t* __restrict__ dst,
+                                                               int64_t ICgp) {
+  const int64_t icb = ICgp / 64;
+  const int64_t total = groups * taps * icb * OCg * 32;  // bf16 pairs
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t jp = i & 31;
     int64_t rest = i >> 5;
-    const int64_t oc = rest % OC;
-    rest /= OC;
+    const int64_t ocl = rest % OCg;
+    rest /= OCg;
     const int64_t cb = rest % icb;
-    const int64_t t = rest / icb;
+    rest /= icb;
+    const int64_t t = rest % taps;
+    const int64_t g = rest / taps;
     const int64_t ic = cb * 64 + 2 * jp;
-    const int a = (ic < IC) ? w[oc * ldw + t * IC + ic] : 0;
-    const int b = (ic + 1 < IC) ? w[oc * ldw + t * IC + ic + 1] : 0;
+    const int8_t* row = w + (g * OCg + ocl) * ldw + t * ICg;
+    const int a = (ic < ICg) ? row[ic] : 0;
+    const int b = (ic + 1 < ICg) ? row[ic + 1] : 0;
     dst[i] = bf16x2_from_ints(a, b);
   }
 }
 
-cudaError_t launch_convt_weight_bf16(const int8_t* w, int64_t OC, int64_t taps, int64_t IC,
-                                     int64_t ldw, __nv_bfloat16* dst, int64_t ICp, cudaStream_t s) {
-  const int64_t items = OC * taps * ICp / 2;
+cudaError_t launch_conv_weight_bf16(const int8_t* w, int64_t groups, int64_t OCg, int64_t taps,
+                                    int64_t ICg, int64_t ldw, __nv_bfloat16* dst, int64_t ICgp,
+                                    cudaStream_t s) {
+  const int64_t items = groups * OCg * taps * ICgp / 2;
   if (items == 0) return cudaSuccess;
-  convt_weight_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
-      w, OC, taps, IC, ldw, reinterpret_cast<uint32_t*>(dst), ICp);
+  conv_weight_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
+      w, groups, OCg, taps, ICg, ldw, reinterpret_cast<uint32_t*>(dst), ICgp);
   return cudaGetLastError();
 }
 

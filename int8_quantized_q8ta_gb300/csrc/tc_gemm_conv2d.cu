@@ -1,0 +1,28 @@
+// tc_gemm_conv2d.cu -- q8ta_conv2d (the direct convolution) on the
+// tensor-core GEMM (tc_gemm_kernel.cuh): an implicit GEMM over 128-pixel
+// output tiles whose input taps are 5-D TMA boxes with element strides
+// (stride_w, stride_h), starting at (ow*stride_w - pad_w + kw*dil_w, ...);
+// the boxes' zero fill covers the padding.  One launch per group.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "q8ta_internal.h"
+#include "tc_gemm_conv_setup.cuh"
+
+namespace q8 {
+
+cudaError_t launch_tc_conv2d(const TcConvT& C, cudaStream_t s) {
+  ConvSetup S;
+  if (!conv_setup(C, S)) return cudaErrorInvalidValue;
+  if (S.p.total_units == 0) return cudaSuccess;
+  switch (S.bn * 4 + S.kd) {
+    case 64 * 4 + 1: return launch_tc_kernel<64, 16, 2, 1, 1>(S.ma, S.mb, S.p, S.ostage, s);
+    case 64 * 4 + 2: return launch_tc_kernel<64, 16, 2, 2, 1>(S.ma, S.mb, S.p, S.ostage, s);
+    case 128 * 4 + 1: return launch_tc_kernel<128, 16, 2, 1, 1>(S.ma, S.mb, S.p, S.ostage, s);
+    case 128 * 4 + 2: return launch_tc_kernel<128, 16, 2, 2, 1>(S.ma, S.mb, S.p, S.ostage, s);
+    case 256 * 4 + 1: return launch_tc_kernel<256, 8, 2, 1, 1>(S.ma, S.mb, S.p, S.ostage, s);
+    default: return launch_tc_kernel<256, 8, 2, 2, 1>(S.ma, S.mb, S.p, S.ostage, s);
+  }
+}
+
+}  // namespace q8

@@ -1,0 +1,169 @@
+// tc_gemm_conv_setup.cuh -- host set-up shared by the two convolution GEMM
+// launchers: tile shape, TMA tensor maps and kernel parameters of one group.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "q8ta_internal.h"
+#include "tc_gemm_kernel.cuh"
+
+namespace q8 {
+
+inline int64_t gcd64(int64_t a, int64_t b) {
+  while (b != 0) {
+    const int64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// a^-1 modulo m for coprime a, m (extended Euclid); 0 when m == 1.
+inline int64_t inv_mod(int64_t a, int64_t m) {
+  if (m == 1) return 0;
+  int64_t t = 0, nt = 1, r = m, nr = a % m;
+  while (nr != 0) {
+    const int64_t q = r / nr;
+    const int64_t t2 = t - q * nt;
+    t = nt;
+    nt = t2;
+    const int64_t r2 = r - q * nr;
+    r = nr;
+    nr = r2;
+  }
+  return t < 0 ? t + m : t;
+}
+
+// Row taps of transposed-convolution phase ph: kh with kh * dil = ph + pad
+// (mod stride), kh < K (the count the kernel's decode derives).
+inline int conv_t_phase_taps(int64_t ph, int64_t pad, int64_t stride, int64_t dil, int64_t K) {
+  const int64_t g = gcd64(dil, stride), ts = stride / g;
+  const int64_t t = (ph + pad) % stride;
+  if (t % g != 0) return 0;
+  const int64_t k0 = (t / g) * inv_mod(dil / g, ts) % ts;
+  return k0 < K ? static_cast<int>((K - k0 + ts - 1) / ts) : 0;
+}
+
+struct ConvSetup {
+  CUtensorMap ma, mb;
+  TcParams p;
+  size_t ostage;
+  int bn, kd;
+};
+
+// Tile shape: 128 output pixels (bw columns x bh rows of a stride phase for
+// the transposed convolution, of the output for the direct one) x bn output
+// channels.  The direct convolution reads its input through boxes with
+// element strides (stride_w, stride_h), whose extents bw * stride_w and
+// bh * stride_h must stay within the TMA limit of 256.
+inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
+  const bool direct = C.direct;
+  const int bn = pick_bn(C.OC);
+  const int64_t Hq = direct ? C.H_out : (C.H_out + C.stride_h - 1) / C.stride_h;
+  const int64_t Wq = direct ? C.W_out : (C.W_out + C.stride_w - 1) / C.stride_w;
+  const int64_t ew = direct ? C.stride_w : 1, eh = direct ? C.stride_h : 1;
+  int bw = 1;
+  while (bw < Wq && bw < kBM) bw *= 2;
+  while (bw > 1 && bw * ew > 256) bw /= 2;
+  while (bw < kBM && (kBM / bw) * eh > 256) bw *= 2;
+  const int bh = kBM / bw;
+  if (bw * ew > 256 || bh * eh > 256) return false;
+  const uint64_t icb = static_cast<uint64_t>(C.ICp / kBK);
+  // two k-blocks (channel blocks) per TMA box when they split evenly: the
+  // 128-wide tiles need bigger boxes to keep enough bytes in flight per SM
+  const int kd = (icb % 2 == 0) ? 2 : 1;
+  {
+    // the group's channel blocks of [N][cb_total][H_in][W_in][64] bf16
+    const uint64_t dims[5] = {kBK, static_cast<uint64_t>(C.W_in), static_cast<uint64_t>(C.H_in),
+                              icb, static_cast<uint64_t>(C.N)};
+    const uint64_t row = kBK * 2;
+    const uint64_t str[4] = {row, row * C.W_in, row * C.W_in * C.H_in,
+                             row * C.W_in * C.H_in * static_cast<uint64_t>(C.cb_total)};
+    const uint32_t box[5] = {kBK, static_cast<uint32_t>(bw * ew), static_cast<uint32_t>(bh * eh),
+                             static_cast<uint32_t>(kd), 1};
+    const uint32_t estr[5] = {1, static_cast<uint32_t>(ew), static_cast<uint32_t>(eh), 1, 1};
+    if (!encode_bf16_tmap(&S.ma, C.a, 5, dims, str, box, estr)) return false;
+  }
+  {
+    // weight [taps][ICp/64][OC][64] bf16
+    const uint64_t dims[3] = {kBK, static_cast<uint64_t>(C.OC),
+                              static_cast<uint64_t>(C.Kh * C.Kw) * icb};
+    const uint64_t str[2] = {kBK * 2, static_cast<uint64_t>(C.OC) * kBK * 2};
+    const uint32_t box[3] = {kBK, static_cast<uint32_t>(bn), static_cast<uint32_t>(kd)};
+    if (!encode_bf16_tmap(&S.mb, C.b, 3, dims, str, box)) return false;
+  }
+  TcParams p{};
+  p.mode = direct ? 2 : 1;
+  p.kd = kd;
+  p.Nimg = static_cast<int>(C.N);
+  p.OC = static_cast<int>(C.OC);
+  p.out_ch = static_cast<int>(C.out_ch);
+  p.Kh = static_cast<int>(C.Kh);
+  p.Kw = static_cast<int>(C.Kw);
+  p.H_out = static_cast<int>(C.H_out);
+  p.W_out = static_cast<int>(C.W_out);
+  p.sh = static_cast<int>(C.stride_h);
+  p.sw = static_cast<int>(C.stride_w);
+  p.pad_h = static_cast<int>(C.pad_h);
+  p.pad_w = static_cast<int>(C.pad_w);
+  p.dil_h = static_cast<int>(C.dil_h);
+  p.dil_w = static_cast<int>(C.dil_w);
+  p.gh = static_cast<int>(gcd64(C.dil_h, C.stride_h));
+  p.gw = static_cast<int>(gcd64(C.dil_w, C.stride_w));
+  p.tsh = static_cast<int>(C.stride_h / p.gh);
+  p.tsw = static_cast<int>(C.stride_w / p.gw);
+  p.dsh = static_cast<int>(C.dil_h / p.gh);
+  p.dsw = static_cast<int>(C.dil_w / p.gw);
+  p.invh = static_cast<int>(inv_mod(p.dsh, p.tsh));
+  p.invw = static_cast<int>(inv_mod(p.dsw, p.tsw));
+  p.osh = direct ? 1 : p.sh;
+  p.osw = direct ? 1 : p.sw;
+  p.ICp = static_cast<int>(C.ICp);
+  p.icb = static_cast<int>(icb);
+  p.BW = bw;
+  p.BH = bh;
+  p.tiles_w = static_cast<int>((Wq + bw - 1) / bw);
+  p.tiles_h = static_cast<int>((Hq + bh - 1) / bh);
+  p.tiles_oc = static_cast<int>((C.OC + bn - 1) / bn);
+  const int64_t phases = direct ? 1 : C.stride_h;
+  const int64_t units = phases * C.N * p.tiles_h * p.tiles_w * p.tiles_oc;
+  if (units > (1ll << 30)) return false;
+  p.total_units = static_cast<int>(units);
+  p.subtiles = direct ? 1 : static_cast<int>(C.stride_w);
+  if (!direct && C.stride_h <= kMaxPhases) {
+    // row phases with more taps first, so the heaviest units start earliest
+    int order[kMaxPhases], taps[kMaxPhases];
+    for (int ph = 0; ph < C.stride_h; ++ph) {
+      taps[ph] = conv_t_phase_taps(ph, C.pad_h, C.stride_h, C.dil_h, C.Kh);
+      order[ph] = ph;
+    }
+    std::stable_sort(order, order + C.stride_h, [&](int x, int y) { return taps[x] > taps[y]; });
+    for (int i = 0; i < C.stride_h; ++i) p.ph_order[i] = static_cast<int8_t>(order[i]);
+  }
+  p.ws = C.ws;
+  p.bias = C.bias;
+  p.rq = C.rq;
+  p.out = C.out;
+  p.acc_out = C.acc_out;
+  p.store_mode = 0;
+  p.a_bound_dev = nullptr;
+  p.a_bound_host = C.a_bound;
+  // Whole output rows go through shared memory when a unit's rows fit the
+  // stage and split into aligned 16-byte pieces.
+  const int64_t wt = static_cast<int64_t>(bw) * p.osw;
+  const bool staged = C.out != nullptr && C.acc_out == nullptr && bn <= 128 && p.osw <= 2 &&
+                      wt % 16 == 0 && C.W_out % 16 == 0 &&
+                      reinterpret_cast<uintptr_t>(C.out) % 16 == 0;
+  p.staged = staged ? 1 : 0;
+  S.ostage = staged ? 2 * static_cast<size_t>(bn) * kBM * p.osw : 0;  // two alternating
+  S.p = p;
+  S.bn = bn;
+  S.kd = kd;
+  return true;
+}
+
+}  // namespace q8

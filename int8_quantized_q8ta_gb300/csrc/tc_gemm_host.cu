@@ -56,11 +56,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 bool encode_bf16_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                        const uint64_t* strides_bytes, const uint32_t* box) {
+                        const uint64_t* strides_bytes, const uint32_t* box,
+                        const uint32_t* element_strides) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   uint32_t estr[5] = {1, 1, 1, 1, 1};
   if (rank < 1 || rank > 5) return false;
+  if (element_strides != nullptr)
+    for (int i = 0; i < rank; ++i) estr[i] = element_strides[i];
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
                    strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -84,7 +84,7 @@ constexpr int kMaxBN = 256;
 constexpr int kEpFloats = 8 * kMaxBN;  // scale/bias staging (see Ctl::ep)
 
 struct TcParams {
-  int mode;          // 0 = linear, 1 = transposed convolution
+  int mode;          // 0 = linear, 1 = transposed convolution, 2 = direct convolution
   int stages;        // smem ring depth
   int kd;            // k-blocks per ring stage (1 or 2): one TMA box holds kd k-blocks
   int total_units;   // work units; a unit is `subtiles` consecutive tiles
@@ -92,7 +92,16 @@ struct TcParams {
   // linear
   int M, N, kb_total, tiles_m;
   // transposed convolution
-  int Nimg, OC, Kh, Kw, H_out, W_out, sh, sw, pad_h, pad_w, icb, ICp;
+  // (OC: the GEMM's columns, one group's output channels; out_ch: channels
+  // of the output tensor)
+  int Nimg, OC, Kh, Kw, H_out, W_out, sh, sw, pad_h, pad_w, icb, ICp, out_ch;
+  int dil_h, dil_w;
+  // transposed convolution: the row taps of a phase are kh0 + i * tsh and
+  // read input rows dh0 - i * dsh, with gh = gcd(dil_h, sh), tsh = sh / gh,
+  // dsh = dil_h / gh and kh0 = ((ph + pad_h) mod sh / gh) * invh mod tsh,
+  // invh being the inverse of dsh modulo tsh (columns likewise)
+  int gh, gw, tsh, tsw, dsh, dsw, invh, invw;
+  int osh, osw;      // output pixel step of a tile's rows / columns (conv_t: stride; conv2d: 1)
   int BW, BH, tiles_w, tiles_h, tiles_oc;
   int staged;        // conv output goes through the shared-memory stage
   int8_t ph_order[kMaxPhases];  // row phases, most taps first (stride_h <= kMaxPhases)
@@ -123,8 +132,9 @@ struct TileInfo {
                 // past a tap's last channel block holds zeros of A)
   // linear
   int mb, nb;
-  // conv
-  int n, hb, wb, ocb, ph, pw, rh, rw, ntw;
+  // conv: output phase (ph, pw), first taps (rh, rw), tap counts (nth, ntw),
+  // input offsets of the first taps (dh0, dw0)
+  int n, hb, wb, ocb, ph, pw, rh, rw, nth, ntw, dh0, dw0;
 };
 
 // Unit u, sub-tile j -> tile coordinates.  Transposed convolution units are
@@ -142,6 +152,18 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int u, int j,
     ti.nb = u / p.tiles_m;
     ti.num_kb = p.kb_total;
     ti.nstages = (p.kb_total + KD - 1) / KD;
+  } else if constexpr (MODE == 2) {
+    // direct convolution: one output tile of image n, every tap
+    ti.ocb = u % p.tiles_oc;
+    u /= p.tiles_oc;
+    ti.wb = u % p.tiles_w;
+    u /= p.tiles_w;
+    ti.hb = (u % p.tiles_h) * CG + rank;
+    ti.n = u / p.tiles_h;
+    ti.nth = p.Kh;
+    ti.ntw = p.Kw;
+    ti.num_kb = p.Kh * p.Kw * p.icb;
+    ti.nstages = p.Kh * p.Kw * ((p.icb + KD - 1) / KD);
   } else {
     ti.ocb = u % p.tiles_oc;
     u /= p.tiles_oc;
@@ -153,12 +175,22 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int u, int j,
     const int phx = u / p.Nimg;
     ti.ph = (p.sh <= kMaxPhases) ? p.ph_order[phx] : phx;
     ti.pw = j;
-    ti.rh = (ti.ph + p.pad_h) % p.sh;
-    ti.rw = (ti.pw + p.pad_w) % p.sw;
-    const int nth = ti.rh < p.Kh ? (p.Kh - ti.rh + p.sh - 1) / p.sh : 0;
-    ti.ntw = ti.rw < p.Kw ? (p.Kw - ti.rw + p.sw - 1) / p.sw : 0;
-    ti.num_kb = nth * ti.ntw * p.icb;
-    ti.nstages = nth * ti.ntw * ((p.icb + KD - 1) / KD);
+    // first taps: the least kh >= 0 with kh * dil_h = ph + pad_h (mod sh), if any
+    const int th0 = (ti.ph + p.pad_h) % p.sh, tw0 = (ti.pw + p.pad_w) % p.sw;
+    ti.nth = 0;
+    ti.ntw = 0;
+    if (th0 % p.gh == 0) {
+      ti.rh = (th0 / p.gh) * p.invh % p.tsh;
+      ti.nth = ti.rh < p.Kh ? (p.Kh - ti.rh + p.tsh - 1) / p.tsh : 0;
+      ti.dh0 = (ti.ph + p.pad_h - ti.rh * p.dil_h) / p.sh;  // exact
+    }
+    if (tw0 % p.gw == 0) {
+      ti.rw = (tw0 / p.gw) * p.invw % p.tsw;
+      ti.ntw = ti.rw < p.Kw ? (p.Kw - ti.rw + p.tsw - 1) / p.tsw : 0;
+      ti.dw0 = (ti.pw + p.pad_w - ti.rw * p.dil_w) / p.sw;
+    }
+    ti.num_kb = ti.nth * ti.ntw * p.icb;
+    ti.nstages = ti.nth * ti.ntw * ((p.icb + KD - 1) / KD);
   }
   return ti;
 }
@@ -226,7 +258,8 @@ __device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uin
   return ok;
 }
 
-// MODE 0: q8ta_linear tiles; MODE 1: transposed-convolution units.
+// MODE 0: q8ta_linear tiles; MODE 1: transposed-convolution units; MODE 2:
+// direct-convolution tiles.
 // KD: k-blocks per ring stage (one TMA box spans KD k-blocks).
 // CG: 1 = one CTA per 128-row tile (cta_group::1); 2 = a cluster of two CTAs
 // shares one 256-row tile through the 2-SM MMA (cta_group::2): each CTA
@@ -254,7 +287,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
   static_assert((BN / CG) % 8 == 0, "B tiles keep the 1024-byte swizzle-atom alignment");
   static_assert(EPI <= kMaxEpiWarps && kColsPerWarp <= kMaxColsPerWarp, "epilogue smem slices");
   static_assert(MODE != 0 || 4 * BN <= kEpFloats, "linear scale/bias buffers exceed Ctl::ep");
-  static_assert(MODE != 1 || EPI * 2 * kColsPerWarp <= kEpFloats,
+  static_assert(MODE == 0 || EPI * 2 * kColsPerWarp <= kEpFloats,
                 "per-warp scale/bias slices exceed Ctl::ep");
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM * CG, BN);
   constexpr bool kPair = (CG == 2);
@@ -324,17 +357,24 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           // k-blocks in (row tap, column tap, channel block) order, with the
           // input offsets stepped incrementally: no division in this loop.
           // Linear tiles are one "tap" of kb_total channel blocks.
-          const int ntaps_h = (MODE == 0) ? 1 : (ti.num_kb > 0 ? ti.num_kb / (ti.ntw * p.icb) : 0);
+          const int ntaps_h = (MODE == 0) ? 1 : ti.nth;
           const int ntaps_w = (MODE == 0) ? 1 : ti.ntw;
           // channel blocks per tap, KD per stage (a last stage may run past them)
           const int nblk = (MODE == 0) ? ti.num_kb : p.icb;
-          const int dh0 = (MODE == 0) ? 0 : (ti.ph + p.pad_h - ti.rh) / p.sh;
-          const int dw0 = (MODE == 0) ? 0 : (ti.pw + p.pad_w - ti.rw) / p.sw;
-          const int a_w = ti.wb * p.BW, a_h = ti.hb * p.BH;
+          // input coordinates of the tile's first tap: conv_t phases read
+          // (oh' + dh0 - th*dsh); the direct convolution reads
+          // (oh*sh - pad_h + th*dil_h) through a box with element stride sh
+          const int a_w = (MODE == 2) ? ti.wb * p.BW * p.sw - p.pad_w : ti.wb * p.BW + ti.dw0;
+          const int a_h = (MODE == 2) ? ti.hb * p.BH * p.sh - p.pad_h : ti.hb * p.BH + ti.dh0;
+          const int step_w = (MODE == 2) ? p.dil_w : -p.dsw;
+          const int step_h = (MODE == 2) ? p.dil_h : -p.dsh;
           for (int th = 0; th < ntaps_h && ok; ++th) {
             for (int tw = 0; tw < ntaps_w && ok; ++tw) {
-              // tap (kh, kw) = (rh + th*sh, rw + tw*sw) reads input (oh' + dh, ow' + dw)
-              const int b_blk = ((ti.rh + th * p.sh) * p.Kw + ti.rw + tw * p.sw) * p.icb;
+              // tap (kh, kw): conv_t (rh + th*tsh, rw + tw*tsw); conv2d (th, tw)
+              const int b_blk = (MODE == 2)
+                                    ? (th * p.Kw + tw) * p.icb
+                                    : ((ti.rh + th * p.tsh) * p.Kw + ti.rw + tw * p.tsw) * p.icb;
+              const int c_w = a_w + tw * step_w, c_h = a_h + th * step_h;
               for (int blk = 0; blk < nblk; blk += KD) {
                 if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag,
                               kErrWaitEmpty, p.err)) {
@@ -352,7 +392,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                     tma_load_3d_pair(sa, &tmA, full, 0, ti.mb * kBM, blk);
                     tma_load_3d_pair(sb, &tmB, full, 0, b_row, blk);
                   } else {
-                    tma_load_5d_pair(sa, &tmA, full, 0, a_w + dw0 - tw, a_h + dh0 - th, blk, ti.n);
+                    tma_load_5d_pair(sa, &tmA, full, 0, c_w, c_h, blk, ti.n);
                     tma_load_3d_pair(sb, &tmB, full, 0, b_row, b_blk + blk);
                   }
                 } else {
@@ -362,7 +402,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                     tma_load_3d(sa, &tmA, full, 0, ti.mb * kBM, blk);
                     tma_load_3d(sb, &tmB, full, 0, b_row, blk);
                   } else {
-                    tma_load_5d(sa, &tmA, full, 0, a_w + dw0 - tw, a_h + dh0 - th, blk, ti.n);
+                    tma_load_5d(sa, &tmA, full, 0, c_w, c_h, blk, ti.n);
                     tma_load_3d(sb, &tmB, full, 0, b_row, b_blk + blk);
                   }
                 }
@@ -605,16 +645,16 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           }
         } else {
           const int hh = row / p.BW, ww = row % p.BW;
-          const int oh = (ti.hb * p.BH + hh) * p.sh + ti.ph;
-          const int ow = (ti.wb * p.BW + ww) * p.sw + ti.pw;
+          const int oh = (ti.hb * p.BH + hh) * p.osh + ti.ph;
+          const int ow = (ti.wb * p.BW + ww) * p.osw + ti.pw;
           const int oc0 = gcolbase + col0;
           const bool inside = (oh < p.H_out && ow < p.W_out);
           if (p.staged && p.acc_out == nullptr) {
             // stage[oc][hh][wl], wl = ww * sw + pw: one unit's rows, all columns;
             // two stages alternate by unit, so one rendezvous per unit suffices
-            const int wt = p.BW * p.sw;
+            const int wt = p.BW * p.osw;
             uint8_t* stage_base = ostage + unit_par * (BN * p.BH * wt);
-            uint8_t* st = stage_base + hh * wt + ww * p.sw + ti.pw;
+            uint8_t* st = stage_base + hh * wt + ww * p.osw + ti.pw;
 #pragma unroll
             for (int g = 0; g < kColsPerWarp / 16; ++g) {
 #pragma unroll
@@ -633,7 +673,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 st[(ocl + 3) * p.BH * wt] = static_cast<uint8_t>(v3);
               }
             }
-            if (ti.pw == p.sw - 1) {
+            if (ti.pw == p.osw - 1) {
               // every column phase of this unit is staged: write whole rows
               if (!epi_sync(ctl, epi_phase, abort_flag, p.err)) {
                 ok = false;
@@ -647,11 +687,11 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 const int r = it / chunks_per_row, ch = it - r * chunks_per_row;
                 const int ocl = r / p.BH, rh = r - ocl * p.BH;
                 const int oc = ti.ocb * BN + ocl;
-                const int ohh = (ti.hb * p.BH + rh) * p.sh + ti.ph;
+                const int ohh = (ti.hb * p.BH + rh) * p.osh + ti.ph;
                 const int oww = ow0 + 16 * ch;
                 if (oc < p.OC && ohh < p.H_out && oww < p.W_out) {
                   const uint4 v = *reinterpret_cast<const uint4*>(stage_base + r * wt + 16 * ch);
-                  int8_t* dst = p.out + (static_cast<int64_t>(ti.n) * p.OC + oc) * plane +
+                  int8_t* dst = p.out + (static_cast<int64_t>(ti.n) * p.out_ch + oc) * plane +
                                 static_cast<int64_t>(ohh) * p.W_out + oww;
                   *reinterpret_cast<uint4*>(dst) = v;   // W_out % 16 == 0 when staged
                 }
@@ -660,10 +700,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
             }
           } else if (inside) {
             const int64_t plane = static_cast<int64_t>(p.H_out) * p.W_out;
-            int8_t* dst = p.out ? p.out + (static_cast<int64_t>(ti.n) * p.OC + oc0) * plane +
+            int8_t* dst = p.out ? p.out + (static_cast<int64_t>(ti.n) * p.out_ch + oc0) * plane +
                                       static_cast<int64_t>(oh) * p.W_out + ow
                                 : nullptr;
-            int32_t* adst = p.acc_out ? p.acc_out + (static_cast<int64_t>(ti.n) * p.OC + oc0) * plane +
+            int32_t* adst = p.acc_out ? p.acc_out + (static_cast<int64_t>(ti.n) * p.out_ch + oc0) * plane +
                                             static_cast<int64_t>(oh) * p.W_out + ow
                                       : nullptr;
 #pragma unroll

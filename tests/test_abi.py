@@ -65,7 +65,8 @@ def test_linear_guards(name):
     M = 1
     assert _lin(f, M=M, N=30) == q8.Q8_ERR_SHAPE                    # N % 4
     assert _lin(f, M=M, K=63) == q8.Q8_ERR_SHAPE                    # M*K % 4 with M = 1
-    assert _lin(f, M=M, act=b"relu") == q8.Q8_ERR_UNSUPPORTED
+    assert _lin(f, M=M, act=b"gelu") == q8.Q8_ERR_UNSUPPORTED
+    assert _lin(f, M=M, act=b"relu", N=30) == q8.Q8_ERR_SHAPE      # relu passes the activation guard
     assert _lin(f, M=M, act=None) == q8.Q8_ERR_NULL
     assert _lin(f, M=M, ws=None) == q8.Q8_ERR_NULL
     assert _lin(f, M=M, out=None) == q8.Q8_ERR_NULL
@@ -106,7 +107,7 @@ def test_operand_guards():
                                              None) == q8.Q8_ERR_ARG
     assert lib.q8_linear_operand_packed(FAKE, 8, 64, 0.02, FAKE, 30, FAKE, None, 0.1, 0, b"none",
                                         FAKE, None) == q8.Q8_ERR_SHAPE
-    assert lib.q8_linear_operand_packed(FAKE, 8, 64, 0.02, FAKE, 32, FAKE, None, 0.1, 0, b"relu",
+    assert lib.q8_linear_operand_packed(FAKE, 8, 64, 0.02, FAKE, 32, FAKE, None, 0.1, 0, b"tanh",
                                         FAKE, None) == q8.Q8_ERR_UNSUPPORTED
 
 
@@ -123,14 +124,19 @@ def _conv(**kw):
 
 
 def test_conv_t_guards():
-    assert _conv(groups=2) == q8.Q8_ERR_UNSUPPORTED
-    assert _conv(dilation=2) == q8.Q8_ERR_UNSUPPORTED
+    assert _conv(groups=0) == q8.Q8_ERR_UNSUPPORTED
+    assert _conv(dilation=0) == q8.Q8_ERR_UNSUPPORTED
+    assert _conv(groups=2) == q8.Q8_ERR_SHAPE                      # IC = 3 is not divisible
     assert _conv(stride=0) == q8.Q8_ERR_SHAPE
     assert _conv(W_out=9) == q8.Q8_ERR_SHAPE                       # W_out % 4
     assert _conv(w_shape=(4, 26)) == q8.Q8_ERR_SHAPE               # row stride < Kh*Kw*IC
     assert _conv(padding=-1) == q8.Q8_ERR_SHAPE
-    assert _conv(act=b"relu") == q8.Q8_ERR_UNSUPPORTED
+    assert _conv(act=b"gelu") == q8.Q8_ERR_UNSUPPORTED
     assert _conv() == q8.Q8_ERR_WORKSPACE                          # all guards pass
+    assert _conv(act=b"relu") == q8.Q8_ERR_WORKSPACE
+    assert _conv(dilation=2) == q8.Q8_ERR_WORKSPACE
+    # groups = 2 with IC = 4, OC = 4: rows of Kh*Kw*IC/2 = 18
+    assert _conv(x_shape=(1, 4, 5, 4), w_shape=(4, 18), groups=2) == q8.Q8_ERR_WORKSPACE
     s = q8.conv_t_shape((1, 3, 5, 4), (4, 27), 3, 3, 10, 8, 2, 1, 1)
     assert lib.q8_conv2d_transposed(FAKE, None, 0.02, 0, FAKE, None, FAKE, None, 0.1, 0, b"none",
                                     FAKE, None, 0, None) == q8.Q8_ERR_NULL
@@ -142,3 +148,32 @@ def test_binding_refuses_cpu_tensors():
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError, match="CUDA"):
         q8.quantize_per_tensor(torch.zeros(8), 0.1, 0)
+
+
+def _conv2d(**kw):
+    base = dict(x_shape=(1, 3, 6, 8), w_shape=(4, 27), Kh=3, Kw=3, H_out=6, W_out=8, stride=1,
+                padding=1, dilation=1, groups=1)
+    base.update(kw)
+    s = q8.conv2d_shape(base["x_shape"], base["w_shape"], base["Kh"], base["Kw"], base["H_out"],
+                        base["W_out"], base["stride"], base["padding"], base["dilation"],
+                        base["groups"])
+    act = kw.get("act", b"none")
+    return lib.q8_conv2d(FAKE, ctypes.byref(s), 0.02, 0, FAKE, FAKE, None, 0.1, 0, act, FAKE,
+                         None, 0, None)
+
+
+def test_conv2d_guards_and_sizes():
+    assert _conv2d(stride=9) == q8.Q8_ERR_UNSUPPORTED              # TMA element stride <= 8
+    assert _conv2d(stride=0) == q8.Q8_ERR_SHAPE
+    assert _conv2d(W_out=6) == q8.Q8_ERR_SHAPE
+    assert _conv2d(groups=3, w_shape=(4, 9)) == q8.Q8_ERR_SHAPE   # OC = 4 not divisible by 3
+    assert _conv2d(act=b"sigmoid") == q8.Q8_ERR_UNSUPPORTED
+    assert _conv2d() == q8.Q8_ERR_WORKSPACE
+    assert _conv2d(stride=8, act=b"relu") == q8.Q8_ERR_WORKSPACE
+    s = q8.conv2d_shape((2, 96, 10, 12), (64, 9 * 48), 3, 3, 10, 12, 1, 1, 1, 2)
+    # relayout: 2 groups of 48 channels padded to 64; packed weight: 2 x 9 x 32 x 64
+    assert lib.q8_conv2d_packed_workspace_bytes(ctypes.byref(s)) == 2 * 10 * 12 * 128 * 2
+    assert lib.q8_conv2d_packed_weight_bytes(ctypes.byref(s)) == 2 * 9 * 32 * 64 * 2
+    assert lib.q8_conv2d_workspace_bytes(ctypes.byref(s)) == 2 * 10 * 12 * 128 * 2 + 2 * 9 * 32 * 64 * 2
+    bad = q8.conv2d_shape((2, 96, 10, 12), (64, 9 * 48), 3, 3, 10, 10, 1, 1, 1, 2)  # W_out % 4
+    assert lib.q8_conv2d_workspace_bytes(ctypes.byref(bad)) == 0
