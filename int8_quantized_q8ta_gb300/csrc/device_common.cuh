@@ -33,21 +33,28 @@ __device__ __forceinline__ int8_t round_add_clamp(float u, float zp) {
 
 // clamp(rint(u) + zp, -128, 127) with rint half-to-even, as an int32, on
 // plain FP32/INT32 ALU operations (no float<->int conversion instruction):
-//  * u is first clamped to [-2^21, 2^21]; any u beyond that saturates the
-//    result anyway, and fmaxf maps NaN to -2^21, i.e. -128 -- the same value
-//    round_add_clamp gives for NaN;
-//  * adding 1.5 * 2^23 rounds to an integer (round-to-nearest-even: the sum
-//    lies in [2^23, 2^24), where the spacing of floats is exactly 1), and the
-//    integer is the low bits of the sum's encoding: bits(sum) - 0x4B400000.
+//  * u is first raised to at least -2^22 (fmaxf maps NaN to -2^22 too);
+//  * adding 1.5 * 2^23 rounds to an integer (round-to-nearest-even: for
+//    -2^22 <= u < 2^22 the sum lies in [2^23, 2^24), where the spacing of
+//    floats is exactly 1), and the integer is the low bits of the sum's
+//    encoding: bits(sum) - 0x4B400000.  For larger u the encoding only grows
+//    (the sum stays positive), so the clamp saturates at 127 as it should;
+//    for u < -2^22, and NaN, it gives -128 as round_add_clamp does.
 // Equal to round_add_clamp for every float u and every zp in [-128, 127]
 // when lo = -128.  lo = zp gives the relu form: max(v, 0) before the
 // requantization is max(q, zp) after it, v * inv_out being monotone and
 // rint(0) = 0.
-__device__ __forceinline__ int32_t round_add_clamp_i(float u, int32_t zp, int32_t lo) {
-  const float c = fminf(fmaxf(u, -2097152.0f), 2097152.0f);
-  const float y = __fadd_rn(c, 12582912.0f);
+constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23, encoded 0x4B400000
+constexpr float kRoundFloor = -4194304.0f;   // -2^22
+
+__device__ __forceinline__ int32_t magic_to_q(float y, int32_t zp, int32_t lo) {
   const int32_t q = __float_as_int(y) - (0x4B400000 - zp);
   return min(max(q, lo), 127);
+}
+
+__device__ __forceinline__ int32_t round_add_clamp_i(float u, int32_t zp, int32_t lo) {
+  const float y = __fadd_rn(fmaxf(u, kRoundFloor), kRoundMagic);
+  return magic_to_q(y, zp, lo);
 }
 
 // The fused epilogue of one accumulator, in the order of "Add q8ta_linear op"

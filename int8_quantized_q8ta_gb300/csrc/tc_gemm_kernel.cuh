@@ -662,10 +662,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 const float4 w4 = *reinterpret_cast<const float4*>(sws + 16 * g + 4 * q);
                 const float4 b4 = *reinterpret_cast<const float4*>(sbs + 16 * g + 4 * q);
                 const int s0 = 16 * g + 4 * q;
-                const int8_t v0 = requant_one(sum[s0 + 0], w4.x, b4.x, p.rq);
-                const int8_t v1 = requant_one(sum[s0 + 1], w4.y, b4.y, p.rq);
-                const int8_t v2 = requant_one(sum[s0 + 2], w4.z, b4.z, p.rq);
-                const int8_t v3 = requant_one(sum[s0 + 3], w4.w, b4.w, p.rq);
+                const int32_t v0 = requant_i(sum[s0 + 0], w4.x, b4.x, p.rq);
+                const int32_t v1 = requant_i(sum[s0 + 1], w4.y, b4.y, p.rq);
+                const int32_t v2 = requant_i(sum[s0 + 2], w4.z, b4.z, p.rq);
+                const int32_t v3 = requant_i(sum[s0 + 3], w4.w, b4.w, p.rq);
                 const int ocl = col0 + s0;
                 st[(ocl + 0) * p.BH * wt] = static_cast<uint8_t>(v0);
                 st[(ocl + 1) * p.BH * wt] = static_cast<uint8_t>(v1);
@@ -718,10 +718,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 } else {
                   const float4 w4 = *reinterpret_cast<const float4*>(sws + s0);
                   const float4 b4 = *reinterpret_cast<const float4*>(sbs + s0);
-                  const int8_t v[4] = {requant_one(sum[s0 + 0], w4.x, b4.x, p.rq),
-                                       requant_one(sum[s0 + 1], w4.y, b4.y, p.rq),
-                                       requant_one(sum[s0 + 2], w4.z, b4.z, p.rq),
-                                       requant_one(sum[s0 + 3], w4.w, b4.w, p.rq)};
+                  const int32_t v[4] = {requant_i(sum[s0 + 0], w4.x, b4.x, p.rq),
+                                        requant_i(sum[s0 + 1], w4.y, b4.y, p.rq),
+                                        requant_i(sum[s0 + 2], w4.z, b4.z, p.rq),
+                                        requant_i(sum[s0 + 3], w4.w, b4.w, p.rq)};
 #pragma unroll
                   for (int e = 0; e < 4; ++e)
                     if (oc0 + s0 + e < p.OC) dst[(s0 + e) * plane] = v[e];

@@ -1,9 +1,9 @@
 """The CUDA epilogue's conversion-free rounding equals the plain one (CPU).
 
 The GEMM and gemv epilogues compute clamp(rint(u) + zp, -128, 127) without a
-float->int conversion instruction: u is clamped to [-2^21, 2^21], 1.5 * 2^23
+float->int conversion instruction: u is raised to at least -2^22, 1.5 * 2^23
 is added in f32 (round to nearest even), and the integer is read from the
-sum's encoding.  This test replays both forms in numpy float32 -- whose
+sum's encoding, then clamped as an integer.  This test replays both forms in numpy float32 -- whose
 addition rounds to nearest even like the GPU's __fadd_rn -- over every
 rounding tie near the int8 range, their float neighbours, random bit
 patterns (NaN, infinities, subnormals included) and every zero point.
@@ -24,10 +24,13 @@ def plain(u, zp):
 
 
 def alu_only(u, zp):
-    c = np.where(np.isnan(u), F(-2097152.0), u).astype(F)      # fmaxf(NaN, c) = c
-    c = np.minimum(np.maximum(c, F(-2097152.0)), F(2097152.0)).astype(F)
+    c = np.where(np.isnan(u), F(-4194304.0), u).astype(F)      # fmaxf(NaN, c) = c
+    c = np.maximum(c, F(-4194304.0)).astype(F)
     y = (c + F(12582912.0)).astype(F)
-    q = y.view(np.int32).astype(np.int64) - (0x4B400000 - zp)
+    bits = y.view(np.int32).astype(np.int32)
+    assert (bits > 0).all()                                     # y stays positive
+    q = (bits - np.int32(0x4B400000 - zp)).astype(np.int64)    # int32 arithmetic, no overflow
+    assert (q < 2 ** 31).all() and (q >= -2 ** 31).all()
     return np.clip(q, -128, 127).astype(np.int32)
 
 
@@ -37,8 +40,9 @@ def _samples():
     base = np.concatenate([ties, ints]).astype(F)
     up = np.nextafter(base, F(np.inf))
     down = np.nextafter(base, F(-np.inf))
-    big = np.array([2.0 ** 21, 2.0 ** 21 + 0.5, 2.0 ** 22, 2.0 ** 23, 2.0 ** 24, 3.4e38, 1e30,
-                    4194303.5, 8388607.5, 12582912.0], dtype=np.float64)
+    big = np.array([2.0 ** 21, 2.0 ** 21 + 0.5, 2.0 ** 22, 2.0 ** 22 - 0.5, 2.0 ** 22 + 1,
+                    2.0 ** 23, 2.0 ** 24, 3.4e38, 1e30, 4194303.5, 8388607.5, 12582912.0,
+                    12582911.5, 16777215.0], dtype=np.float64)
     big = np.concatenate([big, -big]).astype(F)
     special = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-45, -1e-45, 1e-38], dtype=F)
     rng = np.random.default_rng(7)
