@@ -87,8 +87,8 @@ q8_status q8_quantize_per_tensor(const float* x, int64_t numel, double scale, in
   if (!x || !out) return Q8_ERR_NULL;
   if (numel < 0 || numel % 4 != 0) return Q8_ERR_SHAPE;
   if (!scale_ok(scale) || !zp_ok(zero_point)) return Q8_ERR_ARG;
-  return cuda_status(q8::launch_quantize(x, numel, recip_f32(scale),
-                                         static_cast<float>(zero_point), out, cs(stream)));
+  return cuda_status(q8::launch_quantize(x, numel, recip_f32(scale), zero_point, out,
+                                         cs(stream)));
 }
 
 q8_status q8_dequantize_per_tensor(const int8_t* q, int64_t numel, double scale,

@@ -24,13 +24,6 @@ struct Requant {
   int32_t lo;     // output floor: -128, or ozp_i for activation "relu"
 };
 
-__device__ __forceinline__ int8_t round_add_clamp(float u, float zp) {
-  float r = rintf(u);             // round half to even
-  float t = __fadd_rn(r, zp);
-  t = fminf(fmaxf(t, -128.0f), 127.0f);
-  return (int8_t)__float2int_rz(t);
-}
-
 // clamp(rint(u) + zp, -128, 127) with rint half-to-even, as an int32, on
 // plain FP32/INT32 ALU operations (no float<->int conversion instruction):
 //  * u is first raised to at least -2^22 (fmaxf maps NaN to -2^22 too);
@@ -39,8 +32,10 @@ __device__ __forceinline__ int8_t round_add_clamp(float u, float zp) {
 //    floats is exactly 1), and the integer is the low bits of the sum's
 //    encoding: bits(sum) - 0x4B400000.  For larger u the encoding only grows
 //    (the sum stays positive), so the clamp saturates at 127 as it should;
-//    for u < -2^22, and NaN, it gives -128 as round_add_clamp does.
-// Equal to round_add_clamp for every float u and every zp in [-128, 127]
+//    for u < -2^22, and NaN, it gives -128 (the float form's fmaxf/fminf
+//    clamp gives the same).
+// Equal to the float form -- r = rint(u); t = r + zp; clamp t to
+// [-128, 127]; (int8)t -- for every float u and every zp in [-128, 127]
 // when lo = -128.  lo = zp gives the relu form: max(v, 0) before the
 // requantization is max(q, zp) after it, v * inv_out being monotone and
 // rint(0) = 0.

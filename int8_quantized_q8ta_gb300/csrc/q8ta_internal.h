@@ -22,7 +22,7 @@ inline size_t align_ws(size_t v) { return (v + kWorkspaceAlign - 1) / kWorkspace
 int device_sm_count();
 
 // ---- bandwidth-bound kernels (stream_kernels.cu) --------------------------
-cudaError_t launch_quantize(const float* x, int64_t numel, float inv_scale, float zp, int8_t* out,
+cudaError_t launch_quantize(const float* x, int64_t numel, float inv_scale, int32_t zp, int8_t* out,
                             cudaStream_t s);
 cudaError_t launch_dequantize(const int8_t* q, int64_t numel, float scale, float zp, float* out,
                               cudaStream_t s);

@@ -58,13 +58,15 @@ static int resident_grid(Kernel kernel, int (&cache)[64], int64_t work_items, in
 // Vector path: one float4 in, one packed 32-bit word out per item; U items
 // per thread per round are loaded before any is converted.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int8_t quantize_one(float x, float inv, float zp) {
-  return round_add_clamp(__fmul_rn(x, inv), zp);
+// clamp(rint(x * inv) + zp, -128, 127) on ALU instructions
+// (round_add_clamp_i, equal to the float form for every x; zp in [-128, 127]).
+__device__ __forceinline__ int8_t quantize_one(float x, float inv, int32_t zp) {
+  return static_cast<int8_t>(round_add_clamp_i(__fmul_rn(x, inv), zp, -128));
 }
 
 template <int U>
 __global__ void __launch_bounds__(256) quantize_vec_kernel(const float4* __restrict__ x, int64_t n4,
-                                                           float inv, float zp,
+                                                           float inv, int32_t zp,
                                                            uint32_t* __restrict__ out) {
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * U;
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * U + threadIdx.x; base < n4;
@@ -86,14 +88,14 @@ __global__ void __launch_bounds__(256) quantize_vec_kernel(const float4* __restr
 }
 
 __global__ void __launch_bounds__(256) quantize_scalar_kernel(const float* __restrict__ x, int64_t n,
-                                                              float inv, float zp,
+                                                              float inv, int32_t zp,
                                                               int8_t* __restrict__ out) {
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     out[i] = quantize_one(x[i], inv, zp);
 }
 
-cudaError_t launch_quantize(const float* x, int64_t numel, float inv, float zp, int8_t* out,
+cudaError_t launch_quantize(const float* x, int64_t numel, float inv, int32_t zp, int8_t* out,
                             cudaStream_t s) {
   if (numel == 0) return cudaSuccess;
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
@@ -264,11 +266,15 @@ cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w
 // Operand preparation for the tensor-core GEMM.  int8 values, and the
 // differences x - zp in [-255, 255], are exact in bf16 (8 significant bits).
 // ---------------------------------------------------------------------------
+// On integer and FP32 ALU instructions only (no conversion instruction): for
+// |v| < 2^22, bits(1.5 * 2^23) + v is the encoding of 1.5 * 2^23 + v, so one
+// exact f32 subtraction gives (float)v; with at most 8 significant bits its
+// low 16 encoding bits are zero, and the high 16 are its bf16 encoding.
+__device__ __forceinline__ uint32_t bf16_bits_hi(int v) {
+  return __float_as_uint(__fsub_rn(__int_as_float(0x4B400000 + v), 12582912.0f));
+}
 __device__ __forceinline__ uint32_t bf16x2_from_ints(int lo, int hi) {
-  const __nv_bfloat16 a = __float2bfloat16_rn(static_cast<float>(lo));
-  const __nv_bfloat16 b = __float2bfloat16_rn(static_cast<float>(hi));
-  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+  return __byte_perm(bf16_bits_hi(lo), bf16_bits_hi(hi), 0x7632);
 }
 
 // Destination layout of the GEMM operands ("K-blocked"): dst[kb][r][kk] with
@@ -338,7 +344,7 @@ __global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
     *bound_word = max(128 + zp, 127 - zp);
   const Idx per_row = Kp / 8;
   const Idx total = rows * per_row;
-  const float zpf = static_cast<float>(zp);
+  const int32_t zpf = zp;
   const bool vec = (K % 8 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                    (xq == nullptr || reinterpret_cast<uintptr_t>(xq) % 8 == 0);
   const Idx step = static_cast<Idx>(gridDim.x) * blockDim.x * U;

@@ -61,3 +61,19 @@ def test_alu_rounding_matches_rint_add_clamp_for_every_zero_point():
 def test_ties_round_to_even():
     u = np.array([0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5, -127.5], dtype=F)
     assert alu_only(u, 0).tolist() == [0, 2, 2, 0, -2, -2, 126, -128]
+
+
+def test_bf16_of_small_integers_by_bit_pattern():
+    """The operand preparation forms bf16(v) for v = x - zp in [-255, 255]
+    without a conversion instruction: f = float(bits(1.5 * 2^23) + v) - 1.5 *
+    2^23 (exact), and the bf16 encoding is the high half of f's encoding,
+    whose low half is zero (at most 8 significant bits)."""
+    v = np.arange(-255, 256, dtype=np.int64)
+    f = ((np.int64(0x4B400000) + v).astype(np.int32).view(F) - F(12582912.0)).astype(F)
+    np.testing.assert_array_equal(f, v.astype(F))
+    bits = f.view(np.uint32)
+    assert (bits & 0xFFFF == 0).all()
+    # against a rounding conversion to bfloat16 of the exact float (round to nearest even)
+    u = v.astype(F).view(np.uint32).astype(np.uint64)
+    rne = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint32)
+    np.testing.assert_array_equal(bits >> 16, rne)
