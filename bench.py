@@ -199,65 +199,114 @@ class Path:
             return sum(n.values())
         return {"quantize": 1, "linear": 2, "gemv": 1, "conv_t": 2}[self.only]
 
-    def step(self, ev=None):
-        """Enqueue one step; ev (list of 6 CUDA events) brackets each op."""
+    # the four ops of a step, their activation inputs and outputs (attribute names)
+    OPS = ("quantize", "linear", "gemv", "conv_t")
+    INPUTS = {"quantize": "xq", "linear": "lx", "gemv": "gx", "conv_t": "cx"}
+    OUTPUTS = {"quantize": "q_out", "linear": "l_out", "gemv": "g_out", "conv_t": "c_out"}
+
+    def run_op(self, name, rec=None):
+        """Enqueue one op on the current stream (the linear op is the fused
+        quantize -> operand launch and the GEMM; rec(i) marks between them)."""
         q8, qp, lp, gp, cp = self.q8, Q.params, L.params, G.params, C.params
-        rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
-        rec(0)
-        if self.only in ("all", "quantize"):
+        if name == "quantize":
             q8.quantize_per_tensor(self.xq, qp["in_scale"], qp["in_zp"], out=self.q_out)
-        rec(1)
-        if self.only in ("all", "linear"):
+        elif name == "linear":
             q8.quantize_to_operand(self.lx, lp["in_scale"], lp["in_zp"], x_q=self.l_xq,
                                    operand=self.operand)
-        rec(2)
-        if self.only in ("all", "linear"):
+            if rec:
+                rec()
             q8.linear_operand_packed(self.operand, lp["in_scale"], self.packed, self.lws, self.lb,
                                      lp["out_scale"], lp["out_zp"], out=self.l_out)
-        rec(3)
-        if self.only in ("all", "gemv"):
+        elif name == "gemv":
             q8.linear_gemv(self.gx, gp["in_scale"], gp["in_zp"], self.gw, None, self.gws, self.gb,
                            gp["out_scale"], gp["out_zp"], out=self.g_out)
-        rec(4)
-        if self.only in ("all", "conv_t"):
+        else:
             q8.conv2d_transposed_packed(self.cx, cp["in_scale"], cp["in_zp"], self.c_packed,
                                         self.cws, self.cb, cp["out_scale"], cp["out_zp"],
                                         stride=CD["s"], padding=CD["p"],
                                         output_padding=CD["op"], out=self.c_out,
                                         workspace=self.c_ws)
+
+    def step(self, ev=None):
+        """Enqueue one step; ev (list of 6 CUDA events) brackets each op."""
+        rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
+        rec(0)
+        if self.only in ("all", "quantize"):
+            self.run_op("quantize")
+        rec(1)
+        if self.only in ("all", "linear"):
+            self.run_op("linear", rec=lambda: rec(2))
+        else:
+            rec(2)
+        rec(3)
+        if self.only in ("all", "gemv"):
+            self.run_op("gemv")
+        rec(4)
+        if self.only in ("all", "conv_t"):
+            self.run_op("conv_t")
         rec(5)
 
 
-def e2e_measure(path, h, steps):
-    """Same step through the public API with host buffers: pinned host ->
-    device copies of every activation, the step, device -> pinned host copies
-    of every output, all inside the timed region."""
-    torch = path.torch
+def e2e_measure(paths, h, steps):
+    """The step through the public API with host buffers: every activation is
+    copied in from pinned host memory and every output copied back to pinned
+    host memory, all inside the timed region.  As a user would, the copies
+    run on their own streams and overlap the kernels: op k's inputs go in
+    while op k-1 computes, and its output comes back while op k+1 computes.
+    Two sets of device buffers (``paths``) alternate between steps, so a
+    step's copies never wait for the previous step's kernels on the same
+    buffers; events order every reuse."""
+    torch = paths[0].torch
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    hx = {k: pin(h[k]) for k in ("xq", "lx", "gx", "cx")}
-    dst = {"xq": path.xq, "lx": path.lx, "gx": path.gx, "cx": path.cx}
-    outs = [path.q_out, path.l_out, path.g_out, path.c_out]
-    houts = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    OPS, INP, OUT = Path.OPS, Path.INPUTS, Path.OUTPUTS
+    hx = {op: pin(h[INP[op]]) for op in OPS}
+    houts = {op: torch.empty(getattr(paths[0], OUT[op]).shape,
+                             dtype=getattr(paths[0], OUT[op]).dtype).pin_memory() for op in OPS}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    d2h = sum(t.numel() * t.element_size() for t in houts.values())
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    consumed = {}   # (set, op) -> event: the op's kernels have read that set's inputs
+    drained = {}    # (set, op) -> event: that set's output has been copied out
 
-    def one():
-        for k, t in hx.items():
-            dst[k].copy_(t, non_blocking=True)
-        path.step()
-        for o, ho in zip(outs, houts):
-            ho.copy_(o, non_blocking=True)
+    def one(t):
+        b = t % len(paths)
+        P = paths[b]
+        for op in OPS:
+            with torch.cuda.stream(s_in):
+                if (b, op) in consumed:
+                    s_in.wait_event(consumed[(b, op)])
+                getattr(P, INP[op]).copy_(hx[op], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            with torch.cuda.stream(s_run):
+                s_run.wait_event(ready)
+                if (b, op) in drained:
+                    s_run.wait_event(drained[(b, op)])
+                P.run_op(op)
+                done = torch.cuda.Event()
+                done.record(s_run)
+                consumed[(b, op)] = done
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                houts[op].copy_(getattr(P, OUT[op]), non_blocking=True)
+                out = torch.cuda.Event()
+                out.record(s_out)
+                drained[(b, op)] = out
 
-    for _ in range(2):
-        one()
+    for t in range(2):
+        one(t)
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        one()
-    e.record()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    s_run.wait_stream(s_in)
+    s_out.wait_stream(s_in)
+    for t in range(steps):
+        one(t)
+    s_in.wait_stream(s_run)
+    s_in.wait_stream(s_out)
+    end.record(s_in)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
+    ms = start.elapsed_time(end) / steps
     return ms, h2d, d2h
 
 
@@ -428,12 +477,14 @@ def run_ours(args, rank, world, local_rank):
     if args.only != "all":
         result["config"]["only"] = args.only
     if rank == 0 and not args.no_e2e and args.only == "all":
-        e2e_ms, h2d, d2h = e2e_measure(path, h, max(3, min(K, 10)))
+        e2e_ms, h2d, d2h = e2e_measure([path, Path(h, dev, "all")], h, max(3, min(K, 10)))
         result["e2e"] = {"value": world * OPS_STEP / (e2e_ms * 1e-3) / 1e12,
                          "unit": result["unit"], "ms_per_step": e2e_ms,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "note": "activations copied in from pinned host memory and every output "
-                                 "copied back each step; weights resident"}
+                                 "copied back each step, on copy streams overlapping the "
+                                 "kernels (two alternating device buffer sets); weights "
+                                 "resident"}
     if rank == 0 and not args.no_cpu_baseline and args.only == "all":
         t_cpu, cores, sample, parts = cpu_oracle_step_estimate(h)
         result["cpu_baseline"] = {"value": OPS_STEP / t_cpu / 1e12, "unit": result["unit"],
