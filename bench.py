@@ -406,7 +406,6 @@ def run_ours(args, rank, world, local_rank):
         tdist.barrier()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -414,10 +413,17 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t_start.record()
     for k in range(K):
-        path.step(evs[k])
+        path.step()
     t_end.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    # Per-op times come from a second pass with an event between ops (an
+    # event on the stream also stops one kernel from starting under the
+    # previous one's tail, so these times include each op's own ramp).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for k in range(K):
+        path.step(evs[k])
+    torch.cuda.synchronize()
     if dist:
         tdist.barrier()
     ms_total = t_start.elapsed_time(t_end)

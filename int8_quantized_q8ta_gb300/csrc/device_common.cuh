@@ -82,6 +82,20 @@ __device__ __forceinline__ uint32_t pack4(int8_t a, int8_t b, int8_t c, int8_t d
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization: it may start while the previous
+// kernel on the stream is still finishing.  pdl_wait() returns once that
+// kernel has completed and its memory operations are visible, so a kernel
+// calls it before its first access to global memory (reads and writes);
+// pdl_launch_dependents() lets the next kernel's blocks be scheduled.
+// Outside such a launch both are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Shared memory, mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -21,6 +21,26 @@ inline size_t align_ws(size_t v) { return (v + kWorkspaceAlign - 1) / kWorkspace
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Launch with programmatic stream serialization (the kernel calls
+// pdl_wait() before touching global memory, see device_common.cuh).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // ---- bandwidth-bound kernels (stream_kernels.cu) --------------------------
 cudaError_t launch_quantize(const float* x, int64_t numel, float inv_scale, int32_t zp, int8_t* out,
                             cudaStream_t s);

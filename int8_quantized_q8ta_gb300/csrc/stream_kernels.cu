@@ -68,6 +68,8 @@ template <int U>
 __global__ void __launch_bounds__(256) quantize_vec_kernel(const float4* __restrict__ x, int64_t n4,
                                                            float inv, int32_t zp,
                                                            uint32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * U;
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * U + threadIdx.x; base < n4;
        base += step) {
@@ -90,6 +92,8 @@ __global__ void __launch_bounds__(256) quantize_vec_kernel(const float4* __restr
 __global__ void __launch_bounds__(256) quantize_scalar_kernel(const float* __restrict__ x, int64_t n,
                                                               float inv, int32_t zp,
                                                               int8_t* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     out[i] = quantize_one(x[i], inv, zp);
@@ -105,10 +109,11 @@ cudaError_t launch_quantize(const float* x, int64_t numel, float inv, int32_t zp
     const int64_t n4 = numel / 4;
     static int occ[64];
     const int grid = resident_grid(quantize_vec_kernel<U>, occ, (n4 + U - 1) / U, 256);
-    quantize_vec_kernel<U><<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(x), n4, inv, zp,
-                                                reinterpret_cast<uint32_t*>(out));
+    return launch_pdl(quantize_vec_kernel<U>, grid, 256, 0, s, reinterpret_cast<const float4*>(x),
+                      n4, inv, zp, reinterpret_cast<uint32_t*>(out));
   } else {
-    quantize_scalar_kernel<<<stream_grid(numel, 256, 8), 256, 0, s>>>(x, numel, inv, zp, out);
+    return launch_pdl(quantize_scalar_kernel, stream_grid(numel, 256, 8), 256, 0, s, x, numel, inv,
+                      zp, out);
   }
   return cudaGetLastError();
 }
@@ -119,6 +124,8 @@ cudaError_t launch_quantize(const float* x, int64_t numel, float inv, int32_t zp
 __global__ void __launch_bounds__(256) dequantize_kernel(const int8_t* __restrict__ q, int64_t n,
                                                          float scale, float zp,
                                                          float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const bool vec = (reinterpret_cast<uintptr_t>(q) % 4 == 0) &&
                    (reinterpret_cast<uintptr_t>(out) % 16 == 0);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -151,7 +158,8 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const int8_t* __restric
 cudaError_t launch_dequantize(const int8_t* q, int64_t numel, float scale, float zp, float* out,
                               cudaStream_t s) {
   if (numel == 0) return cudaSuccess;
-  dequantize_kernel<<<stream_grid(numel / 4 + 1, 256, 8), 256, 0, s>>>(q, numel, scale, zp, out);
+  return launch_pdl(dequantize_kernel, stream_grid(numel / 4 + 1, 256, 8), 256, 0, s, q, numel,
+                    scale, zp, out);
   return cudaGetLastError();
 }
 
@@ -177,6 +185,17 @@ __global__ void __launch_bounds__(128) gemv_kernel(const int8_t* __restrict__ x,
   __shared__ int8_t res[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 4 + warp;
+  // The weight row is requested into L2 before waiting for the previous
+  // kernel: L2 is where the GPU's memory is coherent, so a prefetch can never
+  // return stale data to the loads below, and the row's DRAM latency overlaps
+  // the previous kernel's tail.
+  if (n < N) {
+    const int8_t* wr = w + static_cast<int64_t>(n) * K;
+    for (int off = lane * 128; off < K; off += 32 * 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(wr + off));
+  }
+  pdl_wait();
+  pdl_launch_dependents();
   int dot = 0, wsum = 0;
   if (n < N) {
     const int8_t* wr = w + static_cast<int64_t>(n) * K;
@@ -254,11 +273,14 @@ cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w
   const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(w);
   // 16-byte loads need every row start 16-byte aligned, hence K % 16 == 0.
   if (xa % 16 == 0 && wa % 16 == 0 && K % 16 == 0)
-    gemv_kernel<16><<<grid, 128, 0, s>>>(x, (int)K, izp, w, (int)N, ws, bias, rq, out);
+    return launch_pdl(gemv_kernel<16>, grid, 128, 0, s, x, (int)K, izp, w, (int)N, ws, bias, rq,
+                      out);
   else if (xa % 4 == 0 && wa % 4 == 0 && K % 4 == 0)
-    gemv_kernel<4><<<grid, 128, 0, s>>>(x, (int)K, izp, w, (int)N, ws, bias, rq, out);
+    return launch_pdl(gemv_kernel<4>, grid, 128, 0, s, x, (int)K, izp, w, (int)N, ws, bias, rq,
+                      out);
   else
-    gemv_kernel<1><<<grid, 128, 0, s>>>(x, (int)K, izp, w, (int)N, ws, bias, rq, out);
+    return launch_pdl(gemv_kernel<1>, grid, 128, 0, s, x, (int)K, izp, w, (int)N, ws, bias, rq,
+                      out);
   return cudaGetLastError();
 }
 
@@ -290,6 +312,8 @@ __global__ void __launch_bounds__(256) rows_to_bf16_kernel(const int8_t* __restr
                                                            int64_t rows, int64_t K, int64_t ld,
                                                            int32_t zp, uint4* __restrict__ dst,
                                                            int64_t Kp, int32_t* bound_word) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (bound_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
     *bound_word = max(128 + zp, 127 - zp);
   const int64_t per_row = Kp / 8;
@@ -326,8 +350,8 @@ cudaError_t launch_rows_to_bf16(const int8_t* src, int64_t rows, int64_t K, int6
                                 int32_t* bound_word) {
   if (rows == 0) return cudaSuccess;
   const int64_t items = rows * (Kp / 8);
-  rows_to_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
-      src, rows, K, ld, zp, reinterpret_cast<uint4*>(dst), Kp, bound_word);
+  return launch_pdl(rows_to_bf16_kernel, stream_grid(items, 256, 8), 256, 0, s, src, rows, K, ld,
+                    zp, reinterpret_cast<uint4*>(dst), Kp, bound_word);
   return cudaGetLastError();
 }
 
@@ -340,6 +364,8 @@ template <int U, typename Idx>
 __global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
     const float* __restrict__ x, Idx rows, Idx K, float inv, int32_t zp,
     int8_t* __restrict__ xq, uint4* __restrict__ dst, Idx Kp, int32_t* bound_word) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (bound_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
     *bound_word = max(128 + zp, 127 - zp);
   const Idx per_row = Kp / 8;
@@ -415,14 +441,14 @@ cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, f
   if (items + 256 * U < (int64_t(1) << 31)) {
     static int occ[64];
     const int grid = resident_grid(quantize_rows_bf16_kernel<U, uint32_t>, occ, (items + U - 1) / U, 256);
-    quantize_rows_bf16_kernel<U, uint32_t><<<grid, 256, 0, s>>>(
-        x, static_cast<uint32_t>(rows), static_cast<uint32_t>(K), inv, zp, xq,
-        reinterpret_cast<uint4*>(dst), static_cast<uint32_t>(Kp), bound_word);
+    return launch_pdl(quantize_rows_bf16_kernel<U, uint32_t>, grid, 256, 0, s, x,
+                      static_cast<uint32_t>(rows), static_cast<uint32_t>(K), inv, zp, xq,
+                      reinterpret_cast<uint4*>(dst), static_cast<uint32_t>(Kp), bound_word);
   } else {
     static int occ[64];
     const int grid = resident_grid(quantize_rows_bf16_kernel<U, int64_t>, occ, (items + U - 1) / U, 256);
-    quantize_rows_bf16_kernel<U, int64_t><<<grid, 256, 0, s>>>(
-        x, rows, K, inv, zp, xq, reinterpret_cast<uint4*>(dst), Kp, bound_word);
+    return launch_pdl(quantize_rows_bf16_kernel<U, int64_t>, grid, 256, 0, s, x, rows, K, inv, zp,
+                      xq, reinterpret_cast<uint4*>(dst), Kp, bound_word);
   }
   return cudaGetLastError();
 }
@@ -441,6 +467,8 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __
                                                                 Idx H, int64_t W, int32_t zp,
                                                                 uint4* __restrict__ dst,
                                                                 int64_t ICgp) {
+  pdl_wait();
+  pdl_launch_dependents();
   const Idx W4 = static_cast<Idx>((W + 3) / 4);
   const Idx CBg = static_cast<Idx>(ICgp / 64);
   const Idx CB = CBg * static_cast<Idx>(groups);
@@ -501,14 +529,14 @@ cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t groups,
   if (items + 256 < (int64_t(1) << 31)) {
     static int occ[64];
     const int grid = resident_grid(nchw_to_nhwc_bf16_kernel<uint32_t>, occ, items, 256);
-    nchw_to_nhwc_bf16_kernel<uint32_t><<<grid, 256, 0, s>>>(
-        x, static_cast<uint32_t>(N * H), groups, ICg, static_cast<uint32_t>(H), W, zp,
-        reinterpret_cast<uint4*>(dst), ICgp);
+    return launch_pdl(nchw_to_nhwc_bf16_kernel<uint32_t>, grid, 256, 0, s, x,
+                      static_cast<uint32_t>(N * H), groups, ICg, static_cast<uint32_t>(H), W, zp,
+                      reinterpret_cast<uint4*>(dst), ICgp);
   } else {
     static int occ[64];
     const int grid = resident_grid(nchw_to_nhwc_bf16_kernel<int64_t>, occ, items, 256);
-    nchw_to_nhwc_bf16_kernel<int64_t><<<grid, 256, 0, s>>>(
-        x, N * H, groups, ICg, H, W, zp, reinterpret_cast<uint4*>(dst), ICgp);
+    return launch_pdl(nchw_to_nhwc_bf16_kernel<int64_t>, grid, 256, 0, s, x, N * H, groups, ICg, H,
+                      W, zp, reinterpret_cast<uint4*>(dst), ICgp);
   }
   return cudaGetLastError();
 }
@@ -523,6 +551,8 @@ __global__ void __launch_bounds__(256) conv_weight_bf16_kernel(const int8_t* __r
                                                                int64_t ldw,
                                                                uint32_t* __restrict__ dst,
                                                                int64_t ICgp) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t icb = ICgp / 64;
   const int64_t total = groups * taps * icb * OCg * 32;  // bf16 pairs
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -548,8 +578,8 @@ cudaError_t launch_conv_weight_bf16(const int8_t* w, int64_t groups, int64_t OCg
                                     cudaStream_t s) {
   const int64_t items = groups * OCg * taps * ICgp / 2;
   if (items == 0) return cudaSuccess;
-  conv_weight_bf16_kernel<<<stream_grid(items, 256, 8), 256, 0, s>>>(
-      w, groups, OCg, taps, ICg, ldw, reinterpret_cast<uint32_t*>(dst), ICgp);
+  return launch_pdl(conv_weight_bf16_kernel, stream_grid(items, 256, 8), 256, 0, s, w, groups, OCg,
+                    taps, ICg, ldw, reinterpret_cast<uint32_t*>(dst), ICgp);
   return cudaGetLastError();
 }
 

@@ -344,6 +344,9 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
   if constexpr (kPair) cluster_sync_all();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  // set-up done: from here on global memory is read and written
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -785,13 +788,17 @@ inline cudaError_t launch_tc_kernel(const CUtensorMap& a, const CUtensorMap& b, 
   cfg.blockDim = dim3(static_cast<unsigned>(cta_threads(EPI)), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CG;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the set-up above the kernel's pdl_wait()
+  // overlaps the previous kernel on the stream
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // persistent: one CTA per SM, or one CTA pair per co-resident SM pair (a
   // pair must share a GPC, so fewer than SMs / 2 pairs may fit at once)
   int resident = device_sm_count() / CG;
