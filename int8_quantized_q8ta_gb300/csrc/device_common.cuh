@@ -55,14 +55,19 @@ __device__ __forceinline__ int32_t round_add_clamp_i(float u, int32_t zp, int32_
 // The fused epilogue of one accumulator, in the order of "Add q8ta_linear op"
 // (Solution paragraph): ((acc * input_scale) * weight_scale + bias) *
 // (1 / output_scale), rounded, plus the output zero point, clamped (from
-// below at the zero point under the relu activation).
-__device__ __forceinline__ int32_t requant_i(int32_t acc, float ws, float b, const Requant& rq) {
-  float a = __int2float_rn(acc);
+// below at the zero point under the relu activation).  requant_f takes
+// a = (float)acc.
+__device__ __forceinline__ int32_t requant_f(float a, float ws, float b, const Requant& rq) {
   float t = __fmul_rn(a, rq.s_in);
   t = __fmul_rn(t, ws);
   float v = __fadd_rn(t, b);
   float u = __fmul_rn(v, rq.inv_out);
   return round_add_clamp_i(u, rq.ozp_i, rq.lo);
+}
+
+// From the int32 accumulator: a = (float)acc, rounded to nearest even.
+__device__ __forceinline__ int32_t requant_i(int32_t acc, float ws, float b, const Requant& rq) {
+  return requant_f(__int2float_rn(acc), ws, b, rq);
 }
 
 __device__ __forceinline__ int8_t requant_one(int32_t acc, float ws, float b, const Requant& rq) {

@@ -550,6 +550,13 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           sws = slice;
           sbs = slice + kColsPerWarp;
         }
+        // A convolution tile of a single exact chunk keeps the f32
+        // accumulator as it is (an exact integer: converting it to int32 and
+        // back would return the same value); longer tiles add the chunks as
+        // int32.  (Only where the column slice is small: the extra path
+        // costs registers that the wide linear slices do not have.)
+        constexpr bool kSingleChunkPath = (MODE != 0) && (kColsPerWarp <= 64);
+        const bool single = kSingleChunkPath && ti.nstages <= chunk_st;
         int32_t sum[kColsPerWarp];
 #pragma unroll
         for (int c = 0; c < kColsPerWarp; ++c) sum[c] = 0;
@@ -574,11 +581,16 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               tmem_ld_16cols(tmem_base + lane_addr + buf * kAccStride + col0 + kDrainCols * c + 16 * h,
                              *reinterpret_cast<uint32_t(*)[16]>(&r[16 * h]));
             tmem_ld_wait();
+            if (single) {
 #pragma unroll
-            for (int i = 0; i < kDrainCols; ++i)
-              sum[kDrainCols * c + i] = static_cast<int32_t>(
-                  static_cast<uint32_t>(sum[kDrainCols * c + i]) +
-                  static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i]))));
+              for (int i = 0; i < kDrainCols; ++i) sum[kDrainCols * c + i] = static_cast<int32_t>(r[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < kDrainCols; ++i)
+                sum[kDrainCols * c + i] = static_cast<int32_t>(
+                    static_cast<uint32_t>(sum[kDrainCols * c + i]) +
+                    static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i]))));
+            }
           }
           tc_fence_before();
           __syncwarp();
@@ -592,6 +604,18 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           ++acc_it;
         }
         if (!ok) break;
+        // sum[] in one form for what follows: int32 accumulators for the
+        // acc_out debug output, else the f32 value (float(acc), rounded to
+        // nearest even when |acc| > 2^24) the requantization starts from
+        if (p.acc_out != nullptr) {
+          if (single) {
+#pragma unroll
+            for (int c = 0; c < kColsPerWarp; ++c) sum[c] = __float2int_rn(__int_as_float(sum[c]));
+          }
+        } else if (!single) {
+#pragma unroll
+          for (int c = 0; c < kColsPerWarp; ++c) sum[c] = __float_as_int(__int2float_rn(sum[c]));
+        }
 
         // ---- fused epilogue
         if constexpr (MODE == 0) {
@@ -628,10 +652,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                   const float4 w4 = *reinterpret_cast<const float4*>(sws + 16 * g + 4 * q);
                   const float4 b4 = *reinterpret_cast<const float4*>(sbs + 16 * g + 4 * q);
                   const int s0 = 16 * g + 4 * q;
-                  wds[q] = pack4_i(requant_i(sum[s0 + 0], w4.x, b4.x, p.rq),
-                                   requant_i(sum[s0 + 1], w4.y, b4.y, p.rq),
-                                   requant_i(sum[s0 + 2], w4.z, b4.z, p.rq),
-                                   requant_i(sum[s0 + 3], w4.w, b4.w, p.rq));
+                  wds[q] = pack4_i(requant_f(__int_as_float(sum[s0 + 0]), w4.x, b4.x, p.rq),
+                                   requant_f(__int_as_float(sum[s0 + 1]), w4.y, b4.y, p.rq),
+                                   requant_f(__int_as_float(sum[s0 + 2]), w4.z, b4.z, p.rq),
+                                   requant_f(__int_as_float(sum[s0 + 3]), w4.w, b4.w, p.rq));
                 }
                 if (p.store_mode == 2 && c + 16 <= p.N) {
                   *reinterpret_cast<uint4*>(dst + c) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
@@ -665,10 +689,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 const float4 w4 = *reinterpret_cast<const float4*>(sws + 16 * g + 4 * q);
                 const float4 b4 = *reinterpret_cast<const float4*>(sbs + 16 * g + 4 * q);
                 const int s0 = 16 * g + 4 * q;
-                const int32_t v0 = requant_i(sum[s0 + 0], w4.x, b4.x, p.rq);
-                const int32_t v1 = requant_i(sum[s0 + 1], w4.y, b4.y, p.rq);
-                const int32_t v2 = requant_i(sum[s0 + 2], w4.z, b4.z, p.rq);
-                const int32_t v3 = requant_i(sum[s0 + 3], w4.w, b4.w, p.rq);
+                const int32_t v0 = requant_f(__int_as_float(sum[s0 + 0]), w4.x, b4.x, p.rq);
+                const int32_t v1 = requant_f(__int_as_float(sum[s0 + 1]), w4.y, b4.y, p.rq);
+                const int32_t v2 = requant_f(__int_as_float(sum[s0 + 2]), w4.z, b4.z, p.rq);
+                const int32_t v3 = requant_f(__int_as_float(sum[s0 + 3]), w4.w, b4.w, p.rq);
                 const int ocl = col0 + s0;
                 st[(ocl + 0) * p.BH * wt] = static_cast<uint8_t>(v0);
                 st[(ocl + 1) * p.BH * wt] = static_cast<uint8_t>(v1);
@@ -686,9 +710,9 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               const int rows_total = BN * p.BH;
               const int64_t plane = static_cast<int64_t>(p.H_out) * p.W_out;
               const int ow0 = ti.wb * wt;
-              for (int it = et; it < rows_total * chunks_per_row; it += kEpiThreads) {
-                const int r = it / chunks_per_row, ch = it - r * chunks_per_row;
-                const int ocl = r / p.BH, rh = r - ocl * p.BH;
+              const int bh_log = __ffs(p.BH) - 1;  // BH = 128 / BW, a power of two
+              auto store_row_chunk = [&](int r, int ch) {
+                const int ocl = r >> bh_log, rh = r & (p.BH - 1);
                 const int oc = ti.ocb * BN + ocl;
                 const int ohh = (ti.hb * p.BH + rh) * p.osh + ti.ph;
                 const int oww = ow0 + 16 * ch;
@@ -697,6 +721,17 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                   int8_t* dst = p.out + (static_cast<int64_t>(ti.n) * p.out_ch + oc) * plane +
                                 static_cast<int64_t>(ohh) * p.W_out + oww;
                   *reinterpret_cast<uint4*>(dst) = v;   // W_out % 16 == 0 when staged
+                }
+              };
+              if (kEpiThreads % chunks_per_row == 0) {
+                // each thread keeps one chunk column: one division per unit
+                const int ch = et % chunks_per_row, step_r = kEpiThreads / chunks_per_row;
+                for (int r = et / chunks_per_row; r < rows_total; r += step_r)
+                  store_row_chunk(r, ch);
+              } else {
+                for (int it = et; it < rows_total * chunks_per_row; it += kEpiThreads) {
+                  const int r = it / chunks_per_row;
+                  store_row_chunk(r, it - r * chunks_per_row);
                 }
               }
               unit_par ^= 1u;
@@ -721,10 +756,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 } else {
                   const float4 w4 = *reinterpret_cast<const float4*>(sws + s0);
                   const float4 b4 = *reinterpret_cast<const float4*>(sbs + s0);
-                  const int32_t v[4] = {requant_i(sum[s0 + 0], w4.x, b4.x, p.rq),
-                                        requant_i(sum[s0 + 1], w4.y, b4.y, p.rq),
-                                        requant_i(sum[s0 + 2], w4.z, b4.z, p.rq),
-                                        requant_i(sum[s0 + 3], w4.w, b4.w, p.rq)};
+                  const int32_t v[4] = {requant_f(__int_as_float(sum[s0 + 0]), w4.x, b4.x, p.rq),
+                                        requant_f(__int_as_float(sum[s0 + 1]), w4.y, b4.y, p.rq),
+                                        requant_f(__int_as_float(sum[s0 + 2]), w4.z, b4.z, p.rq),
+                                        requant_f(__int_as_float(sum[s0 + 3]), w4.w, b4.w, p.rq)};
 #pragma unroll
                   for (int e = 0; e < 4; ++e)
                     if (oc0 + s0 + e < p.OC) dst[(s0 + e) * plane] = v[e];
