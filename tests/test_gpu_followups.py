@@ -167,3 +167,53 @@ def test_conv2d_acc32_exact_at_the_chunk_bound():
     ref = oracle.conv2d_acc(x, 0, w, K, K, 8, 8, (1, 1), (1, 1))
     got = H(q8.conv2d_acc32(T(x), 0, T(w), K, (8, 8), stride=1, padding=1))
     np.testing.assert_array_equal(got, ref)
+
+
+# ------------------------------------------------- back-to-back launches
+
+def test_dependent_launches_back_to_back():
+    """Every kernel starts under the previous one's tail (programmatic
+    dependent launch) and waits for it before touching global memory.  A
+    chain where each op consumes the previous op's output, enqueued without
+    host synchronisation, checks that ordering: quantize -> linear (reading
+    the quantized activations) -> linear again (reading that output) ->
+    gemv -> conv2d on the reshaped result, then the same chain again into
+    the same buffers."""
+    M, K, N = 256, 512, 512
+    xf = synth.normal(71, "x", (M, K), 0.0, 3.0)
+    w1 = synth.int8_uniform(71, "w1", (N, K), -127, 127)
+    w2 = synth.int8_uniform(71, "w2", (N, N), -127, 127)
+    ws1 = synth.uniform_float(71, "s1", (N,), 0.001, 0.005)
+    ws2 = synth.uniform_float(71, "s2", (N,), 0.001, 0.005)
+    b = synth.normal(71, "b", (N,), 0.0, 0.1)
+    g_w = synth.int8_uniform(71, "gw", (64, N), -127, 127)
+    cw = synth.int8_uniform(71, "cw", (8, 9 * 16), -127, 127)
+    c_ws = synth.uniform_float(71, "cs", (8,), 0.002, 0.01)
+    # oracle chain
+    xq = oracle.quantize_per_tensor(xf, 0.03, -5)
+    y1 = oracle.linear(xq, 0.03, -5, w1, ws1, b, 0.1, 1)
+    y2 = oracle.linear(y1, 0.1, 1, w2, ws2, b, 0.2, -2, activation="relu")
+    g = oracle.linear(y2[:1], 0.2, -2, g_w, ws1[:64], b[:64], 0.5, 0)
+    ximg = y2.reshape(8, 16, 32, 32)[:1]
+    c = oracle.conv2d(ximg, 0.2, -2, cw, 3, 3, c_ws, None, 0.3, 3, 32, 32, (1, 1), (1, 1))
+    # GPU chain, twice into the same buffers, one stream, no host sync inside
+    Txf, Tw1, Tw2, Tgw, Tcw = T(xf), T(w1), T(w2), T(g_w), T(cw)
+    Tws1, Tws2, Tb, Tcws = T(ws1), T(ws2), T(b), T(c_ws)
+    p1, p2 = q8.pack_weight(Tw1), q8.pack_weight(Tw2)
+    q_out = torch.empty((M, K), dtype=torch.int8, device=DEV)
+    y1_d = torch.empty((M, N), dtype=torch.int8, device=DEV)
+    y2_d = torch.empty((M, N), dtype=torch.int8, device=DEV)
+    g_d = torch.empty((1, 64), dtype=torch.int8, device=DEV)
+    c_d = torch.empty((1, 8, 32, 32), dtype=torch.int8, device=DEV)
+    for _ in range(2):
+        q8.quantize_per_tensor(Txf, 0.03, -5, out=q_out)
+        q8.linear_packed(q_out, 0.03, -5, p1, Tws1, Tb, 0.1, 1, out=y1_d)
+        q8.linear_packed(y1_d, 0.1, 1, p2, Tws2, Tb, 0.2, -2, activation="relu", out=y2_d)
+        q8.linear_gemv(y2_d[:1], 0.2, -2, Tgw, None, Tws1[:64], Tb[:64], 0.5, 0, out=g_d)
+        q8.conv2d(y2_d.view(8, 16, 32, 32)[:1], 0.2, -2, Tcw, Tcws, None, 0.3, 3, 3, padding=1,
+                  out=c_d)
+    np.testing.assert_array_equal(H(q_out), xq)
+    np.testing.assert_array_equal(H(y1_d), y1)
+    np.testing.assert_array_equal(H(y2_d), y2)
+    np.testing.assert_array_equal(H(g_d), g)
+    np.testing.assert_array_equal(H(c_d), c)
