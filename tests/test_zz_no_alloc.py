@@ -41,12 +41,12 @@ def _case(seed, M, K, N, izp):
     return T(x), T(w), T(ws), T(b), izp
 
 
-def _noalloc(x, w, ws, b, izp, out):
+def _noalloc(x, w, ws, b, izp, out, act=b"none"):
     M, K = x.shape
     N = w.shape[0]
     stream = ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)
     return q8.lib().q8_linear_noalloc(_ptr(x), M, K, 0.03, izp, _ptr(w), N, None, _ptr(ws),
-                                      _ptr(b), 0.1, 1, b"none", _ptr(out), stream)
+                                      _ptr(b), 0.1, 1, act, _ptr(out), stream)
 
 
 def test_noalloc_matches_q8_linear_on_two_calls():
@@ -60,6 +60,12 @@ def test_noalloc_matches_q8_linear_on_two_calls():
         ref = q8.linear(x, 0.03, izp, w, None, ws, b, 0.1, 1)
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
+    # the relu activation through the same scratch
+    out = torch.empty((M, N), dtype=torch.int8, device=DEV)
+    assert _noalloc(x, w, ws, b, izp, out, b"relu") == q8.Q8_OK
+    ref = q8.linear(x, 0.03, izp, w, None, ws, b, 0.1, 1, activation="relu")
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
     assert q8.device_error(clear=True) == 0
 
 
