@@ -88,7 +88,8 @@ q8_status q8_device_error(uint32_t* code, int clear);
  * out[i] = clamp(rint(x[i] * inv_scale) + zero_point, -128, 127).
  * x: float32[numel]; out: int8[numel].
  * Guards (as on the page): x, out non-NULL; numel % 4 == 0 (the page's
- * packed-word binding); numel >= 0 (0 is a no-op).
+ * packed-word binding); numel >= 0 (0 is a no-op, and then the pointers
+ * may be NULL).
  */
 q8_status q8_quantize_per_tensor(const float* x, int64_t numel, double scale,
                                  int32_t zero_point, int8_t* out, q8_stream_t stream);

@@ -84,18 +84,20 @@ q8_status q8_device_error(uint32_t* code, int clear) {
 // ---------------------------------------------------------------- quantize
 q8_status q8_quantize_per_tensor(const float* x, int64_t numel, double scale, int32_t zero_point,
                                  int8_t* out, q8_stream_t stream) {
-  if (!x || !out) return Q8_ERR_NULL;
   if (numel < 0 || numel % 4 != 0) return Q8_ERR_SHAPE;
   if (!scale_ok(scale) || !zp_ok(zero_point)) return Q8_ERR_ARG;
+  if (numel == 0) return Q8_OK;  // nothing to read or write
+  if (!x || !out) return Q8_ERR_NULL;
   return cuda_status(q8::launch_quantize(x, numel, recip_f32(scale), zero_point, out,
                                          cs(stream)));
 }
 
 q8_status q8_dequantize_per_tensor(const int8_t* q, int64_t numel, double scale,
                                    int32_t zero_point, float* out, q8_stream_t stream) {
-  if (!q || !out) return Q8_ERR_NULL;
   if (numel < 0 || numel % 4 != 0) return Q8_ERR_SHAPE;
   if (!scale_ok(scale) || !zp_ok(zero_point)) return Q8_ERR_ARG;
+  if (numel == 0) return Q8_OK;  // nothing to read or write
+  if (!q || !out) return Q8_ERR_NULL;
   return cuda_status(q8::launch_dequantize(q, numel, static_cast<float>(scale),
                                            static_cast<float>(zero_point), out, cs(stream)));
 }

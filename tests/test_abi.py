@@ -45,6 +45,8 @@ def test_quantize_guards():
     f = lib.q8_quantize_per_tensor
     assert f(None, 4, 0.1, 0, FAKE, None) == q8.Q8_ERR_NULL
     assert f(FAKE, 4, 0.1, 0, None, None) == q8.Q8_ERR_NULL
+    assert f(None, 0, 0.1, 0, None, None) == q8.Q8_OK               # empty: nothing to do
+    assert lib.q8_dequantize_per_tensor(None, 0, 0.1, 0, None, None) == q8.Q8_OK
     assert f(FAKE, 6, 0.1, 0, FAKE, None) == q8.Q8_ERR_SHAPE        # numel % 4
     assert f(FAKE, -4, 0.1, 0, FAKE, None) == q8.Q8_ERR_SHAPE
     assert f(FAKE, 4, 0.0, 0, FAKE, None) == q8.Q8_ERR_ARG

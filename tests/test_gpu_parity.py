@@ -296,3 +296,74 @@ def test_conv_t_8x256x64x64_sampled():
                                        ws[ocs], b[ocs], p["out_scale"], p["out_zp"], Ho, Wo,
                                        (2, 2), (1, 1))
         np.testing.assert_array_equal(got[n:n + 1, ocs], ref)
+
+
+# ------------------------------------------------- empty and large sizes
+
+def test_quantize_and_dequantize_empty():
+    x = torch.empty(0, dtype=torch.float32, device=DEV)
+    assert q8.quantize_per_tensor(x, 0.1, 0).numel() == 0
+    q = torch.empty((0, 4), dtype=torch.int8, device=DEV)
+    assert q8.dequantize_per_tensor(q, 0.1, 0).shape == (0, 4)
+
+
+def _pattern_f32(idx):
+    """x[i] = ((i mod 509) - 254) * 0.0173 in float32 (both sides compute it)."""
+    return ((idx % 509) - 254).astype(np.float32) * np.float32(0.0173)
+
+
+def test_quantize_beyond_2_pow_31_elements():
+    """64-bit element indexing: 2^31 + 8 elements (8.6 GB of fp32), filled on
+    the device with a closed-form pattern and checked at sampled indices,
+    including the last ones."""
+    n = (1 << 31) + 8
+    x = torch.empty(n, dtype=torch.float32, device=DEV)
+    blk = 1 << 26
+    for b0 in range(0, n, blk):
+        idx = torch.arange(b0, min(n, b0 + blk), device=DEV, dtype=torch.int64)
+        x[b0:b0 + idx.numel()] = ((idx % 509) - 254).to(torch.float32) * 0.0173
+    out = q8.quantize_per_tensor(x, 0.05, 3)
+    rng = np.random.default_rng(0)
+    sample = np.concatenate([np.arange(0, 64), np.arange(n - 64, n),
+                             np.arange((1 << 31) - 32, (1 << 31) + 8),
+                             rng.integers(0, n, 4096)]).astype(np.int64)
+    got = H(out[torch.from_numpy(sample).to(DEV)])
+    ref = oracle.quantize_per_tensor(_pattern_f32(sample), 0.05, 3)
+    np.testing.assert_array_equal(got, ref)
+    del x, out
+
+
+def test_linear_output_beyond_2_pow_31_bytes():
+    """A linear whose int8 output holds more than 2^31 bytes (M * N > 2^31):
+    64-bit output addressing in the GEMM epilogue, checked on sampled rows."""
+    M, K, N = 70000, 64, 32768
+    x = synth.int8_uniform(81, "x", (M, K), -128, 127)
+    w = synth.int8_uniform(81, "w", (N, K), -127, 127)
+    ws = synth.uniform_float(81, "ws", (N,), 0.001, 0.005)
+    b = synth.normal(81, "b", (N,), 0.0, 0.1)
+    out = q8.linear_packed(T(x), 0.03, -1, q8.pack_weight(T(w)), T(ws), T(b), 0.1, 2)
+    rows = np.array([0, 1, 255, 256, 65535, 65536, M - 2, M - 1], dtype=np.int64)
+    got = H(out[torch.from_numpy(rows).to(DEV)])
+    np.testing.assert_array_equal(got, oracle.linear(x[rows], 0.03, -1, w, ws, b, 0.1, 2))
+    del out
+
+
+def test_gemv_weight_beyond_2_pow_31_bytes():
+    """A gemv whose weight holds more than 2^31 bytes (N * K > 2^31), filled
+    on the device with a closed-form pattern; sampled outputs."""
+    N, K = 65536 + 4, 32768
+    w = torch.empty((N, K), dtype=torch.int8, device=DEV)
+    kk = torch.arange(K, device=DEV, dtype=torch.int64)
+    for n0 in range(0, N, 4096):
+        nn = torch.arange(n0, min(N, n0 + 4096), device=DEV, dtype=torch.int64)[:, None]
+        w[n0:n0 + nn.shape[0]] = ((nn * 131 + kk * 7) % 255 - 127).to(torch.int8)
+    x = synth.int8_uniform(82, "x", (1, K), -128, 127)
+    ws = synth.uniform_float(82, "ws", (N,), 0.002, 0.01)
+    b = synth.normal(82, "b", (N,), 0.0, 0.1)
+    out = q8.linear_gemv(T(x), 0.02, 5, w, None, T(ws), T(b), 0.5, -1)
+    rows = np.array([0, 1, 65535, 65536, N - 1], dtype=np.int64)
+    k = np.arange(K, dtype=np.int64)
+    w_rows = ((rows[:, None] * 131 + k[None, :] * 7) % 255 - 127).astype(np.int8)
+    ref = oracle.linear(x, 0.02, 5, w_rows, ws[rows], b[rows], 0.5, -1)
+    np.testing.assert_array_equal(H(out)[:, rows], ref)
+    del w, out
