@@ -18,13 +18,16 @@
 // (modulo 2^32, like the pages' i32 accumulator).
 //
 // Transposed convolution is an implicit GEMM per stride phase: outputs with
-// oh % stride_h == ph and ow % stride_w == pw all use the same taps
-// kh = (ph + pad_h) mod stride_h + i*stride_h (likewise kw), and tap (kh, kw)
-// reads the input at (oh' + dh, ow' + dw) with dh = (ph + pad_h - kh) /
-// stride_h, an integer by construction.  A 4-D TMA box over the NHWC bf16
-// input fetches that shifted window; coordinates outside the input are
-// filled with zeros by the TMA unit, which is exactly "taps outside the input
-// contribute nothing" because the stored values are x - input_zero_point.
+// oh % stride_h == ph and ow % stride_w == pw all use the same taps, those
+// kh with kh * dil_h = ph + pad_h (mod stride_h) -- kh0 + i * stride_h / g
+// for g = gcd(dil_h, stride_h) (likewise kw) -- and tap (kh, kw) reads the
+// input at (oh' + dh, ow' + dw) with dh = (ph + pad_h - kh * dil_h) /
+// stride_h, an integer by construction.  A 5-D TMA box over the
+// channel-blocked NHWC bf16 input fetches that shifted window; coordinates
+// outside the input are filled with zeros by the TMA unit, which is exactly
+// "taps outside the input contribute nothing" because the stored values are
+// x - input_zero_point.  The direct convolution (mode 2) reads each tap's
+// window through a box with element strides (stride_w, stride_h).
 //
 // Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one thread)
@@ -204,7 +207,6 @@ struct Ctl {
   uint64_t epi_bar;            // epilogue-warps rendezvous (one arrival per epilogue warp)
   uint32_t tmem_base;
   uint32_t abort_flag;
-  // each epilogue warp's column scales and biases for its current tile
   // column scales and biases of the current tile:
   //   linear: shared by all epilogue warps, two buffers by tile parity, [2][2][BN]
   //   conv:   one slice per epilogue warp, [warp][2][BN / (warps / 4)] = 8 * BN
