@@ -20,12 +20,12 @@ cudaError_t launch_tc_conv_t(const TcConvT& C, cudaStream_t s) {
   // one CTA per 128-row tile: on the transposed-convolution workload the
   // 2-SM MMA measured no faster (its k-blocks are short and many)
   switch (S.bn * 4 + S.kd) {
-    case 64 * 4 + 1: return launch_tc_kernel<64, 16, 1, 1, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    case 64 * 4 + 2: return launch_tc_kernel<64, 16, 1, 2, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    case 128 * 4 + 1: return launch_tc_kernel<128, 16, 1, 1, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    case 128 * 4 + 2: return launch_tc_kernel<128, 16, 1, 2, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    case 256 * 4 + 1: return launch_tc_kernel<256, 8, 1, 1, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    default: return launch_tc_kernel<256, 8, 1, 2, 1>(S.ma, S.mb, S.p, S.ostage, s);
+    case 64 * 4 + 1: return launch_tc_kernel<64, 16, 1, 1, 1>(S.ma, S.mb, S.p, s);
+    case 64 * 4 + 2: return launch_tc_kernel<64, 16, 1, 2, 1>(S.ma, S.mb, S.p, s);
+    case 128 * 4 + 1: return launch_tc_kernel<128, 16, 1, 1, 1>(S.ma, S.mb, S.p, s);
+    case 128 * 4 + 2: return launch_tc_kernel<128, 16, 1, 2, 1>(S.ma, S.mb, S.p, s);
+    case 256 * 4 + 1: return launch_tc_kernel<256, 8, 1, 1, 1>(S.ma, S.mb, S.p, s);
+    default: return launch_tc_kernel<256, 8, 1, 2, 1>(S.ma, S.mb, S.p, s);
   }
 }
 

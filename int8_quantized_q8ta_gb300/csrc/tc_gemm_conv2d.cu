@@ -16,12 +16,12 @@ cudaError_t launch_tc_conv2d(const TcConvT& C, cudaStream_t s) {
   if (!conv_setup(C, S)) return cudaErrorInvalidValue;
   if (S.p.total_units == 0) return cudaSuccess;
   switch (S.bn * 4 + S.kd) {
-    case 64 * 4 + 1: return launch_tc_kernel<64, 16, 2, 1, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    case 64 * 4 + 2: return launch_tc_kernel<64, 16, 2, 2, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    case 128 * 4 + 1: return launch_tc_kernel<128, 16, 2, 1, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    case 128 * 4 + 2: return launch_tc_kernel<128, 16, 2, 2, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    case 256 * 4 + 1: return launch_tc_kernel<256, 8, 2, 1, 1>(S.ma, S.mb, S.p, S.ostage, s);
-    default: return launch_tc_kernel<256, 8, 2, 2, 1>(S.ma, S.mb, S.p, S.ostage, s);
+    case 64 * 4 + 1: return launch_tc_kernel<64, 16, 2, 1, 1>(S.ma, S.mb, S.p, s);
+    case 64 * 4 + 2: return launch_tc_kernel<64, 16, 2, 2, 1>(S.ma, S.mb, S.p, s);
+    case 128 * 4 + 1: return launch_tc_kernel<128, 16, 2, 1, 1>(S.ma, S.mb, S.p, s);
+    case 128 * 4 + 2: return launch_tc_kernel<128, 16, 2, 2, 1>(S.ma, S.mb, S.p, s);
+    case 256 * 4 + 1: return launch_tc_kernel<256, 8, 2, 1, 1>(S.ma, S.mb, S.p, s);
+    default: return launch_tc_kernel<256, 8, 2, 2, 1>(S.ma, S.mb, S.p, s);
   }
 }
 

@@ -51,7 +51,6 @@ inline int conv_t_phase_taps(int64_t ph, int64_t pad, int64_t stride, int64_t di
 struct ConvSetup {
   CUtensorMap ma, mb;
   TcParams p;
-  size_t ostage;
   int bn, kd;
 };
 
@@ -152,14 +151,13 @@ inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
   p.store_mode = 0;
   p.a_bound_dev = nullptr;
   p.a_bound_host = C.a_bound;
-  // Whole output rows go through shared memory when a unit's rows fit the
-  // stage and split into aligned 16-byte pieces.
-  const int64_t wt = static_cast<int64_t>(bw) * p.osw;
-  const bool staged = C.out != nullptr && C.acc_out == nullptr && bn <= 128 && p.osw <= 2 &&
-                      wt % 16 == 0 && C.W_out % 16 == 0 &&
-                      reinterpret_cast<uintptr_t>(C.out) % 16 == 0;
-  p.staged = staged ? 1 : 0;
-  S.ostage = staged ? 2 * static_cast<size_t>(bn) * kBM * p.osw : 0;  // two alternating
+  // Output stores.  Register staging (2): each thread keeps its pixel's
+  // earlier column phases and writes osw consecutive bytes per channel at the
+  // unit's last phase (osw <= 2, aligned); otherwise one byte per output.
+  const bool regstage = C.out != nullptr && C.acc_out == nullptr && bn <= 128 &&
+                        (p.osw == 1 || p.osw == 2) && C.W_out % p.osw == 0 &&
+                        reinterpret_cast<uintptr_t>(C.out) % p.osw == 0;
+  p.staged = regstage ? 2 : 0;
   S.p = p;
   S.bn = bn;
   S.kd = kd;

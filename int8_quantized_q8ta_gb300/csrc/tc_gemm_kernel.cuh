@@ -106,9 +106,9 @@ struct TcParams {
   int gh, gw, tsh, tsw, dsh, dsw, invh, invw;
   int osh, osw;      // output pixel step of a tile's rows / columns (conv_t: stride; conv2d: 1)
   int BW, BH, tiles_w, tiles_h, tiles_oc;
-  int staged;        // conv output goes through the shared-memory stage
+  int staged;        // conv output: 2 = column phases held in registers, one
+                     // store per channel; 0 = one byte store per output
   int8_t ph_order[kMaxPhases];  // row phases, most taps first (stride_h <= kMaxPhases)
-  uint32_t stage_off;  // byte offset of that stage from the aligned smem base
   // epilogue
   const float* ws;
   const float* bias;
@@ -302,7 +302,6 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_base);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + S * kStageBytes);
-  uint8_t* ostage = smem + p.stage_off;
   volatile uint32_t* abort_flag = &ctl->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -504,11 +503,15 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     const int col0 = group * kColsPerWarp;
     const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t acc_it = 0, epi_phase = 0, unit_par = 0, tile_par = 0;
+    uint32_t acc_it = 0, epi_phase = 0, tile_par = 0;
     int cur_ocb = -1;
     const int ew = warp - 2;  // epilogue warp index
     bool ok = true;
     for (int u = unit0; u < p.total_units && ok; u += unit_step) {
+      // register staging: this thread's bytes of the unit's earlier column
+      // phases, four output channels per word
+      constexpr int kHeld = (MODE != 0 && kColsPerWarp <= 64) ? kColsPerWarp / 4 : 1;
+      uint32_t held[kHeld];
       for (int j = 0; j < p.subtiles && ok; ++j) {
         const TileInfo ti = decode_tile<MODE, CG, KD>(p, u, j, rank);
         const int gcolbase = (MODE == 0) ? ti.nb * BN : ti.ocb * BN;
@@ -678,66 +681,51 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           const int ow = (ti.wb * p.BW + ww) * p.osw + ti.pw;
           const int oc0 = gcolbase + col0;
           const bool inside = (oh < p.H_out && ow < p.W_out);
-          if (p.staged && p.acc_out == nullptr) {
-            // stage[oc][hh][wl], wl = ww * sw + pw: one unit's rows, all columns;
-            // two stages alternate by unit, so one rendezvous per unit suffices
-            const int wt = p.BW * p.osw;
-            uint8_t* stage_base = ostage + unit_par * (BN * p.BH * wt);
-            uint8_t* st = stage_base + hh * wt + ww * p.osw + ti.pw;
-#pragma unroll
-            for (int g = 0; g < kColsPerWarp / 16; ++g) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float4 w4 = *reinterpret_cast<const float4*>(sws + 16 * g + 4 * q);
-                const float4 b4 = *reinterpret_cast<const float4*>(sbs + 16 * g + 4 * q);
-                const int s0 = 16 * g + 4 * q;
-                const int32_t v0 = requant_f(__int_as_float(sum[s0 + 0]), w4.x, b4.x, p.rq);
-                const int32_t v1 = requant_f(__int_as_float(sum[s0 + 1]), w4.y, b4.y, p.rq);
-                const int32_t v2 = requant_f(__int_as_float(sum[s0 + 2]), w4.z, b4.z, p.rq);
-                const int32_t v3 = requant_f(__int_as_float(sum[s0 + 3]), w4.w, b4.w, p.rq);
-                const int ocl = col0 + s0;
-                st[(ocl + 0) * p.BH * wt] = static_cast<uint8_t>(v0);
-                st[(ocl + 1) * p.BH * wt] = static_cast<uint8_t>(v1);
-                st[(ocl + 2) * p.BH * wt] = static_cast<uint8_t>(v2);
-                st[(ocl + 3) * p.BH * wt] = static_cast<uint8_t>(v3);
-              }
-            }
-            if (ti.pw == p.osw - 1) {
-              // every column phase of this unit is staged: write whole rows
-              if (!epi_sync(ctl, epi_phase, abort_flag, p.err)) {
-                ok = false;
-                break;
-              }
-              const int chunks_per_row = wt / 16;
-              const int rows_total = BN * p.BH;
+          bool done = false;
+          if constexpr (kHeld > 1) {
+            if (p.staged == 2) {
+              // Register staging (osw <= 2): the unit's column phases of one
+              // output pixel pair are processed by this same thread; earlier
+              // phases wait packed in held[], and the last one writes osw
+              // consecutive bytes per output channel (a warp covers 32 * osw
+              // contiguous bytes of an output row).
+              done = true;
+              const bool last = (ti.pw == p.osw - 1);
               const int64_t plane = static_cast<int64_t>(p.H_out) * p.W_out;
-              const int ow0 = ti.wb * wt;
-              const int bh_log = __ffs(p.BH) - 1;  // BH = 128 / BW, a power of two
-              auto store_row_chunk = [&](int r, int ch) {
-                const int ocl = r >> bh_log, rh = r & (p.BH - 1);
-                const int oc = ti.ocb * BN + ocl;
-                const int ohh = (ti.hb * p.BH + rh) * p.osh + ti.ph;
-                const int oww = ow0 + 16 * ch;
-                if (oc < p.OC && ohh < p.H_out && oww < p.W_out) {
-                  const uint4 v = *reinterpret_cast<const uint4*>(stage_base + r * wt + 16 * ch);
-                  int8_t* dst = p.out + (static_cast<int64_t>(ti.n) * p.out_ch + oc) * plane +
-                                static_cast<int64_t>(ohh) * p.W_out + oww;
-                  *reinterpret_cast<uint4*>(dst) = v;   // W_out % 16 == 0 when staged
-                }
-              };
-              if (kEpiThreads % chunks_per_row == 0) {
-                // each thread keeps one chunk column: one division per unit
-                const int ch = et % chunks_per_row, step_r = kEpiThreads / chunks_per_row;
-                for (int r = et / chunks_per_row; r < rows_total; r += step_r)
-                  store_row_chunk(r, ch);
-              } else {
-                for (int it = et; it < rows_total * chunks_per_row; it += kEpiThreads) {
-                  const int r = it / chunks_per_row;
-                  store_row_chunk(r, it - r * chunks_per_row);
+              int8_t* dst = p.out + (static_cast<int64_t>(ti.n) * p.out_ch + oc0) * plane +
+                            static_cast<int64_t>(oh) * p.W_out + (ow - ti.pw);
+#pragma unroll
+              for (int g = 0; g < kColsPerWarp / 16; ++g) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float4 w4 = *reinterpret_cast<const float4*>(sws + 16 * g + 4 * q);
+                  const float4 b4 = *reinterpret_cast<const float4*>(sbs + 16 * g + 4 * q);
+                  const int s0 = 16 * g + 4 * q;
+                  const int32_t v[4] = {requant_f(__int_as_float(sum[s0 + 0]), w4.x, b4.x, p.rq),
+                                        requant_f(__int_as_float(sum[s0 + 1]), w4.y, b4.y, p.rq),
+                                        requant_f(__int_as_float(sum[s0 + 2]), w4.z, b4.z, p.rq),
+                                        requant_f(__int_as_float(sum[s0 + 3]), w4.w, b4.w, p.rq)};
+                  if (!last) {
+                    held[s0 / 4] = pack4_i(v[0], v[1], v[2], v[3]);
+                  } else if (inside) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      if (oc0 + s0 + e >= p.OC) continue;
+                      if (p.osw == 2) {
+                        const uint32_t lo = (held[s0 / 4] >> (8 * e)) & 0xffu;
+                        *reinterpret_cast<uint16_t*>(dst + (s0 + e) * plane) =
+                            static_cast<uint16_t>(lo | ((static_cast<uint32_t>(v[e]) & 0xffu) << 8));
+                      } else {
+                        dst[(s0 + e) * plane] = static_cast<int8_t>(v[e]);
+                      }
+                    }
+                  }
                 }
               }
-              unit_par ^= 1u;
             }
+          }
+          if (done) {
+            // stored above
           } else if (inside) {
             const int64_t plane = static_cast<int64_t>(p.H_out) * p.W_out;
             int8_t* dst = p.out ? p.out + (static_cast<int64_t>(ti.n) * p.out_ch + oc0) * plane +
@@ -798,19 +786,17 @@ inline int pick_bn(int64_t n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
 
 template <int BN, int EPI, int MODE, int KD, int CG>
 inline cudaError_t launch_tc_kernel(const CUtensorMap& a, const CUtensorMap& b, TcParams p,
-                                    size_t out_stage_bytes, cudaStream_t s) {
+                                    cudaStream_t s) {
   const size_t kStage = static_cast<size_t>(KD) * (static_cast<size_t>(kBM) * kBK * 2 +
                                                    static_cast<size_t>(BN / CG) * kBK * 2);
-  const size_t fixed = sizeof(Ctl) + 1024 + out_stage_bytes;
+  const size_t fixed = sizeof(Ctl) + 1024;
   const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemBudget - fixed) / kStage));
   if (stages < 2) return cudaErrorInvalidValue;
   p.err = device_error_word();
   if (p.err == nullptr) return cudaErrorInvalidValue;
   p.stages = stages;
   p.kd = KD;
-  const size_t ctl_end = static_cast<size_t>(stages) * kStage + sizeof(Ctl);
-  p.stage_off = static_cast<uint32_t>((ctl_end + 127) / 128 * 128);
-  const size_t smem = p.stage_off + out_stage_bytes + 1024;
+  const size_t smem = static_cast<size_t>(stages) * kStage + sizeof(Ctl) + 1024;
   auto kernel = tc_gemm_kernel<BN, EPI, MODE, KD, CG>;
   static std::once_flag attr_once[64];
   int dev = 0;

@@ -85,17 +85,17 @@ cudaError_t launch_tc_linear(const TcLinear& L, cudaStream_t s) {
   if (p.total_units == 0) return cudaSuccess;
   if (pair) {
     switch (bn) {
-      case 256: return launch_tc_kernel<256, 8, 0, 2, 2>(ma, mb, p, 0, s);
-      case 240: return launch_tc_kernel<240, 12, 0, 2, 2>(ma, mb, p, 0, s);
-      case 224: return launch_tc_kernel<224, 8, 0, 2, 2>(ma, mb, p, 0, s);
-      default: return launch_tc_kernel<192, 8, 0, 2, 2>(ma, mb, p, 0, s);
+      case 256: return launch_tc_kernel<256, 8, 0, 2, 2>(ma, mb, p, s);
+      case 240: return launch_tc_kernel<240, 12, 0, 2, 2>(ma, mb, p, s);
+      case 224: return launch_tc_kernel<224, 8, 0, 2, 2>(ma, mb, p, s);
+      default: return launch_tc_kernel<192, 8, 0, 2, 2>(ma, mb, p, s);
     }
   }
   // 16 epilogue warps where their register share fits the column slice
   switch (bn) {
-    case 64: return launch_tc_kernel<64, 16, 0, 1, 1>(ma, mb, p, 0, s);
-    case 128: return launch_tc_kernel<128, 16, 0, 1, 1>(ma, mb, p, 0, s);
-    default: return launch_tc_kernel<256, 8, 0, 1, 1>(ma, mb, p, 0, s);
+    case 64: return launch_tc_kernel<64, 16, 0, 1, 1>(ma, mb, p, s);
+    case 128: return launch_tc_kernel<128, 16, 0, 1, 1>(ma, mb, p, s);
+    default: return launch_tc_kernel<256, 8, 0, 1, 1>(ma, mb, p, s);
   }
 }
 
