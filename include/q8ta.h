@@ -178,7 +178,10 @@ q8_status q8_linear_gemv(const int8_t* x, int64_t M, int64_t K, double input_sca
  * Load-time weight packing.  A linear layer's weight is a constant, so the
  * bf16 copy the tensor cores read can be made once:
  *   q8_linear_pack_weight writes q8_linear_packed_weight_bytes(N, K) bytes
- *   (256-byte aligned buffer) from the int8 [N, K] weight.
+ *   (256-byte aligned buffer) from the int8 [N, K] weight: the bf16 rows,
+ *   then a 256-byte trailer whose first int32 is the largest sum of |w| over
+ *   64 consecutive weights of one row (the kernels size their exact f32
+ *   partial sums from it; results never depend on it).
  * Results of every *_packed call are identical to q8_linear.
  */
 size_t q8_linear_packed_weight_bytes(int64_t N, int64_t K);
@@ -291,9 +294,15 @@ q8_status q8_conv2d_transposed_acc32(const int8_t* x, const q8_conv2d_transposed
  *   q8_conv2d_transposed_pack_weight writes the weight's tensor-core layout
  *     (bf16, per group [taps][IC/64][OC/groups][64]) into `packed`
  *     (q8_conv2d_transposed_packed_weight_bytes(shape) bytes, 256-byte
- *     aligned, owned by the caller);
+ *     aligned, owned by the caller), followed by a 256-byte trailer whose
+ *     first int32 is the largest sum of |w| over 64 input channels of one
+ *     tap of one output channel: the kernels size their exact f32 partial
+ *     sums from it (with |x - input_zero_point|), so results never depend
+ *     on it;
  *   q8_conv2d_transposed_packed runs the op from it; its workspace holds only
- *     the input copy (q8_conv2d_transposed_packed_workspace_bytes(shape)).
+ *     the input copy (q8_conv2d_transposed_packed_workspace_bytes(shape));
+ *   q8_conv2d_transposed_packed_acc32 writes the exact int32 accumulators
+ *     (as q8_conv2d_transposed_acc32) from it, same workspace.
  * Guards: those of q8_conv2d_transposed. */
 size_t q8_conv2d_transposed_packed_weight_bytes(const q8_conv2d_transposed_shape* shape);
 size_t q8_conv2d_transposed_packed_workspace_bytes(const q8_conv2d_transposed_shape* shape);
@@ -307,6 +316,11 @@ q8_status q8_conv2d_transposed_packed(const int8_t* x, const q8_conv2d_transpose
                                       int32_t output_zero_point, const char* activation,
                                       int8_t* out, void* workspace, size_t workspace_bytes,
                                       q8_stream_t stream);
+q8_status q8_conv2d_transposed_packed_acc32(const int8_t* x,
+                                            const q8_conv2d_transposed_shape* shape,
+                                            int32_t input_zero_point, const void* packed_weight,
+                                            int32_t* acc, void* workspace, size_t workspace_bytes,
+                                            q8_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* q8ta_conv2d (direct convolution)                                   [conv] */
@@ -359,6 +373,9 @@ q8_status q8_conv2d_packed(const int8_t* x, const q8_conv2d_shape* shape, double
                            const float* weight_scales, const float* bias, double output_scale,
                            int32_t output_zero_point, const char* activation, int8_t* out,
                            void* workspace, size_t workspace_bytes, q8_stream_t stream);
+q8_status q8_conv2d_packed_acc32(const int8_t* x, const q8_conv2d_shape* shape,
+                                 int32_t input_zero_point, const void* packed_weight, int32_t* acc,
+                                 void* workspace, size_t workspace_bytes, q8_stream_t stream);
 
 #ifdef __cplusplus
 }

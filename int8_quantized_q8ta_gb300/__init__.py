@@ -36,9 +36,10 @@ EXPORTS = (
     "q8_conv2d_transposed_workspace_bytes", "q8_conv2d_transposed",
     "q8_conv2d_transposed_acc32", "q8_conv2d_transposed_packed_weight_bytes",
     "q8_conv2d_transposed_packed_workspace_bytes", "q8_conv2d_transposed_pack_weight",
-    "q8_conv2d_transposed_packed",
+    "q8_conv2d_transposed_packed", "q8_conv2d_transposed_packed_acc32",
     "q8_conv2d_workspace_bytes", "q8_conv2d", "q8_conv2d_acc32", "q8_conv2d_packed_weight_bytes",
     "q8_conv2d_packed_workspace_bytes", "q8_conv2d_pack_weight", "q8_conv2d_packed",
+    "q8_conv2d_packed_acc32",
 )
 
 
@@ -106,6 +107,7 @@ def _load() -> ctypes.CDLL:
         "q8_conv2d_transposed_pack_weight": (ctypes.c_int, [P, SP, P, S, P]),
         "q8_conv2d_transposed_packed": (ctypes.c_int, [P, SP, D, I32, P, P, P, D, I32, C, P, P, S,
                                                        P]),
+        "q8_conv2d_transposed_packed_acc32": (ctypes.c_int, [P, SP, I32, P, P, P, S, P]),
         "q8_conv2d_workspace_bytes": (S, [DP]),
         "q8_conv2d": (ctypes.c_int, [P, DP, D, I32, P, P, P, D, I32, C, P, P, S, P]),
         "q8_conv2d_acc32": (ctypes.c_int, [P, DP, I32, P, P, P, S, P]),
@@ -113,6 +115,7 @@ def _load() -> ctypes.CDLL:
         "q8_conv2d_packed_workspace_bytes": (S, [DP]),
         "q8_conv2d_pack_weight": (ctypes.c_int, [P, DP, P, S, P]),
         "q8_conv2d_packed": (ctypes.c_int, [P, DP, D, I32, P, P, P, D, I32, C, P, P, S, P]),
+        "q8_conv2d_packed_acc32": (ctypes.c_int, [P, DP, I32, P, P, P, S, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -556,6 +559,30 @@ def conv2d_transposed_packed(x, input_scale, input_zero_point, packed: PackedCon
     return out
 
 
+def conv2d_transposed_packed_acc32(x, input_zero_point, packed: PackedConvWeight, output_size,
+                                   stride=1, padding=0, dilation=1, out=None, workspace=None):
+    """Exact int32 accumulators of q8ta_conv2d_transposed from a packed weight."""
+    if not packed.transposed:
+        raise ValueError("packed weight is a q8ta_conv2d weight")
+    _need(x, torch.int8, "x")
+    if x.shape[1] != packed.IC:
+        raise ValueError(f"x has {x.shape[1]} channels, the packed weight {packed.IC}")
+    H_out, W_out = output_size
+    ldw = packed.Kh * packed.Kw * (packed.IC // packed.groups)
+    shape = conv_t_shape(tuple(x.shape), (packed.OC, ldw), packed.Kh, packed.Kw, H_out, W_out,
+                         stride, padding, 0, dilation, packed.groups)
+    if out is None:
+        out = torch.empty((x.shape[0], packed.OC, H_out, W_out), dtype=torch.int32,
+                          device=x.device)
+    _need(out, torch.int32, "out")
+    nbytes = _lib.q8_conv2d_transposed_packed_workspace_bytes(ctypes.byref(shape))
+    ws = _workspace(nbytes, x.device, workspace)
+    _check(_lib.q8_conv2d_transposed_packed_acc32(
+        _ptr(x), ctypes.byref(shape), int(input_zero_point), _ptr(packed.data), _ptr(out),
+        _ptr(ws), nbytes, _stream(x)), "q8_conv2d_transposed_packed_acc32")
+    return out
+
+
 # ---------------------------------------------------------------------------
 # q8ta_conv2d (the direct convolution)
 # ---------------------------------------------------------------------------
@@ -661,4 +688,32 @@ def conv2d_packed(x, input_scale, input_zero_point, packed: PackedConvWeight, we
         _ptr(packed.data), _ptr(weight_scales), _ptr(bias), float(output_scale),
         int(output_zero_point), activation.encode(), _ptr(out), _ptr(ws), nbytes, _stream(x)),
         "q8_conv2d_packed")
+    return out
+
+
+def conv2d_packed_acc32(x, input_zero_point, packed: PackedConvWeight, output_size=None, stride=1,
+                        padding=0, dilation=1, out=None, workspace=None):
+    """Exact int32 accumulators of q8ta_conv2d from a packed weight."""
+    if packed.transposed:
+        raise ValueError("packed weight is a q8ta_conv2d_transposed weight")
+    _need(x, torch.int8, "x")
+    if x.shape[1] != packed.IC:
+        raise ValueError(f"x has {x.shape[1]} channels, the packed weight {packed.IC}")
+    Kh, Kw = packed.Kh, packed.Kw
+    if output_size is None:
+        output_size = conv2d_output_size(x.shape[2], x.shape[3], (Kh, Kw), stride, padding,
+                                         dilation)
+    H_out, W_out = output_size
+    ldw = Kh * Kw * (packed.IC // packed.groups)
+    shape = conv2d_shape(tuple(x.shape), (packed.OC, ldw), Kh, Kw, H_out, W_out, stride, padding,
+                         dilation, packed.groups)
+    if out is None:
+        out = torch.empty((x.shape[0], packed.OC, H_out, W_out), dtype=torch.int32,
+                          device=x.device)
+    _need(out, torch.int32, "out")
+    nbytes = _lib.q8_conv2d_packed_workspace_bytes(ctypes.byref(shape))
+    ws = _workspace(nbytes, x.device, workspace)
+    _check(_lib.q8_conv2d_packed_acc32(_ptr(x), ctypes.byref(shape), int(input_zero_point),
+                                       _ptr(packed.data), _ptr(out), _ptr(ws), nbytes, _stream(x)),
+           "q8_conv2d_packed_acc32")
     return out

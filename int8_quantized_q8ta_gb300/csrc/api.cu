@@ -50,6 +50,8 @@ size_t bf16_rows_bytes(int64_t rows, int64_t K) {
 
 // A prepared operand is the bf16 data followed by one 256-byte trailer whose
 // first int32 holds a_bound_of(zp) of the zero point it was prepared with.
+// A packed weight likewise: its trailer's first int32 holds the largest sum
+// of |w| over one k-block (64 consecutive weights) of one row.
 int32_t* operand_bound_word(void* operand, int64_t M, int64_t K) {
   return reinterpret_cast<int32_t*>(static_cast<char*>(operand) + bf16_rows_bytes(M, K));
 }
@@ -110,7 +112,7 @@ size_t q8_linear_workspace_bytes(int64_t M, int64_t K, int64_t N) {
 
 size_t q8_linear_packed_weight_bytes(int64_t N, int64_t K) {
   if (N < 1 || K < 1) return 0;
-  return bf16_rows_bytes(N, K);
+  return bf16_rows_bytes(N, K) + q8::kWorkspaceAlign;
 }
 
 size_t q8_linear_operand_bytes(int64_t M, int64_t K) {
@@ -179,9 +181,12 @@ q8_status q8_linear_pack_weight(const int8_t* weight, int64_t N, int64_t K, void
   if (N < 1 || K < 1 || !mul_ok(N, K) || N > INT32_MAX || K > INT32_MAX / 2) return Q8_ERR_SHAPE;
   if (packed_bytes < q8_linear_packed_weight_bytes(N, K)) return Q8_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(packed) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
-  return cuda_status(q8::launch_rows_to_bf16(weight, N, K, K, 0,
-                                             static_cast<__nv_bfloat16*>(packed),
-                                             round_up(K, kTileK), cs(stream)));
+  cudaError_t e = q8::launch_rows_to_bf16(weight, N, K, K, 0, static_cast<__nv_bfloat16*>(packed),
+                                          round_up(K, kTileK), cs(stream));
+  if (e == cudaSuccess)
+    e = q8::launch_weight_block_bound(weight, N, K, 1, K, operand_bound_word(packed, N, K),
+                                      cs(stream));
+  return cuda_status(e);
 }
 
 static q8_status check_operand(const void* operand, size_t operand_bytes, int64_t M, int64_t K) {
@@ -242,6 +247,7 @@ static q8_status run_operand_packed(const void* operand, int64_t M, int64_t K, d
   L.acc_out = acc_out;
   L.a_bound_dev = operand_bound_word(const_cast<void*>(operand), M, K);
   L.a_bound_host = 255;
+  L.w_bound_dev = operand_bound_word(const_cast<void*>(packed), N, K);
   return cuda_status(q8::launch_tc_linear(L, cs(stream)));
 }
 

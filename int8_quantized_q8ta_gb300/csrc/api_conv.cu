@@ -81,8 +81,18 @@ size_t relayout_bytes(const Geom& g) {
   return align_ws(static_cast<size_t>(g.N * g.H_in * g.W_in) * g.groups * g.ICgp() * 2);
 }
 
-size_t packed_bytes(const Geom& g) {
+// The packed weight, then a 256-byte trailer whose first int32 holds the
+// largest sum of |w| over one k-block (64 input channels of one tap) of one
+// output row, written by the load-time pack.
+size_t packed_data_bytes(const Geom& g) {
   return align_ws(static_cast<size_t>(g.groups * g.taps() * g.OCg()) * g.ICgp() * 2);
+}
+
+size_t packed_bytes(const Geom& g) { return packed_data_bytes(g) + q8::kWorkspaceAlign; }
+
+int32_t* packed_bound_word(const Geom& g, const void* packed) {
+  return reinterpret_cast<int32_t*>(static_cast<char*>(const_cast<void*>(packed)) +
+                                    packed_data_bytes(g));
 }
 
 q8_status check_ptr(const void* p, size_t have, size_t need) {
@@ -97,10 +107,12 @@ q8_status pack(const Geom& g, const int8_t* weight, void* packed, q8_stream_t st
                                                  g.ICgp(), cs(stream)));
 }
 
-// The relayout of x into `relayout`, then one GEMM per group.
+// The relayout of x into `relayout`, then one GEMM per group.  w_bound: the
+// packed weight's k-block bound word, or null (the worst case).
 q8_status run(const Geom& g, const int8_t* x, double input_scale, int32_t izp, const void* packed,
-              const float* ws, const float* bias, double output_scale, int32_t ozp, int relu,
-              int8_t* out, int32_t* acc_out, void* relayout, q8_stream_t stream) {
+              const int32_t* w_bound, const float* ws, const float* bias, double output_scale,
+              int32_t ozp, int relu, int8_t* out, int32_t* acc_out, void* relayout,
+              q8_stream_t stream) {
   if (reinterpret_cast<uintptr_t>(packed) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
   auto* a = static_cast<__nv_bfloat16*>(relayout);
   cudaError_t e = q8::launch_nchw_to_nhwc_bf16(x, g.N, g.groups, g.ICg(), g.H_in, g.W_in, izp, a,
@@ -137,6 +149,7 @@ q8_status run(const Geom& g, const int8_t* x, double input_scale, int32_t izp, c
     C.out = out ? out + j * g.OCg() * plane : nullptr;
     C.acc_out = acc_out ? acc_out + j * g.OCg() * plane : nullptr;
     C.a_bound = a_bound_of(izp);
+    C.w_bound = w_bound;
     e = q8::launch_tc_conv_t(C, cs(stream));
     if (e != cudaSuccess) return Q8_ERR_CUDA;
   }
@@ -170,13 +183,14 @@ q8_status full(const Geom& g, const int8_t* x, double input_scale, int32_t izp,
     return Q8_ERR_ARG;
   }
   const size_t ra = relayout_bytes(g);
-  st = check_ptr(workspace, workspace_bytes, ra + packed_bytes(g));
+  st = check_ptr(workspace, workspace_bytes, ra + packed_data_bytes(g));
   if (st != Q8_OK) return st;
   void* packed = static_cast<char*>(workspace) + ra;
   st = pack(g, weight, packed, stream);
   if (st != Q8_OK) return st;
-  return run(g, x, input_scale, izp, packed, ws, bias, output_scale, ozp, relu, out, acc_out,
-             workspace, stream);
+  // a per-call weight copy: no bound word (that costs a pass over the weight)
+  return run(g, x, input_scale, izp, packed, nullptr, ws, bias, output_scale, ozp, relu, out,
+             acc_out, workspace, stream);
 }
 
 q8_status packed_form(const Geom& g, const int8_t* x, double input_scale, int32_t izp,
@@ -191,8 +205,23 @@ q8_status packed_form(const Geom& g, const int8_t* x, double input_scale, int32_
   if (st != Q8_OK) return st;
   st = check_ptr(workspace, workspace_bytes, relayout_bytes(g));
   if (st != Q8_OK) return st;
-  return run(g, x, input_scale, izp, packed, ws, bias, output_scale, ozp, relu, out, nullptr,
-             workspace, stream);
+  return run(g, x, input_scale, izp, packed, packed_bound_word(g, packed), ws, bias, output_scale,
+             ozp, relu, out, nullptr, workspace, stream);
+}
+
+// The int32 accumulators from a packed weight (exact chunks sized by its
+// k-block bound, as in packed_form).
+q8_status packed_acc_form(const Geom& g, const int8_t* x, int32_t izp, const void* packed,
+                          int32_t* acc, void* workspace, size_t workspace_bytes,
+                          q8_stream_t stream) {
+  if (!x || !packed || !acc) return Q8_ERR_NULL;
+  q8_status st = check_geom(g);
+  if (st != Q8_OK) return st;
+  if (!zp_ok(izp)) return Q8_ERR_ARG;
+  st = check_ptr(workspace, workspace_bytes, relayout_bytes(g));
+  if (st != Q8_OK) return st;
+  return run(g, x, 1.0, izp, packed, packed_bound_word(g, packed), nullptr, nullptr, 1.0, 0, 0,
+             nullptr, acc, workspace, stream);
 }
 
 q8_status pack_form(const Geom& g, const int8_t* weight, void* packed, size_t bytes,
@@ -202,7 +231,10 @@ q8_status pack_form(const Geom& g, const int8_t* weight, void* packed, size_t by
   if (st != Q8_OK) return st;
   st = check_ptr(packed, bytes, packed_bytes(g));
   if (st != Q8_OK) return st;
-  return pack(g, weight, packed, stream);
+  st = pack(g, weight, packed, stream);
+  if (st != Q8_OK) return st;
+  return cuda_status(q8::launch_weight_block_bound(weight, g.OC, g.ldw, g.taps(), g.ICg(),
+                                                   packed_bound_word(g, packed), cs(stream)));
 }
 
 size_t sized(const Geom& g, size_t bytes) { return check_geom(g) == Q8_OK ? bytes : 0; }
@@ -215,7 +247,7 @@ extern "C" {
 size_t q8_conv2d_transposed_workspace_bytes(const q8_conv2d_transposed_shape* shape) {
   if (!shape) return 0;
   const Geom g = geom_t(*shape);
-  return sized(g, relayout_bytes(g) + packed_bytes(g));
+  return sized(g, relayout_bytes(g) + packed_data_bytes(g));
 }
 
 size_t q8_conv2d_transposed_packed_weight_bytes(const q8_conv2d_transposed_shape* shape) {
@@ -273,11 +305,21 @@ q8_status q8_conv2d_transposed_packed(const int8_t* x, const q8_conv2d_transpose
                      workspace, workspace_bytes, stream);
 }
 
+q8_status q8_conv2d_transposed_packed_acc32(const int8_t* x,
+                                            const q8_conv2d_transposed_shape* shape,
+                                            int32_t input_zero_point, const void* packed_weight,
+                                            int32_t* acc, void* workspace, size_t workspace_bytes,
+                                            q8_stream_t stream) {
+  if (!shape) return Q8_ERR_NULL;
+  return packed_acc_form(geom_t(*shape), x, input_zero_point, packed_weight, acc, workspace,
+                         workspace_bytes, stream);
+}
+
 // ------------------------------------------------------------ conv2d
 size_t q8_conv2d_workspace_bytes(const q8_conv2d_shape* shape) {
   if (!shape) return 0;
   const Geom g = geom_d(*shape);
-  return sized(g, relayout_bytes(g) + packed_bytes(g));
+  return sized(g, relayout_bytes(g) + packed_data_bytes(g));
 }
 
 size_t q8_conv2d_packed_weight_bytes(const q8_conv2d_shape* shape) {
@@ -326,6 +368,14 @@ q8_status q8_conv2d_packed(const int8_t* x, const q8_conv2d_shape* shape, double
   return packed_form(geom_d(*shape), x, input_scale, input_zero_point, packed_weight,
                      weight_scales, bias, output_scale, output_zero_point, activation, out,
                      workspace, workspace_bytes, stream);
+}
+
+q8_status q8_conv2d_packed_acc32(const int8_t* x, const q8_conv2d_shape* shape,
+                                 int32_t input_zero_point, const void* packed_weight, int32_t* acc,
+                                 void* workspace, size_t workspace_bytes, q8_stream_t stream) {
+  if (!shape) return Q8_ERR_NULL;
+  return packed_acc_form(geom_d(*shape), x, input_zero_point, packed_weight, acc, workspace,
+                         workspace_bytes, stream);
 }
 
 }  // extern "C"

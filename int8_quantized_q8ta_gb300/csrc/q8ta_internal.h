@@ -69,6 +69,11 @@ cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t groups,
                                      int64_t ICgp, cudaStream_t s);
 // Packed convolution weight, per group j (rows oc = j*OCg + ocl):
 // dst[j][t][ic/64][ocl][ic%64] = bf16(w[oc*ldw + t*ICg + ic]) for ic < ICg, else 0.
+// Largest sum of |w| over one k-block (64 input channels of one tap) of
+// one output row of a rows x [taps][ICg] int8 weight (row stride ldw), into
+// the device word *bound (zeroed here first).
+cudaError_t launch_weight_block_bound(const int8_t* w, int64_t rows, int64_t ldw, int64_t taps,
+                                      int64_t ICg, int32_t* bound, cudaStream_t s);
 cudaError_t launch_conv_weight_bf16(const int8_t* w, int64_t groups, int64_t OCg, int64_t taps,
                                     int64_t ICg, int64_t ldw, __nv_bfloat16* dst, int64_t ICgp,
                                     cudaStream_t s);
@@ -89,6 +94,9 @@ struct TcLinear {
   // chunk may hold (255, the int8 worst case, gives 8).
   const int32_t* a_bound_dev;
   int a_bound_host;
+  // Largest sum of |w| over one k-block of one weight row (a device word
+  // written when the weight was packed), or null for the worst case 64 * 128.
+  const int32_t* w_bound_dev;
 };
 cudaError_t launch_tc_linear(const TcLinear& p, cudaStream_t s);
 
@@ -110,6 +118,7 @@ struct TcConvT {
   int8_t* out;       // the group's first output channel of [N, out_ch, H_out, W_out]
   int32_t* acc_out;  // int32 debug output laid out like out, or null
   int a_bound;       // largest |x - input_zero_point| (see TcLinear)
+  const int32_t* w_bound;  // per-k-block weight bound on the device, or null (see TcLinear)
 };
 cudaError_t launch_tc_conv_t(const TcConvT& p, cudaStream_t s);
 

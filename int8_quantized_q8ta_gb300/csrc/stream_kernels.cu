@@ -573,6 +573,49 @@ __global__ void __launch_bounds__(256) conv_weight_bf16_kernel(const int8_t* __r
   }
 }
 
+// Largest sum of |w| over one k-block of one output row: rows of
+// [taps][ICg] int8 (row stride ldw), a k-block being 64 consecutive input
+// channels of one tap (the last one of a tap may be shorter).  One warp per
+// k-block; each warp's maximum goes to *bound by atomicMax (the caller zeroes
+// it first).  With |x - zp| <= a, the products of one k-block then sum to at
+// most a * bound in magnitude, whatever the row.
+__global__ void __launch_bounds__(256) weight_block_bound_kernel(const int8_t* __restrict__ w,
+                                                                 int64_t rows, int64_t ldw,
+                                                                 int64_t taps, int64_t ICg,
+                                                                 int32_t* __restrict__ bound) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t nblk = (ICg + 63) / 64;
+  const int64_t items = rows * taps * nblk;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  int best = 0;
+  for (int64_t it = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; it < items;
+       it += nwarps) {
+    const int64_t blk = it % nblk;
+    const int64_t rt = it / nblk;  // row * taps + tap
+    const int8_t* seg = w + (rt / taps) * ldw + (rt % taps) * ICg + blk * 64;
+    const int64_t len = ICg - blk * 64;
+    int s = 0;
+    if (lane < len) s += abs(static_cast<int>(seg[lane]));
+    if (lane + 32 < len) s += abs(static_cast<int>(seg[lane + 32]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    best = max(best, s);
+  }
+  if (lane == 0 && best > 0) atomicMax(bound, best);
+}
+
+cudaError_t launch_weight_block_bound(const int8_t* w, int64_t rows, int64_t ldw, int64_t taps,
+                                      int64_t ICg, int32_t* bound, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(bound, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
+  const int64_t items = rows * taps * ((ICg + 63) / 64);
+  if (items == 0) return cudaSuccess;
+  return launch_pdl(weight_block_bound_kernel, stream_grid(items * 32, 256, 8), 256, 0, s, w, rows,
+                    ldw, taps, ICg, bound);
+}
+
 cudaError_t launch_conv_weight_bf16(const int8_t* w, int64_t groups, int64_t OCg, int64_t taps,
                                     int64_t ICg, int64_t ldw, __nv_bfloat16* dst, int64_t ICgp,
                                     cudaStream_t s) {

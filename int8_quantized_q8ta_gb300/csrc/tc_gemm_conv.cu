@@ -2,6 +2,8 @@
 // (tc_gemm_kernel.cuh): per-stride-phase implicit GEMM over the
 // channel-blocked NHWC copy of x - input_zero_point, read through 5-D TMA
 // boxes whose zero fill implements the skipped taps.  One launch per group.
+// More than 64 output channels per group: 128 channels x 256 pixels per tile
+// (exchanged operands, MODE 3); otherwise 128 pixels x 64..256 channels.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -17,8 +19,9 @@ cudaError_t launch_tc_conv_t(const TcConvT& C, cudaStream_t s) {
   ConvSetup S;
   if (!conv_setup(C, S)) return cudaErrorInvalidValue;
   if (S.p.total_units == 0) return cudaSuccess;
-  // one CTA per 128-row tile: on the transposed-convolution workload the
-  // 2-SM MMA measured no faster (its k-blocks are short and many)
+  // one CTA per tile: on the transposed-convolution workload the 2-SM MMA
+  // measured no faster (its k-blocks are short and many)
+  if (S.pixn) return launch_tc_kernel<kPixTile, 16, 3, 1, 1>(S.ma, S.mb, S.p, s);
   switch (S.bn * 4 + S.kd) {
     case 64 * 4 + 1: return launch_tc_kernel<64, 16, 1, 1, 1>(S.ma, S.mb, S.p, s);
     case 64 * 4 + 2: return launch_tc_kernel<64, 16, 1, 2, 1>(S.ma, S.mb, S.p, s);

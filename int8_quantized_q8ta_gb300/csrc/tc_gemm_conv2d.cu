@@ -2,7 +2,9 @@
 // tensor-core GEMM (tc_gemm_kernel.cuh): an implicit GEMM over 128-pixel
 // output tiles whose input taps are 5-D TMA boxes with element strides
 // (stride_w, stride_h), starting at (ow*stride_w - pad_w + kw*dil_w, ...);
-// the boxes' zero fill covers the padding.  One launch per group.
+// the boxes' zero fill covers the padding.  One launch per group.  More
+// than 64 output channels per group: 128 channels x 256 pixels per tile
+// (exchanged operands, MODE 4).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -15,6 +17,7 @@ cudaError_t launch_tc_conv2d(const TcConvT& C, cudaStream_t s) {
   ConvSetup S;
   if (!conv_setup(C, S)) return cudaErrorInvalidValue;
   if (S.p.total_units == 0) return cudaSuccess;
+  if (S.pixn) return launch_tc_kernel<kPixTile, 16, 4, 1, 1>(S.ma, S.mb, S.p, s);
   switch (S.bn * 4 + S.kd) {
     case 64 * 4 + 1: return launch_tc_kernel<64, 16, 2, 1, 1>(S.ma, S.mb, S.p, s);
     case 64 * 4 + 2: return launch_tc_kernel<64, 16, 2, 2, 1>(S.ma, S.mb, S.p, s);

@@ -52,29 +52,41 @@ struct ConvSetup {
   CUtensorMap ma, mb;
   TcParams p;
   int bn, kd;
+  bool pixn;  // output channels on the MMA's M side, bn pixels on N
 };
 
-// Tile shape: 128 output pixels (bw columns x bh rows of a stride phase for
-// the transposed convolution, of the output for the direct one) x bn output
-// channels.  The direct convolution reads its input through boxes with
-// element strides (stride_w, stride_h), whose extents bw * stride_w and
-// bh * stride_h must stay within the TMA limit of 256.
+// Pixels of an exchanged-operand tile (the MMA's N).
+constexpr int kPixTile = 256;
+
+// Tile shape: tile_px output pixels (bw columns x bh rows of a stride phase
+// for the transposed convolution, of the output for the direct one) x the
+// output channels of one block.  More than 64 output channels on images of
+// at least one exchanged tile per phase: 128 channels (M) x 256 pixels (N);
+// otherwise 128 pixels (M) x bn channels (N).  The direct convolution reads
+// its input through boxes with element strides (stride_w, stride_h), whose
+// extents bw * stride_w and bh * stride_h must stay within the TMA limit of
+// 256.
 inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
   const bool direct = C.direct;
-  const int bn = pick_bn(C.OC);
   const int64_t Hq = direct ? C.H_out : (C.H_out + C.stride_h - 1) / C.stride_h;
   const int64_t Wq = direct ? C.W_out : (C.W_out + C.stride_w - 1) / C.stride_w;
   const int64_t ew = direct ? C.stride_w : 1, eh = direct ? C.stride_h : 1;
+  const bool pixn = C.OC > 64 && Hq * Wq >= kPixTile;
+  const int bn = pixn ? kPixTile : pick_bn(C.OC);  // the MMA's N
+  const int oc_blk = pixn ? kBM : bn;              // output channels per tile
+  const int tile_px = pixn ? kPixTile : kBM;
   int bw = 1;
-  while (bw < Wq && bw < kBM) bw *= 2;
+  while (bw < Wq && bw < tile_px) bw *= 2;
   while (bw > 1 && bw * ew > 256) bw /= 2;
-  while (bw < kBM && (kBM / bw) * eh > 256) bw *= 2;
-  const int bh = kBM / bw;
+  while (bw < tile_px && (tile_px / bw) * eh > 256) bw *= 2;
+  const int bh = tile_px / bw;
   if (bw * ew > 256 || bh * eh > 256) return false;
   const uint64_t icb = static_cast<uint64_t>(C.ICp / kBK);
   // two k-blocks (channel blocks) per TMA box when they split evenly: the
-  // 128-wide tiles need bigger boxes to keep enough bytes in flight per SM
-  const int kd = (icb % 2 == 0) ? 2 : 1;
+  // 128-wide tiles need bigger boxes to keep enough bytes in flight per SM;
+  // the exchanged tiles (48 KB per k-block) measured faster with one k-block
+  // per stage (four stages) than with two (two stages)
+  const int kd = (!pixn && icb % 2 == 0) ? 2 : 1;
   {
     // the group's channel blocks of [N][cb_total][H_in][W_in][64] bf16
     const uint64_t dims[5] = {kBK, static_cast<uint64_t>(C.W_in), static_cast<uint64_t>(C.H_in),
@@ -92,11 +104,11 @@ inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
     const uint64_t dims[3] = {kBK, static_cast<uint64_t>(C.OC),
                               static_cast<uint64_t>(C.Kh * C.Kw) * icb};
     const uint64_t str[2] = {kBK * 2, static_cast<uint64_t>(C.OC) * kBK * 2};
-    const uint32_t box[3] = {kBK, static_cast<uint32_t>(bn), static_cast<uint32_t>(kd)};
+    const uint32_t box[3] = {kBK, static_cast<uint32_t>(oc_blk), static_cast<uint32_t>(kd)};
     if (!encode_bf16_tmap(&S.mb, C.b, 3, dims, str, box)) return false;
   }
   TcParams p{};
-  p.mode = direct ? 2 : 1;
+  p.mode = (direct ? 2 : 1) + (pixn ? 2 : 0);
   p.kd = kd;
   p.Nimg = static_cast<int>(C.N);
   p.OC = static_cast<int>(C.OC);
@@ -127,7 +139,7 @@ inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
   p.BH = bh;
   p.tiles_w = static_cast<int>((Wq + bw - 1) / bw);
   p.tiles_h = static_cast<int>((Hq + bh - 1) / bh);
-  p.tiles_oc = static_cast<int>((C.OC + bn - 1) / bn);
+  p.tiles_oc = static_cast<int>((C.OC + oc_blk - 1) / oc_blk);
   const int64_t phases = direct ? 1 : C.stride_h;
   const int64_t units = phases * C.N * p.tiles_h * p.tiles_w * p.tiles_oc;
   if (units > (1ll << 30)) return false;
@@ -151,16 +163,18 @@ inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
   p.store_mode = 0;
   p.a_bound_dev = nullptr;
   p.a_bound_host = C.a_bound;
+  p.w_bound_dev = C.w_bound;
   // Output stores.  Register staging (2): each thread keeps its pixel's
   // earlier column phases and writes osw consecutive bytes per channel at the
   // unit's last phase (osw <= 2, aligned); otherwise one byte per output.
-  const bool regstage = C.out != nullptr && C.acc_out == nullptr && bn <= 128 &&
+  const bool regstage = !pixn && C.out != nullptr && C.acc_out == nullptr && bn <= 128 &&
                         (p.osw == 1 || p.osw == 2) && C.W_out % p.osw == 0 &&
                         reinterpret_cast<uintptr_t>(C.out) % p.osw == 0;
   p.staged = regstage ? 2 : 0;
   S.p = p;
   S.bn = bn;
   S.kd = kd;
+  S.pixn = pixn;
   return true;
 }
 

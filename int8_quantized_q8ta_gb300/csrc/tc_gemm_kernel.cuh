@@ -70,12 +70,14 @@ enum : uint32_t {
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 constexpr int kBM = 128;
 constexpr int kBK = 64;             // bf16 per 128-byte row
-// Exact f32 chunks: a chunk of c k-blocks sums c * 64 products of magnitude
-// at most a_bound * 128 (|x - zp| <= a_bound, |w| <= 128), which stays an
-// exact integer in f32 while c * 64 * a_bound * 128 <= 2^24, i.e.
-// c <= 2048 / a_bound: 8 k-blocks for the int8 worst case a_bound = 255,
-// 16 for a zero point of 0 (a_bound = 128).
-constexpr int kMaxChunkKb = 16;
+// Exact f32 chunks: with |x - zp| <= a_bound and at most w_bound for the sum
+// of |w| over the 64 weights of any k-block of any row, every partial sum of
+// a chunk of c k-blocks is an integer of magnitude at most c * a_bound *
+// w_bound, exact in f32 while that is <= 2^24.  Without a measured weight
+// bound, w_bound = 64 * 128: c <= 2048 / a_bound (8 k-blocks for the int8
+// worst case a_bound = 255, 16 for a zero point of 0).
+constexpr int kWorstWBound = 64 * 128;
+constexpr int kMaxChunkKb = 256;
 constexpr int kMaxStages = 8;
 constexpr int kMaxPhases = 16;
 constexpr int kMaxEpiWarps = 16;
@@ -119,13 +121,17 @@ struct TcParams {
   uint32_t* err;     // the library's device error word
   const int32_t* a_bound_dev;  // largest |x - zp| of A, on the device (or null)
   int a_bound_host;            // the same, when a_bound_dev is null
+  const int32_t* w_bound_dev;  // largest sum of |w| over one k-block of one row (or null)
 };
 
-// Ring stages per exact f32 chunk (see kMaxChunkKb), from A's bound.
+// Ring stages per exact f32 chunk (see kWorstWBound), from A's and W's bounds.
 __device__ __forceinline__ int chunk_stages(const TcParams& p, int kd) {
   int bound = p.a_bound_dev != nullptr ? __ldg(p.a_bound_dev) : p.a_bound_host;
   if (bound < 1 || bound > 255) bound = 255;  // anything else: the int8 worst case
-  const int kb = min(kMaxChunkKb, 2048 / bound);
+  int wb = p.w_bound_dev != nullptr ? __ldg(p.w_bound_dev) : kWorstWBound;
+  if (wb > kWorstWBound || wb < 0) wb = kWorstWBound;
+  wb = max(wb, 1);  // all-zero weights: any length is exact
+  const int kb = min(kMaxChunkKb, (1 << 24) / (bound * wb));
   return max(1, kb / kd);
 }
 
@@ -260,8 +266,143 @@ __device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uin
   return ok;
 }
 
+// Exchanged operands (MODE 3 / 4): one epilogue thread holds one output
+// channel (its TMEM lane) and a run of kCols pixels of the tile (TMEM
+// columns col0 ..), row-major in the tile, BW (a power of two) per row.
+struct PixRun {
+  int64_t chan;  // offset of the output channel's plane
+  int8_t* dst;   // one-row runs: the output byte of the first pixel, phase 0
+  int oh, ow0;   // one-row runs: its output row and column (phase 0)
+  bool row;      // the run is one tile row (BW a multiple of kCols)
+  bool vec;      // ... inside the output row and 32-byte aligned: sector stores
+};
+
+template <int kCols>
+__device__ __forceinline__ PixRun pix_run(const TcParams& p, const TileInfo& ti, int oc, int col0) {
+  PixRun r;
+  r.chan = (static_cast<int64_t>(ti.n) * p.out_ch + oc) * (static_cast<int64_t>(p.H_out) * p.W_out);
+  r.row = (p.BW % kCols) == 0;
+  const int bw_log = __ffs(p.BW) - 1;
+  r.oh = (ti.hb * p.BH + (col0 >> bw_log)) * p.osh + ti.ph;
+  r.ow0 = (ti.wb * p.BW + (col0 & (p.BW - 1))) * p.osw;
+  r.dst = p.out != nullptr ? p.out + r.chan + static_cast<int64_t>(r.oh) * p.W_out + r.ow0 : nullptr;
+  r.vec = r.row && r.dst != nullptr && (p.osw == 1 || p.osw == 2) && r.oh < p.H_out &&
+          r.ow0 + kCols * p.osw <= p.W_out && (reinterpret_cast<uintptr_t>(r.dst) & 31u) == 0;
+  return r;
+}
+
+// Four f32 accumulators of one output channel -> one word of four
+// requantized bytes.
+__device__ __forceinline__ uint32_t rq_pack4(float a0, float a1, float a2, float a3, float ws,
+                                             float b, const Requant& rq) {
+  return pack4_i(requant_f(a0, ws, b, rq), requant_f(a1, ws, b, rq), requant_f(a2, ws, b, rq),
+                 requant_f(a3, ws, b, rq));
+}
+
+// Output pixel of run column c (generic placement).
+__device__ __forceinline__ bool pix_at(const TcParams& p, const TileInfo& ti, int c, int& oh,
+                                       int& ow) {
+  const int bw_log = __ffs(p.BW) - 1;
+  oh = (ti.hb * p.BH + (c >> bw_log)) * p.osh + ti.ph;
+  ow = (ti.wb * p.BW + (c & (p.BW - 1))) * p.osw + ti.pw;
+  return oh < p.H_out && ow < p.W_out;
+}
+
+// One whole 32-byte sector per thread and instruction (256-bit accesses):
+// the lanes of a warp hold different output channels, so narrower stores
+// would leave partial sectors in L2.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void ld_global_v8(const void* ptr, uint32_t (&w)[8]) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(ptr)
+               : "memory");
+}
+
+// Requantize and store the run's columns 32s .. 32s + 31 (f: the exact f32
+// accumulators).  Stride-2 column phases of one unit meet in the output:
+// phase 0 writes its bytes to the even positions (odd ones zero) and phase 1,
+// the same thread later, reads the sector back and fills the odd positions.
+template <int kCols>
+__device__ __forceinline__ void pix_store32(const TcParams& p, const TileInfo& ti, const PixRun& r,
+                                            int col0, int s, const float (&f)[32], float ws,
+                                            float b) {
+  if (r.vec && p.osw == 1) {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      w[k] = rq_pack4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3], ws, b, p.rq);
+    st_global_v8(r.dst + 32 * s, w);
+  } else if (r.vec) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      // 16 pixels of this phase -> one 32-byte sector of the output row
+      uint32_t q[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        q[k] = rq_pack4(f[16 * h + 4 * k], f[16 * h + 4 * k + 1], f[16 * h + 4 * k + 2],
+                        f[16 * h + 4 * k + 3], ws, b, p.rq);
+      int8_t* sec = r.dst + 64 * s + 32 * h;
+      uint32_t w[8];
+      if (ti.pw == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          w[2 * k] = __byte_perm(q[k], 0u, 0x4140);
+          w[2 * k + 1] = __byte_perm(q[k], 0u, 0x4342);
+        }
+      } else {
+        uint32_t e[8];
+        ld_global_v8(sec, e);  // phase 0's bytes, stored by this thread
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          w[2 * k] = __byte_perm(e[2 * k], q[k], 0x5240);
+          w[2 * k + 1] = __byte_perm(e[2 * k + 1], q[k], 0x7260);
+        }
+      }
+      st_global_v8(sec, w);
+    }
+  } else if (r.row) {
+    if (r.oh >= p.H_out) return;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int k = p.osw * (32 * s + i) + ti.pw;
+      if (r.ow0 + k < p.W_out) r.dst[k] = static_cast<int8_t>(requant_f(f[i], ws, b, p.rq));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      int oh, ow;
+      if (pix_at(p, ti, col0 + 32 * s + i, oh, ow))
+        p.out[r.chan + static_cast<int64_t>(oh) * p.W_out + ow] =
+            static_cast<int8_t>(requant_f(f[i], ws, b, p.rq));
+    }
+  }
+}
+
+// The int32 accumulators of the run's columns 32s .. 32s + 31 (debug output).
+__device__ __forceinline__ void pix_store32_acc(const TcParams& p, const TileInfo& ti,
+                                                const PixRun& r, int col0, int s,
+                                                const int32_t (&a)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    int oh, ow;
+    if (pix_at(p, ti, col0 + 32 * s + i, oh, ow))
+      p.acc_out[r.chan + static_cast<int64_t>(oh) * p.W_out + ow] = a[i];
+  }
+}
+
 // MODE 0: q8ta_linear tiles; MODE 1: transposed-convolution units; MODE 2:
-// direct-convolution tiles.
+// direct-convolution tiles.  MODE 3 / 4: the same convolutions with the
+// roles of the operands exchanged: A is 128 output channels of the packed
+// weight and B is a tile of BN output pixels, so the accumulator holds one
+// output channel per TMEM lane and a run of pixels per lane (each epilogue
+// thread writes contiguous output bytes of one channel plane), and a k-block
+// moves 16 + 32 KB for a 128 x 256 product instead of 32 KB for 128 x 128.
 // KD: k-blocks per ring stage (one TMA box spans KD k-blocks).
 // CG: 1 = one CTA per 128-row tile (cta_group::1); 2 = a cluster of two CTAs
 // shares one 256-row tile through the 2-SM MMA (cta_group::2): each CTA
@@ -272,7 +413,6 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
   constexpr int kEpiWarps = EPI;
-  constexpr int kEpiThreads = EPI * 32;
   constexpr int kColGroups = EPI / 4;     // epilogue warps sharing one TMEM lane quarter
   constexpr uint32_t kABytes = kBM * kBK * 2;   // one k-block of A
   constexpr uint32_t kBBytes = (BN / CG) * kBK * 2;  // this CTA's part of one k-block of B
@@ -293,6 +433,9 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 "per-warp scale/bias slices exceed Ctl::ep");
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM * CG, BN);
   constexpr bool kPair = (CG == 2);
+  constexpr bool kPixN = (MODE >= 3);          // output channels on M, pixels on N
+  constexpr int CM = kPixN ? MODE - 2 : MODE;  // the tile geometry: 0, 1 or 2
+  static_assert(!kPixN || CG == 1, "exchanged operands: one CTA per tile");
   static_assert(8 % KD == 0, "the worst-case chunk holds whole stages");
   constexpr uint32_t kStageBytes = static_cast<uint32_t>(KD) * (kABytes + kBBytes);
   const int S = p.stages;
@@ -357,7 +500,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       bool ok = true;
       for (int u = unit0; u < p.total_units && ok; u += unit_step) {
         for (int j = 0; j < p.subtiles && ok; ++j) {
-          const TileInfo ti = decode_tile<MODE, CG, KD>(p, u, j, rank);
+          const TileInfo ti = decode_tile<CM, CG, KD>(p, u, j, rank);
           // k-blocks in (row tap, column tap, channel block) order, with the
           // input offsets stepped incrementally: no division in this loop.
           // Linear tiles are one "tap" of kb_total channel blocks.
@@ -368,14 +511,14 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           // input coordinates of the tile's first tap: conv_t phases read
           // (oh' + dh0 - th*dsh); the direct convolution reads
           // (oh*sh - pad_h + th*dil_h) through a box with element stride sh
-          const int a_w = (MODE == 2) ? ti.wb * p.BW * p.sw - p.pad_w : ti.wb * p.BW + ti.dw0;
-          const int a_h = (MODE == 2) ? ti.hb * p.BH * p.sh - p.pad_h : ti.hb * p.BH + ti.dh0;
-          const int step_w = (MODE == 2) ? p.dil_w : -p.dsw;
-          const int step_h = (MODE == 2) ? p.dil_h : -p.dsh;
+          const int a_w = (CM == 2) ? ti.wb * p.BW * p.sw - p.pad_w : ti.wb * p.BW + ti.dw0;
+          const int a_h = (CM == 2) ? ti.hb * p.BH * p.sh - p.pad_h : ti.hb * p.BH + ti.dh0;
+          const int step_w = (CM == 2) ? p.dil_w : -p.dsw;
+          const int step_h = (CM == 2) ? p.dil_h : -p.dsh;
           for (int th = 0; th < ntaps_h && ok; ++th) {
             for (int tw = 0; tw < ntaps_w && ok; ++tw) {
               // tap (kh, kw): conv_t (rh + th*tsh, rw + tw*tsw); conv2d (th, tw)
-              const int b_blk = (MODE == 2)
+              const int b_blk = (CM == 2)
                                     ? (th * p.Kw + tw) * p.icb
                                     : ((ti.rh + th * p.tsh) * p.Kw + ti.rw + tw * p.tsw) * p.icb;
               const int c_w = a_w + tw * step_w, c_h = a_h + th * step_h;
@@ -405,6 +548,11 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                   if constexpr (MODE == 0) {
                     tma_load_3d(sa, &tmA, full, 0, ti.mb * kBM, blk);
                     tma_load_3d(sb, &tmB, full, 0, b_row, blk);
+                  } else if constexpr (kPixN) {
+                    // the weight's 128 output-channel rows are the M operand,
+                    // the pixel box the N operand
+                    tma_load_3d(sa, &tmB, full, 0, ti.ocb * kBM, b_blk + blk);
+                    tma_load_5d(sb, &tmA, full, 0, c_w, c_h, blk, ti.n);
                   } else {
                     tma_load_5d(sa, &tmA, full, 0, c_w, c_h, blk, ti.n);
                     tma_load_3d(sb, &tmB, full, 0, b_row, b_blk + blk);
@@ -435,7 +583,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       bool ok = true;
       for (int u = unit0; u < p.total_units && ok; u += unit_step) {
         for (int j = 0; j < p.subtiles && ok; ++j) {
-          const TileInfo ti = decode_tile<MODE, CG, KD>(p, u, j, rank);
+          const TileInfo ti = decode_tile<CM, CG, KD>(p, u, j, rank);
           // chunks of chunk_st stages (at most 2048 / a_bound k-blocks each)
           for (int st0 = 0; st0 < ti.nstages && ok; st0 += chunk_st) {
             const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
@@ -501,19 +649,134 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     const int group = (warp - 2) >> 2;      // which column slice
     const int row = quarter * 32 + lane;
     const int col0 = group * kColsPerWarp;
-    const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
+    const int et = threadIdx.x - 64;  // 0 .. 32 * EPI - 1
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc_it = 0, epi_phase = 0, tile_par = 0;
     int cur_ocb = -1;
+    float px_ws = 0.0f, px_b = 0.0f;  // exchanged operands: this lane's channel
     const int ew = warp - 2;  // epilogue warp index
     bool ok = true;
     for (int u = unit0; u < p.total_units && ok; u += unit_step) {
       // register staging: this thread's bytes of the unit's earlier column
       // phases, four output channels per word
-      constexpr int kHeld = (MODE != 0 && kColsPerWarp <= 64) ? kColsPerWarp / 4 : 1;
+      constexpr int kHeld = (MODE != 0 && !kPixN && kColsPerWarp <= 64) ? kColsPerWarp / 4 : 1;
       uint32_t held[kHeld];
       for (int j = 0; j < p.subtiles && ok; ++j) {
-        const TileInfo ti = decode_tile<MODE, CG, KD>(p, u, j, rank);
+        const TileInfo ti = decode_tile<CM, CG, KD>(p, u, j, rank);
+        if constexpr (kPixN) {
+          // ---- exchanged operands: lane = output channel, columns = pixels
+          const int oc = ti.ocb * kBM + row;
+          if (p.acc_out == nullptr && ti.ocb != cur_ocb) {
+            px_ws = (oc < p.OC) ? __ldg(p.ws + oc) : 0.0f;
+            px_b = (oc < p.OC && p.bias) ? __ldg(p.bias + oc) : 0.0f;
+            cur_ocb = ti.ocb;
+          }
+          const PixRun run = pix_run<kColsPerWarp>(p, ti, oc, col0);
+          const bool mine = oc < p.OC;
+          const int nchunks = (ti.nstages + chunk_st - 1) / chunk_st;
+          if (nchunks <= 1) {
+            // one exact chunk (or none: no tap reaches these pixels): the f32
+            // accumulators stream from TMEM through the requantization, 32
+            // columns at a time
+            const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
+            if (nchunks == 1) {
+              bool got = true;
+              if (lane == 0)
+                got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull,
+                               p.err);
+              got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+              if (!got) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+#pragma unroll 1
+            for (int sg = 0; sg < kColsPerWarp / 32; ++sg) {
+              uint32_t r[32];
+              if (nchunks == 1) {
+                const uint32_t ta = tmem_base + lane_addr + buf * kAccStride + col0 + 32 * sg;
+                tmem_ld_16cols(ta, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+                tmem_ld_16cols(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+                tmem_ld_wait();
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = 0u;
+              }
+              if (mine) {
+                if (p.acc_out != nullptr) {
+                  int32_t a[32];
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) a[i] = __float2int_rn(__uint_as_float(r[i]));
+                  pix_store32_acc(p, ti, run, col0, sg, a);
+                } else {
+                  float fv[32];
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) fv[i] = __uint_as_float(r[i]);
+                  pix_store32<kColsPerWarp>(p, ti, run, col0, sg, fv, px_ws, px_b);
+                }
+              }
+            }
+            if (nchunks == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+              ++acc_it;
+            }
+          } else {
+            // several chunks: int32 sums over the chunks (each chunk's f32
+            // sum is an exact integer), then the same stores from float(sum)
+            int32_t sum[kColsPerWarp];
+#pragma unroll
+            for (int c = 0; c < kColsPerWarp; ++c) sum[c] = 0;
+            for (int st0 = 0; st0 < ti.nstages; st0 += chunk_st) {
+              const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
+              bool got = true;
+              if (lane == 0)
+                got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull,
+                               p.err);
+              got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+              if (!got) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int g = 0; g < kColsPerWarp / 16; ++g) {
+                uint32_t r[16];
+                tmem_ld_16cols(tmem_base + lane_addr + buf * kAccStride + col0 + 16 * g, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  sum[16 * g + i] = static_cast<int32_t>(
+                      static_cast<uint32_t>(sum[16 * g + i]) +
+                      static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i]))));
+              }
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+              ++acc_it;
+            }
+            if (!ok) break;
+            if (mine) {
+#pragma unroll
+              for (int sg = 0; sg < kColsPerWarp / 32; ++sg) {
+                if (p.acc_out != nullptr) {
+                  int32_t a[32];
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) a[i] = sum[32 * sg + i];
+                  pix_store32_acc(p, ti, run, col0, sg, a);
+                } else {
+                  float fv[32];
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) fv[i] = __int2float_rn(sum[32 * sg + i]);
+                  pix_store32<kColsPerWarp>(p, ti, run, col0, sg, fv, px_ws, px_b);
+                }
+              }
+            }
+          }
+          continue;
+        }
         const int gcolbase = (MODE == 0) ? ti.nb * BN : ti.ocb * BN;
         const int ncols = (MODE == 0) ? p.N : p.OC;
         // The tile's column scales and biases into shared memory, loaded

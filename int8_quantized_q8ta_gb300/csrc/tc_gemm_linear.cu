@@ -80,6 +80,7 @@ cudaError_t launch_tc_linear(const TcLinear& L, cudaStream_t s) {
   p.acc_out = L.acc_out;
   p.a_bound_dev = L.a_bound_dev;
   p.a_bound_host = L.a_bound_host;
+  p.w_bound_dev = L.w_bound_dev;
   const uintptr_t oa = reinterpret_cast<uintptr_t>(L.out);
   p.store_mode = (L.N % 16 == 0 && oa % 16 == 0) ? 2 : (oa % 4 == 0 ? 1 : 0);
   if (p.total_units == 0) return cudaSuccess;

@@ -89,11 +89,12 @@ def test_linear_workspace_and_gemv_shape_guards():
 
 
 def test_workspace_sizes():
-    # bf16 copies padded to a multiple of 64 along K, 256-byte aligned
-    assert lib.q8_linear_packed_weight_bytes(11008, 4096) == 11008 * 4096 * 2
+    # bf16 copies padded to a multiple of 64 along K, 256-byte aligned; a
+    # packed weight adds a 256-byte trailer holding its per-k-block |w| bound
+    assert lib.q8_linear_packed_weight_bytes(11008, 4096) == 11008 * 4096 * 2 + 256
     # operand: the bf16 data plus a 256-byte trailer holding its |x - zp| bound
     assert lib.q8_linear_operand_bytes(2048, 4096) == 2048 * 4096 * 2 + 256
-    assert lib.q8_linear_packed_weight_bytes(4, 70) == (4 * 128 * 2 + 255) // 256 * 256
+    assert lib.q8_linear_packed_weight_bytes(4, 70) == (4 * 128 * 2 + 255) // 256 * 256 + 256
     s = q8.conv_t_shape((8, 256, 64, 64), (128, 2304), 3, 3, 128, 128, 2, 1, 1)
     assert lib.q8_conv2d_transposed_workspace_bytes(ctypes.byref(s)) == \
         8 * 64 * 64 * 256 * 2 + 128 * 9 * 256 * 2
@@ -175,7 +176,7 @@ def test_conv2d_guards_and_sizes():
     s = q8.conv2d_shape((2, 96, 10, 12), (64, 9 * 48), 3, 3, 10, 12, 1, 1, 1, 2)
     # relayout: 2 groups of 48 channels padded to 64; packed weight: 2 x 9 x 32 x 64
     assert lib.q8_conv2d_packed_workspace_bytes(ctypes.byref(s)) == 2 * 10 * 12 * 128 * 2
-    assert lib.q8_conv2d_packed_weight_bytes(ctypes.byref(s)) == 2 * 9 * 32 * 64 * 2
+    assert lib.q8_conv2d_packed_weight_bytes(ctypes.byref(s)) == 2 * 9 * 32 * 64 * 2 + 256
     assert lib.q8_conv2d_workspace_bytes(ctypes.byref(s)) == 2 * 10 * 12 * 128 * 2 + 2 * 9 * 32 * 64 * 2
     bad = q8.conv2d_shape((2, 96, 10, 12), (64, 9 * 48), 3, 3, 10, 10, 1, 1, 1, 2)  # W_out % 4
     assert lib.q8_conv2d_workspace_bytes(ctypes.byref(bad)) == 0
