@@ -324,76 +324,142 @@ __device__ __forceinline__ void ld_global_v8(const void* ptr, uint32_t (&w)[8]) 
                : "memory");
 }
 
-// Requantize and store the run's columns 32s .. 32s + 31 (f: the exact f32
-// accumulators).  Stride-2 column phases of one unit meet in the output:
-// phase 0 writes its bytes to the even positions (odd ones zero) and phase 1,
-// the same thread later, reads the sector back and fills the odd positions.
+// Requantize and store the run's columns 16g .. 16g + 15 (f: the exact f32
+// accumulators), whole sectors where the run allows:
+//   stride 1: 16 bytes; even groups wait in hold[], odd ones store both;
+//   stride 2: one sector of the output row per group.  The two column
+//     phases of a unit meet in the output: phase 0 writes its bytes to the
+//     even positions (odd ones zero), phase 1 (the same thread, later) merges
+//     its bytes into the sector phase 0 wrote, read back into e[] before.
 template <int kCols>
-__device__ __forceinline__ void pix_store32(const TcParams& p, const TileInfo& ti, const PixRun& r,
-                                            int col0, int s, const float (&f)[32], float ws,
-                                            float b) {
-  if (r.vec && p.osw == 1) {
+__device__ __forceinline__ void pix_store16(const TcParams& p, const TileInfo& ti, const PixRun& r,
+                                            int col0, int g, const float (&f)[16], float ws,
+                                            float b, uint32_t (&hold)[4], const uint32_t (&e)[8]) {
+  if (r.vec) {
+    uint32_t q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      q[k] = rq_pack4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3], ws, b, p.rq);
     uint32_t w[8];
+    if (p.osw == 1) {
+      if ((g & 1) == 0) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      w[k] = rq_pack4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3], ws, b, p.rq);
-    st_global_v8(r.dst + 32 * s, w);
-  } else if (r.vec) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      // 16 pixels of this phase -> one 32-byte sector of the output row
-      uint32_t q[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        q[k] = rq_pack4(f[16 * h + 4 * k], f[16 * h + 4 * k + 1], f[16 * h + 4 * k + 2],
-                        f[16 * h + 4 * k + 3], ws, b, p.rq);
-      int8_t* sec = r.dst + 64 * s + 32 * h;
-      uint32_t w[8];
-      if (ti.pw == 0) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          w[2 * k] = __byte_perm(q[k], 0u, 0x4140);
-          w[2 * k + 1] = __byte_perm(q[k], 0u, 0x4342);
-        }
-      } else {
-        uint32_t e[8];
-        ld_global_v8(sec, e);  // phase 0's bytes, stored by this thread
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          w[2 * k] = __byte_perm(e[2 * k], q[k], 0x5240);
-          w[2 * k + 1] = __byte_perm(e[2 * k + 1], q[k], 0x7260);
-        }
+        for (int k = 0; k < 4; ++k) hold[k] = q[k];
+        return;
       }
-      st_global_v8(sec, w);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w[k] = hold[k];
+        w[4 + k] = q[k];
+      }
+      st_global_v8(r.dst + 16 * (g - 1), w);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w[2 * k] = ti.pw == 0 ? __byte_perm(q[k], 0u, 0x4140) : __byte_perm(e[2 * k], q[k], 0x5240);
+        w[2 * k + 1] =
+            ti.pw == 0 ? __byte_perm(q[k], 0u, 0x4342) : __byte_perm(e[2 * k + 1], q[k], 0x7260);
+      }
+      st_global_v8(r.dst + 32 * g, w);
     }
   } else if (r.row) {
     if (r.oh >= p.H_out) return;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int k = p.osw * (32 * s + i) + ti.pw;
+    for (int i = 0; i < 16; ++i) {
+      const int k = p.osw * (16 * g + i) + ti.pw;
       if (r.ow0 + k < p.W_out) r.dst[k] = static_cast<int8_t>(requant_f(f[i], ws, b, p.rq));
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < 16; ++i) {
       int oh, ow;
-      if (pix_at(p, ti, col0 + 32 * s + i, oh, ow))
+      if (pix_at(p, ti, col0 + 16 * g + i, oh, ow))
         p.out[r.chan + static_cast<int64_t>(oh) * p.W_out + ow] =
             static_cast<int8_t>(requant_f(f[i], ws, b, p.rq));
     }
   }
 }
 
-// The int32 accumulators of the run's columns 32s .. 32s + 31 (debug output).
-__device__ __forceinline__ void pix_store32_acc(const TcParams& p, const TileInfo& ti,
-                                                const PixRun& r, int col0, int s,
-                                                const int32_t (&a)[32]) {
+// The sector that phase 0 of a stride-2 unit wrote for group g (read before
+// the group's accumulators, so the load overlaps them).
+__device__ __forceinline__ void pix_phase0(const TcParams& p, const TileInfo& ti, const PixRun& r,
+                                           int g, uint32_t (&e)[8]) {
+  if (r.vec && p.osw == 2 && ti.pw == 1) ld_global_v8(r.dst + 32 * g, e);
+}
+
+// The int32 accumulators of the run's columns 16g .. 16g + 15 (debug output).
+__device__ __forceinline__ void pix_store16_acc(const TcParams& p, const TileInfo& ti,
+                                                const PixRun& r, int col0, int g,
+                                                const int32_t (&a)[16]) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < 16; ++i) {
     int oh, ow;
-    if (pix_at(p, ti, col0 + 32 * s + i, oh, ow))
+    if (pix_at(p, ti, col0 + 16 * g + i, oh, ow))
       p.acc_out[r.chan + static_cast<int64_t>(oh) * p.W_out + ow] = a[i];
   }
+}
+
+// Exchanged operands, a tile of several exact chunks (a long k-loop with
+// wide input and weight bounds): the chunks' int32 sums, then the same
+// stores.  Out of line, so that its 64 live sums do not crowd the registers
+// of the single-chunk path.
+struct PixChunks {
+  uint32_t acc_it;
+  bool ok;
+};
+
+template <int kCols, uint32_t kAccStride>
+__device__ __noinline__ PixChunks pix_chunks(const TcParams& p, TileInfo ti, PixRun run, Ctl* ctl,
+                                             uint32_t tmem_row, int col0, bool mine, float ws,
+                                             float b, uint32_t acc_it, int chunk_st) {
+  const int lane = threadIdx.x & 31;
+  volatile uint32_t* abort_flag = &ctl->abort_flag;
+  int32_t sum[kCols];
+#pragma unroll
+  for (int c = 0; c < kCols; ++c) sum[c] = 0;
+  for (int st0 = 0; st0 < ti.nstages; st0 += chunk_st) {
+    const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
+    bool got = true;
+    if (lane == 0)
+      got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull, p.err);
+    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+    if (!got) return {acc_it, false};
+    tc_fence_after();
+#pragma unroll
+    for (int g = 0; g < kCols / 16; ++g) {
+      uint32_t r[16];
+      tmem_ld_16cols(tmem_row + buf * kAccStride + col0 + 16 * g, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        sum[16 * g + i] = static_cast<int32_t>(static_cast<uint32_t>(sum[16 * g + i]) +
+                                               static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i]))));
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+    ++acc_it;
+  }
+  if (mine) {
+    uint32_t hold[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int g = 0; g < kCols / 16; ++g) {
+      if (p.acc_out != nullptr) {
+        int32_t a[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = sum[16 * g + i];
+        pix_store16_acc(p, ti, run, col0, g, a);
+      } else {
+        uint32_t e[8];
+        pix_phase0(p, ti, run, g, e);
+        float fv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) fv[i] = __int2float_rn(sum[16 * g + i]);
+        pix_store16<kCols>(p, ti, run, col0, g, fv, ws, b, hold, e);
+      }
+    }
+  }
+  return {acc_it, true};
 }
 
 // MODE 0: q8ta_linear tiles; MODE 1: transposed-convolution units; MODE 2:
@@ -411,7 +477,7 @@ __device__ __forceinline__ void pix_store32_acc(const TcParams& p, const TileInf
 template <int BN, int EPI, int MODE, int KD, int CG>
 __global__ void __launch_bounds__(cta_threads(EPI), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ TcParams p) {
   constexpr int kEpiWarps = EPI;
   constexpr int kColGroups = EPI / 4;     // epilogue warps sharing one TMEM lane quarter
   constexpr uint32_t kABytes = kBM * kBK * 2;   // one k-block of A
@@ -676,7 +742,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           const int nchunks = (ti.nstages + chunk_st - 1) / chunk_st;
           if (nchunks <= 1) {
             // one exact chunk (or none: no tap reaches these pixels): the f32
-            // accumulators stream from TMEM through the requantization, 32
+            // accumulators stream from TMEM through the requantization, 16
             // columns at a time
             const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
             if (nchunks == 1) {
@@ -691,29 +757,30 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               }
               tc_fence_after();
             }
+            uint32_t hold[4] = {0u, 0u, 0u, 0u};
 #pragma unroll 1
-            for (int sg = 0; sg < kColsPerWarp / 32; ++sg) {
-              uint32_t r[32];
+            for (int g = 0; g < kColsPerWarp / 16; ++g) {
+              uint32_t e[8];
+              if (mine && p.acc_out == nullptr) pix_phase0(p, ti, run, g, e);
+              uint32_t r[16];
               if (nchunks == 1) {
-                const uint32_t ta = tmem_base + lane_addr + buf * kAccStride + col0 + 32 * sg;
-                tmem_ld_16cols(ta, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-                tmem_ld_16cols(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+                tmem_ld_16cols(tmem_base + lane_addr + buf * kAccStride + col0 + 16 * g, r);
                 tmem_ld_wait();
               } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = 0u;
+                for (int i = 0; i < 16; ++i) r[i] = 0u;
               }
               if (mine) {
                 if (p.acc_out != nullptr) {
-                  int32_t a[32];
+                  int32_t a[16];
 #pragma unroll
-                  for (int i = 0; i < 32; ++i) a[i] = __float2int_rn(__uint_as_float(r[i]));
-                  pix_store32_acc(p, ti, run, col0, sg, a);
+                  for (int i = 0; i < 16; ++i) a[i] = __float2int_rn(__uint_as_float(r[i]));
+                  pix_store16_acc(p, ti, run, col0, g, a);
                 } else {
-                  float fv[32];
+                  float fv[16];
 #pragma unroll
-                  for (int i = 0; i < 32; ++i) fv[i] = __uint_as_float(r[i]);
-                  pix_store32<kColsPerWarp>(p, ti, run, col0, sg, fv, px_ws, px_b);
+                  for (int i = 0; i < 16; ++i) fv[i] = __uint_as_float(r[i]);
+                  pix_store16<kColsPerWarp>(p, ti, run, col0, g, fv, px_ws, px_b, hold, e);
                 }
               }
             }
@@ -724,55 +791,13 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               ++acc_it;
             }
           } else {
-            // several chunks: int32 sums over the chunks (each chunk's f32
-            // sum is an exact integer), then the same stores from float(sum)
-            int32_t sum[kColsPerWarp];
-#pragma unroll
-            for (int c = 0; c < kColsPerWarp; ++c) sum[c] = 0;
-            for (int st0 = 0; st0 < ti.nstages; st0 += chunk_st) {
-              const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
-              bool got = true;
-              if (lane == 0)
-                got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull,
-                               p.err);
-              got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-              if (!got) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-#pragma unroll
-              for (int g = 0; g < kColsPerWarp / 16; ++g) {
-                uint32_t r[16];
-                tmem_ld_16cols(tmem_base + lane_addr + buf * kAccStride + col0 + 16 * g, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  sum[16 * g + i] = static_cast<int32_t>(
-                      static_cast<uint32_t>(sum[16 * g + i]) +
-                      static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i]))));
-              }
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
-              ++acc_it;
-            }
-            if (!ok) break;
-            if (mine) {
-#pragma unroll
-              for (int sg = 0; sg < kColsPerWarp / 32; ++sg) {
-                if (p.acc_out != nullptr) {
-                  int32_t a[32];
-#pragma unroll
-                  for (int i = 0; i < 32; ++i) a[i] = sum[32 * sg + i];
-                  pix_store32_acc(p, ti, run, col0, sg, a);
-                } else {
-                  float fv[32];
-#pragma unroll
-                  for (int i = 0; i < 32; ++i) fv[i] = __int2float_rn(sum[32 * sg + i]);
-                  pix_store32<kColsPerWarp>(p, ti, run, col0, sg, fv, px_ws, px_b);
-                }
-              }
+            // several chunks (each chunk's f32 sum is an exact integer)
+            const PixChunks c = pix_chunks<kColsPerWarp, kAccStride>(
+                p, ti, run, ctl, tmem_base + lane_addr, col0, mine, px_ws, px_b, acc_it, chunk_st);
+            acc_it = c.acc_it;
+            if (!c.ok) {
+              ok = false;
+              break;
             }
           }
           continue;
