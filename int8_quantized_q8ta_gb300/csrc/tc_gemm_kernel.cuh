@@ -790,8 +790,64 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
               ++acc_it;
             }
+          } else if (nchunks == 2) {
+            // two exact chunks in the two TMEM buffers: held together and
+            // streamed as one.  Each chunk sum is an integer below 2^24 in
+            // magnitude, so one f32 add rounds their exact sum once, to
+            // float(acc) (what the requantization starts from); the int32
+            // output adds the two exact conversions.  The MMA waits for both
+            // buffers meanwhile.
+            const uint32_t b0 = acc_it & 1u, b1 = (acc_it + 1u) & 1u;
+            bool got = true;
+            if (lane == 0) {
+              got = wait_bar(smem_u32(&ctl->acc_full[b0]), (acc_it >> 1) & 1u, abort_flag,
+                             kErrWaitAccFull, p.err) &&
+                    wait_bar(smem_u32(&ctl->acc_full[b1]), ((acc_it + 1u) >> 1) & 1u, abort_flag,
+                             kErrWaitAccFull, p.err);
+            }
+            got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+            if (!got) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            uint32_t hold[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 1
+            for (int g = 0; g < kColsPerWarp / 16; ++g) {
+              uint32_t e[8];
+              if (mine && p.acc_out == nullptr) pix_phase0(p, ti, run, g, e);
+              uint32_t r0[16], r1[16];
+              const uint32_t ta = tmem_base + lane_addr + col0 + 16 * g;
+              tmem_ld_16cols(ta + b0 * kAccStride, r0);
+              tmem_ld_16cols(ta + b1 * kAccStride, r1);
+              tmem_ld_wait();
+              if (mine) {
+                if (p.acc_out != nullptr) {
+                  int32_t a[16];
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    a[i] = static_cast<int32_t>(
+                        static_cast<uint32_t>(__float2int_rn(__uint_as_float(r0[i]))) +
+                        static_cast<uint32_t>(__float2int_rn(__uint_as_float(r1[i]))));
+                  pix_store16_acc(p, ti, run, col0, g, a);
+                } else {
+                  float fv[16];
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    fv[i] = __fadd_rn(__uint_as_float(r0[i]), __uint_as_float(r1[i]));
+                  pix_store16<kColsPerWarp>(p, ti, run, col0, g, fv, px_ws, px_b, hold, e);
+                }
+              }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(smem_u32(&ctl->acc_empty[b0]));
+              mbar_arrive(smem_u32(&ctl->acc_empty[b1]));
+            }
+            acc_it += 2u;
           } else {
-            // several chunks (each chunk's f32 sum is an exact integer)
+            // three chunks or more (each chunk's f32 sum is an exact integer)
             const PixChunks c = pix_chunks<kColsPerWarp, kAccStride>(
                 p, ti, run, ctl, tmem_base + lane_addr, col0, mine, px_ws, px_b, acc_it, chunk_st);
             acc_it = c.acc_it;

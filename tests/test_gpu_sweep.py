@@ -6,7 +6,9 @@ guards, at sizes the oracle finishes quickly; each case compares the int8
 output and the int32 accumulators.  The draws cover what the hand-picked
 cases may miss: odd channel counts, 1-pixel images, tiny and ragged K,
 zero points at both ends, every tile path (one CTA, CTA pairs and their
-tile widths, both convolution modes).
+tile widths, both convolution modes, and the exchanged-operand tiles of
+more than 64 output channels per group on images of at least 256 pixels
+per stride phase).
 """
 import numpy as np
 import pytest
@@ -123,3 +125,63 @@ def test_conv2d_sweep(seed):
                             groups=g))
     np.testing.assert_array_equal(acc, oracle.conv2d_acc(x, izp, w, K, K, Ho, Wo, (s, s), (p, p),
                                                          (d, d), groups=g))
+
+
+def _wide_draw(seed, transposed):
+    g = [1, 1, 2][_draw(seed, "g", 0, 2)]
+    IC = g * _draw(seed, "icg", 1, 130)
+    OC = g * _draw(seed, "ocg", 65, 200)
+    N = _draw(seed, "n", 1, 2)
+    s = _draw(seed, "s", 1, 3 if transposed else 2)
+    H_in = _draw(seed, "h", 16, 28) if transposed else s * _draw(seed, "h", 16, 34)
+    W_in = _draw(seed, "w", 16, 56) if transposed else s * _draw(seed, "w", 16, 80)
+    K = _draw(seed, "k", 1, 3)
+    p = _draw(seed, "p", 0, 1)
+    d = _draw(seed, "d", 1, 2)
+    return g, IC, OC, N, H_in, W_in, K, s, p, d
+
+
+@pytest.mark.parametrize("seed", range(400, 408))
+def test_conv_t_wide_sweep(seed):
+    g, IC, OC, N, H_in, W_in, K, s, p, d = _wide_draw(seed, True)
+    izp, ozp, act, s_in, s_out = _common(seed)
+    Hn, Wn = synth.output_hw(H_in, W_in, K, K, s, s, p, p, 0, 0, d, d)
+    Ho = max(1, Hn + _draw(seed, "oph", 0, 1))
+    Wo = max(4, (max(1, Wn) + 3) // 4 * 4)
+    x = synth.int8_uniform(seed, "x", (N, IC, H_in, W_in), -128, 127)
+    w = synth.int8_uniform(seed, "w", (OC, K * K * (IC // g)), -128, 127)
+    ws = synth.uniform_float(seed, "ws", (OC,), 0.0005, 0.01)
+    b = synth.normal(seed, "b", (OC,), 0.0, 0.2)
+    ref = oracle.conv2d_transposed(x, s_in, izp, w, K, K, ws, b, s_out, ozp, Ho, Wo, (s, s),
+                                   (p, p), (d, d), groups=g, activation=act)
+    packed = q8.pack_conv2d_transposed_weight(T(w), in_channels=IC, kernel_size=K, groups=g)
+    got = H(q8.conv2d_transposed_packed(T(x), s_in, izp, packed, T(ws), T(b), s_out, ozp,
+                                        stride=s, padding=p, dilation=d, activation=act,
+                                        output_size=(Ho, Wo)))
+    np.testing.assert_array_equal(got, ref)
+    acc = H(q8.conv2d_transposed_packed_acc32(T(x), izp, packed, (Ho, Wo), stride=s, padding=p,
+                                              dilation=d))
+    np.testing.assert_array_equal(acc, oracle.conv2d_transposed_acc(
+        x, izp, w, K, K, Ho, Wo, (s, s), (p, p), (d, d), groups=g))
+
+
+@pytest.mark.parametrize("seed", range(500, 506))
+def test_conv2d_wide_sweep(seed):
+    g, IC, OC, N, H_in, W_in, K, s, p, d = _wide_draw(seed, False)
+    izp, ozp, act, s_in, s_out = _common(seed)
+    Hn, Wn = q8.conv2d_output_size(H_in, W_in, K, s, p, d)
+    Ho, Wo = max(1, Hn), max(4, (max(1, Wn) + 3) // 4 * 4)
+    x = synth.int8_uniform(seed, "x", (N, IC, H_in, W_in), -128, 127)
+    w = synth.int8_uniform(seed, "w", (OC, K * K * (IC // g)), -128, 127)
+    ws = synth.uniform_float(seed, "ws", (OC,), 0.0005, 0.01)
+    b = synth.normal(seed, "b", (OC,), 0.0, 0.2)
+    ref = oracle.conv2d(x, s_in, izp, w, K, K, ws, b, s_out, ozp, Ho, Wo, (s, s), (p, p), (d, d),
+                        groups=g, activation=act)
+    got = H(q8.conv2d(T(x), s_in, izp, T(w), T(ws), T(b), s_out, ozp, K, stride=s, padding=p,
+                      dilation=d, groups=g, activation=act, output_size=(Ho, Wo)))
+    np.testing.assert_array_equal(got, ref)
+    packed = q8.pack_conv2d_weight(T(w), in_channels=IC, kernel_size=K, groups=g)
+    acc = H(q8.conv2d_packed_acc32(T(x), izp, packed, (Ho, Wo), stride=s, padding=p, dilation=d))
+    np.testing.assert_array_equal(acc, oracle.conv2d_acc(x, izp, w, K, K, Ho, Wo, (s, s), (p, p),
+                                                         (d, d), groups=g))
+
