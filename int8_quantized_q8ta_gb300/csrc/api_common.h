@@ -46,6 +46,8 @@ inline q8::Requant make_rq(double input_scale, double output_scale, int32_t ozp,
   r.ozp = static_cast<float>(ozp);
   r.ozp_i = ozp;
   r.lo = relu ? ozp : -128;
+  r.lo_f = static_cast<float>(r.lo - ozp);
+  r.hi_f = static_cast<float>(127 - ozp);
   return r;
 }
 

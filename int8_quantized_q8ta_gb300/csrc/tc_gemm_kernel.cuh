@@ -353,12 +353,18 @@ __device__ __forceinline__ void pix_store16(const TcParams& p, const TileInfo& t
         w[4 + k] = q[k];
       }
       st_global_v8(r.dst + 16 * (g - 1), w);
+    } else if (ti.pw == 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w[2 * k] = __byte_perm(q[k], 0u, 0x4140);
+        w[2 * k + 1] = __byte_perm(q[k], 0u, 0x4342);
+      }
+      st_global_v8(r.dst + 32 * g, w);
     } else {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        w[2 * k] = ti.pw == 0 ? __byte_perm(q[k], 0u, 0x4140) : __byte_perm(e[2 * k], q[k], 0x5240);
-        w[2 * k + 1] =
-            ti.pw == 0 ? __byte_perm(q[k], 0u, 0x4342) : __byte_perm(e[2 * k + 1], q[k], 0x7260);
+        w[2 * k] = __byte_perm(e[2 * k], q[k], 0x5240);
+        w[2 * k + 1] = __byte_perm(e[2 * k + 1], q[k], 0x7260);
       }
       st_global_v8(r.dst + 32 * g, w);
     }

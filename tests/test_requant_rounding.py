@@ -1,9 +1,13 @@
 """The CUDA epilogue's conversion-free rounding equals the plain one (CPU).
 
-The GEMM and gemv epilogues compute clamp(rint(u) + zp, -128, 127) without a
-float->int conversion instruction: u is raised to at least -2^22, 1.5 * 2^23
-is added in f32 (round to nearest even), and the integer is read from the
-sum's encoding, then clamped as an integer.  This test replays both forms in numpy float32 -- whose
+The kernels compute clamp(rint(u) + zp, lo, 127) (lo = -128, or zp under
+relu) without a float->int conversion instruction, in two forms:
+  * the quantize kernels raise u to at least -2^22, add 1.5 * 2^23 in f32
+    (round to nearest even), read the integer from the sum's encoding and
+    clamp it as an integer;
+  * the GEMM and gemv epilogues clamp u first, to [lo - zp, 127 - zp], then
+    add 1.5 * 2^23 and read the integer, already in range.
+This test replays the forms in numpy float32 -- whose
 addition rounds to nearest even like the GPU's __fadd_rn -- over every
 rounding tie near the int8 range, their float neighbours, random bit
 patterns (NaN, infinities, subnormals included) and every zero point.
@@ -34,6 +38,21 @@ def alu_only(u, zp):
     return np.clip(q, -128, 127).astype(np.int32)
 
 
+def plain_lo(u, zp, lo):
+    """plain() with the floor lo (relu: lo = zp, the clamp of max(v, 0)
+    after the requantization; NaN -> the floor)."""
+    return np.maximum(plain(u, zp), np.int32(lo)).astype(np.int32)
+
+
+def clamp_first(u, zp, lo):
+    c = np.where(np.isnan(u), F(lo - zp), u).astype(F)            # fmaxf(NaN, c) = c
+    c = np.minimum(np.maximum(c, F(lo - zp)), F(127 - zp)).astype(F)
+    y = (c + F(12582912.0)).astype(F)
+    q = y.view(np.int32).astype(np.int64) - (0x4B400000 - zp)
+    assert (q >= lo).all() and (q <= 127).all()
+    return q.astype(np.int32)
+
+
 def _samples():
     ties = np.arange(-400, 400, dtype=np.float64) + 0.5
     ints = np.arange(-400, 400, dtype=np.float64)
@@ -58,9 +77,21 @@ def test_alu_rounding_matches_rint_add_clamp_for_every_zero_point():
             np.testing.assert_array_equal(alu_only(u, zp), plain(u, zp), err_msg=f"zp={zp}")
 
 
+def test_clamp_first_matches_rint_add_clamp_for_every_zero_point_and_floor():
+    u = _samples()
+    with np.errstate(invalid="ignore", over="ignore"):
+        for zp in range(-128, 128):
+            np.testing.assert_array_equal(clamp_first(u, zp, -128), plain(u, zp),
+                                          err_msg=f"zp={zp}")
+            np.testing.assert_array_equal(clamp_first(u, zp, zp), plain_lo(u, zp, zp),
+                                          err_msg=f"relu zp={zp}")
+
+
 def test_ties_round_to_even():
     u = np.array([0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5, -127.5], dtype=F)
     assert alu_only(u, 0).tolist() == [0, 2, 2, 0, -2, -2, 126, -128]
+    assert clamp_first(u, 0, -128).tolist() == [0, 2, 2, 0, -2, -2, 126, -128]
+    assert clamp_first(u, 1, -128).tolist() == [1, 3, 3, 1, -1, -1, 127, -127]
 
 
 def test_bf16_of_small_integers_by_bit_pattern():
