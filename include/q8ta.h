@@ -74,7 +74,10 @@ int q8_version(void);
 /*
  * Device error word.  Kernels that wait on pipeline barriers give every wait
  * a time limit (about one second); on expiry they record a code here, stop
- * issuing work and return, leaving the CUDA context usable.  This call
+ * issuing work and return, leaving the CUDA context usable (codes 0x101 ..
+ * 0x106: which wait ran out).  Code 0x107: a convolution launched from a
+ * packed weight whose buffer was rewritten after packing (the host's copy of
+ * its k-block bound no longer held); that launch wrote nothing.  This call
  * synchronizes the current device, copies the word to *code (host pointer)
  * and, if clear != 0, resets it to 0.  Q8_OK is returned when the copy
  * succeeded, whatever the word holds.
@@ -298,7 +301,9 @@ q8_status q8_conv2d_transposed_acc32(const int8_t* x, const q8_conv2d_transposed
  *     first int32 is the largest sum of |w| over 64 input channels of one
  *     tap of one output channel: the kernels size their exact f32 partial
  *     sums from it (with |x - input_zero_point|), so results never depend
- *     on it;
+ *     on it.  The call waits for the packing to finish (load time) and keeps
+ *     a host copy of that bound for the buffer, from which launches pick the
+ *     kernel; rewrite a packed buffer only by packing into it again;
  *   q8_conv2d_transposed_packed runs the op from it; its workspace holds only
  *     the input copy (q8_conv2d_transposed_packed_workspace_bytes(shape));
  *   q8_conv2d_transposed_packed_acc32 writes the exact int32 accumulators

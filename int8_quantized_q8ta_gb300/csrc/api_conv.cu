@@ -12,6 +12,8 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
+#include <unordered_map>
 
 #include "api_common.h"
 #include "q8ta.h"
@@ -95,6 +97,32 @@ int32_t* packed_bound_word(const Geom& g, const void* packed) {
                                     packed_data_bytes(g));
 }
 
+// Host copies of the k-block bounds of the weights this library packed, by
+// packed buffer and size: with them a launch picks the single-chunk kernel
+// without reading the device.  A buffer without an entry (or of another
+// size) is taken at the worst case, which never picks that kernel wrongly;
+// an entry whose buffer was rewritten behind the library's back is caught
+// on the device (the kernel runs nothing and sets the error word).
+struct PackedBound {
+  size_t bytes;
+  int32_t bound;
+};
+std::mutex& bound_mutex() {
+  static std::mutex m;
+  return m;
+}
+std::unordered_map<const void*, PackedBound>& bound_map() {
+  static std::unordered_map<const void*, PackedBound> m;
+  return m;
+}
+
+int host_weight_bound(const Geom& g, const void* packed) {
+  std::lock_guard<std::mutex> lock(bound_mutex());
+  const auto it = bound_map().find(packed);
+  if (it == bound_map().end() || it->second.bytes != packed_data_bytes(g)) return q8::kWorstWBound;
+  return it->second.bound;
+}
+
 q8_status check_ptr(const void* p, size_t have, size_t need) {
   if (!p || have < need) return Q8_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(p) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
@@ -108,11 +136,12 @@ q8_status pack(const Geom& g, const int8_t* weight, void* packed, q8_stream_t st
 }
 
 // The relayout of x into `relayout`, then one GEMM per group.  w_bound: the
-// packed weight's k-block bound word, or null (the worst case).
+// packed weight's k-block bound word, or null (the worst case); w_bound_host:
+// the host's copy, or kWorstWBound.
 q8_status run(const Geom& g, const int8_t* x, double input_scale, int32_t izp, const void* packed,
-              const int32_t* w_bound, const float* ws, const float* bias, double output_scale,
-              int32_t ozp, int relu, int8_t* out, int32_t* acc_out, void* relayout,
-              q8_stream_t stream) {
+              const int32_t* w_bound, int w_bound_host, const float* ws, const float* bias,
+              double output_scale, int32_t ozp, int relu, int8_t* out, int32_t* acc_out,
+              void* relayout, q8_stream_t stream) {
   if (reinterpret_cast<uintptr_t>(packed) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
   auto* a = static_cast<__nv_bfloat16*>(relayout);
   cudaError_t e = q8::launch_nchw_to_nhwc_bf16(x, g.N, g.groups, g.ICg(), g.H_in, g.W_in, izp, a,
@@ -150,6 +179,7 @@ q8_status run(const Geom& g, const int8_t* x, double input_scale, int32_t izp, c
     C.acc_out = acc_out ? acc_out + j * g.OCg() * plane : nullptr;
     C.a_bound = a_bound_of(izp);
     C.w_bound = w_bound;
+    C.w_bound_host = w_bound != nullptr ? w_bound_host : q8::kWorstWBound;
     e = q8::launch_tc_conv_t(C, cs(stream));
     if (e != cudaSuccess) return Q8_ERR_CUDA;
   }
@@ -189,8 +219,8 @@ q8_status full(const Geom& g, const int8_t* x, double input_scale, int32_t izp,
   st = pack(g, weight, packed, stream);
   if (st != Q8_OK) return st;
   // a per-call weight copy: no bound word (that costs a pass over the weight)
-  return run(g, x, input_scale, izp, packed, nullptr, ws, bias, output_scale, ozp, relu, out,
-             acc_out, workspace, stream);
+  return run(g, x, input_scale, izp, packed, nullptr, q8::kWorstWBound, ws, bias, output_scale,
+             ozp, relu, out, acc_out, workspace, stream);
 }
 
 q8_status packed_form(const Geom& g, const int8_t* x, double input_scale, int32_t izp,
@@ -205,8 +235,9 @@ q8_status packed_form(const Geom& g, const int8_t* x, double input_scale, int32_
   if (st != Q8_OK) return st;
   st = check_ptr(workspace, workspace_bytes, relayout_bytes(g));
   if (st != Q8_OK) return st;
-  return run(g, x, input_scale, izp, packed, packed_bound_word(g, packed), ws, bias, output_scale,
-             ozp, relu, out, nullptr, workspace, stream);
+  return run(g, x, input_scale, izp, packed, packed_bound_word(g, packed),
+             host_weight_bound(g, packed), ws, bias, output_scale, ozp, relu, out, nullptr,
+             workspace, stream);
 }
 
 // The int32 accumulators from a packed weight (exact chunks sized by its
@@ -220,8 +251,8 @@ q8_status packed_acc_form(const Geom& g, const int8_t* x, int32_t izp, const voi
   if (!zp_ok(izp)) return Q8_ERR_ARG;
   st = check_ptr(workspace, workspace_bytes, relayout_bytes(g));
   if (st != Q8_OK) return st;
-  return run(g, x, 1.0, izp, packed, packed_bound_word(g, packed), nullptr, nullptr, 1.0, 0, 0,
-             nullptr, acc, workspace, stream);
+  return run(g, x, 1.0, izp, packed, packed_bound_word(g, packed), host_weight_bound(g, packed),
+             nullptr, nullptr, 1.0, 0, 0, nullptr, acc, workspace, stream);
 }
 
 q8_status pack_form(const Geom& g, const int8_t* weight, void* packed, size_t bytes,
@@ -233,8 +264,18 @@ q8_status pack_form(const Geom& g, const int8_t* weight, void* packed, size_t by
   if (st != Q8_OK) return st;
   st = pack(g, weight, packed, stream);
   if (st != Q8_OK) return st;
-  return cuda_status(q8::launch_weight_block_bound(weight, g.OC, g.ldw, g.taps(), g.ICg(),
-                                                   packed_bound_word(g, packed), cs(stream)));
+  int32_t* word = packed_bound_word(g, packed);
+  cudaError_t e = q8::launch_weight_block_bound(weight, g.OC, g.ldw, g.taps(), g.ICg(), word,
+                                                cs(stream));
+  // the host's copy of the bound (load time: the call waits for the pack)
+  int32_t host = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&host, word, sizeof(host), cudaMemcpyDeviceToHost, cs(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs(stream));
+  if (e != cudaSuccess) return Q8_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(bound_mutex());
+  bound_map()[packed] = PackedBound{packed_data_bytes(g), host};
+  return Q8_OK;
 }
 
 size_t sized(const Geom& g, size_t bytes) { return check_geom(g) == Q8_OK ? bytes : 0; }

@@ -79,6 +79,10 @@ cudaError_t launch_conv_weight_bf16(const int8_t* w, int64_t groups, int64_t OCg
                                     cudaStream_t s);
 
 // ---- tensor-core GEMM (tc_gemm.cu) -----------------------------------------
+// The largest sum of |w| over one k-block (64 weights) of one row for any
+// int8 weight: the chunk bound used when a weight's own bound is unknown.
+constexpr int kWorstWBound = 64 * 128;
+
 struct TcLinear {
   const __nv_bfloat16* a;  // [M, Kp] bf16, values x - input_zero_point
   const __nv_bfloat16* b;  // [N, Kp] bf16, weight values
@@ -119,6 +123,10 @@ struct TcConvT {
   int32_t* acc_out;  // int32 debug output laid out like out, or null
   int a_bound;       // largest |x - input_zero_point| (see TcLinear)
   const int32_t* w_bound;  // per-k-block weight bound on the device, or null (see TcLinear)
+  // The host's copy of that bound (recorded when the weight was packed), or
+  // 64 * 128, the worst case, when unknown: with it the host picks the
+  // single-chunk kernel, which checks the device bound again.
+  int w_bound_host;
 };
 cudaError_t launch_tc_conv_t(const TcConvT& p, cudaStream_t s);
 

@@ -52,8 +52,19 @@ struct ConvSetup {
   CUtensorMap ma, mb;
   TcParams p;
   int bn, kd;
-  bool pixn;  // output channels on the MMA's M side, bn pixels on N
+  bool pixn;    // output channels on the MMA's M side, bn pixels on N
+  bool single;  // every sub-tile fits one exact chunk (the host's bounds)
 };
+
+// Ring stages per exact f32 chunk, as the kernel's chunk_stages computes it
+// from the same bounds.
+inline int host_chunk_stages(int a_bound, int w_bound, int kd) {
+  if (a_bound < 1 || a_bound > 255) a_bound = 255;
+  if (w_bound > kWorstWBound || w_bound < 0) w_bound = kWorstWBound;
+  w_bound = std::max(w_bound, 1);
+  const int kb = std::min(kMaxChunkKb, (1 << 24) / (a_bound * w_bound));
+  return std::max(1, kb / kd);
+}
 
 // Pixels of an exchanged-operand tile (the MMA's N).
 constexpr int kPixTile = 256;
@@ -145,6 +156,17 @@ inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
   if (units > (1ll << 30)) return false;
   p.total_units = static_cast<int>(units);
   p.subtiles = direct ? 1 : static_cast<int>(C.stride_w);
+  // the most ring stages of any sub-tile (taps x channel-block stages)
+  int max_taps = static_cast<int>(C.Kh * C.Kw);
+  if (!direct) {
+    int th = 0, tw = 0;
+    for (int ph = 0; ph < C.stride_h; ++ph)
+      th = std::max(th, conv_t_phase_taps(ph, C.pad_h, C.stride_h, C.dil_h, C.Kh));
+    for (int pw = 0; pw < C.stride_w; ++pw)
+      tw = std::max(tw, conv_t_phase_taps(pw, C.pad_w, C.stride_w, C.dil_w, C.Kw));
+    max_taps = th * tw;
+  }
+  p.max_nstages = max_taps * static_cast<int>((icb + kd - 1) / kd);
   if (!direct && C.stride_h <= kMaxPhases) {
     // row phases with more taps first, so the heaviest units start earliest
     int order[kMaxPhases], taps[kMaxPhases];
@@ -175,6 +197,7 @@ inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
   S.bn = bn;
   S.kd = kd;
   S.pixn = pixn;
+  S.single = p.max_nstages <= host_chunk_stages(C.a_bound, C.w_bound_host, kd);
   return true;
 }
 

@@ -65,6 +65,7 @@ enum : uint32_t {
   kErrWaitAccEmpty = 0x104,
   kErrWaitDrain = 0x105,
   kErrWaitEpi = 0x106,
+  kErrChunks = 0x107,  // a single-chunk kernel met a tile of several chunks
 };
 
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
@@ -75,8 +76,8 @@ constexpr int kBK = 64;             // bf16 per 128-byte row
 // a chunk of c k-blocks is an integer of magnitude at most c * a_bound *
 // w_bound, exact in f32 while that is <= 2^24.  Without a measured weight
 // bound, w_bound = 64 * 128: c <= 2048 / a_bound (8 k-blocks for the int8
-// worst case a_bound = 255, 16 for a zero point of 0).
-constexpr int kWorstWBound = 64 * 128;
+// worst case a_bound = 255, 16 for a zero point of 0).  kWorstWBound:
+// q8ta_internal.h.
 constexpr int kMaxChunkKb = 256;
 constexpr int kMaxStages = 8;
 constexpr int kMaxPhases = 16;
@@ -94,6 +95,7 @@ struct TcParams {
   int kd;            // k-blocks per ring stage (1 or 2): one TMA box holds kd k-blocks
   int total_units;   // work units; a unit is `subtiles` consecutive tiles
   int subtiles;      // 1 (linear) or stride_w (transposed convolution)
+  int max_nstages;   // the most ring stages of any sub-tile (convolutions)
   // linear
   int M, N, kb_total, tiles_m;
   // transposed convolution
@@ -469,12 +471,14 @@ __device__ __noinline__ PixChunks pix_chunks(const TcParams& p, TileInfo ti, Pix
 }
 
 // MODE 0: q8ta_linear tiles; MODE 1: transposed-convolution units; MODE 2:
-// direct-convolution tiles.  MODE 3 / 4: the same convolutions with the
+// direct-convolution tiles.  MODE 3 / 4 (5 / 6): the same convolutions with the
 // roles of the operands exchanged: A is 128 output channels of the packed
 // weight and B is a tile of BN output pixels, so the accumulator holds one
 // output channel per TMEM lane and a run of pixels per lane (each epilogue
 // thread writes contiguous output bytes of one channel plane), and a k-block
 // moves 16 + 32 KB for a 128 x 256 product instead of 32 KB for 128 x 128.
+// MODE 5 / 6 hold only the single-chunk path (no register pressure from the
+// multi-chunk ones); the host picks them when every sub-tile fits one chunk.
 // KD: k-blocks per ring stage (one TMA box spans KD k-blocks).
 // CG: 1 = one CTA per 128-row tile (cta_group::1); 2 = a cluster of two CTAs
 // shares one 256-row tile through the 2-SM MMA (cta_group::2): each CTA
@@ -505,8 +509,9 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 "per-warp scale/bias slices exceed Ctl::ep");
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM * CG, BN);
   constexpr bool kPair = (CG == 2);
-  constexpr bool kPixN = (MODE >= 3);          // output channels on M, pixels on N
-  constexpr int CM = kPixN ? MODE - 2 : MODE;  // the tile geometry: 0, 1 or 2
+  constexpr bool kPixN = (MODE >= 3);                  // output channels on M, pixels on N
+  constexpr bool kSingleOnly = (MODE >= 5);            // every sub-tile one exact chunk
+  constexpr int CM = kPixN ? (MODE - 3) % 2 + 1 : MODE;  // the tile geometry: 0, 1 or 2
   static_assert(!kPixN || CG == 1, "exchanged operands: one CTA per tile");
   static_assert(8 % KD == 0, "the worst-case chunk holds whole stages");
   constexpr uint32_t kStageBytes = static_cast<uint32_t>(KD) * (kABytes + kBBytes);
@@ -526,8 +531,6 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
   // persistent loop over units: a CTA pair walks the units together
   const int unit0 = static_cast<int>(blockIdx.x) / CG;
   const int unit_step = static_cast<int>(gridDim.x) / CG;
-  // exact-f32 chunk length in ring stages (MMA issuer and epilogue agree)
-  const int chunk_st = chunk_stages(p, KD);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -563,8 +566,23 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
   // set-up done: from here on global memory is read and written
   pdl_wait();
   pdl_launch_dependents();
+  // exact-f32 chunk length in ring stages (MMA issuer and epilogue agree),
+  // from bound words that the previous kernel may have written
+  const int chunk_st = chunk_stages(p, KD);
+  // The single-chunk instantiation runs only where the host's choice holds
+  // on the device too; otherwise (a packed weight changed after packing)
+  // nothing runs and the error word says why.
+  bool run = true;
+  if constexpr (kSingleOnly) {
+    if (p.max_nstages > chunk_st) {
+      run = false;
+      if (threadIdx.x == 0 && blockIdx.x == 0) atomicCAS(p.err, 0u, kErrChunks);
+    }
+  }
 
-  if (warp == 0) {
+  if (!run) {
+    // nothing to do (see above)
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
@@ -796,6 +814,9 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
               ++acc_it;
             }
+          } else if constexpr (kSingleOnly) {
+            ok = false;  // excluded on entry (max_nstages <= chunk_st)
+            break;
           } else if (nchunks == 2) {
             // two exact chunks in the two TMEM buffers: held together and
             // streamed as one.  Each chunk sum is an integer below 2^24 in

@@ -86,3 +86,46 @@ def test_conv2d_packed_bound_takes_the_largest_block():
     acc = H(q8.conv2d_packed_acc32(T(x), 127, packed, (Ho, Wo), stride=1, padding=1))
     np.testing.assert_array_equal(acc, acc_ref)
 
+
+def test_operand_reused_back_to_back_with_a_wider_zero_point():
+    """Two acc32 calls on one workspace, back to back: the second prepares
+    its operand with zero point 127 (|x - zp| bound 255, chunks of 8 k-blocks
+    against all-127 weights) over the first one's (zero point 0: chunks of
+    16).  The GEMM reads the operand's bound word only after the preceding
+    kernel has finished (programmatic dependent launch), so it never sizes
+    its chunks from the earlier zero point."""
+    M, K, N = 256, 4096, 256
+    x = np.full((M, K), -128, dtype=np.int8)
+    w = np.full((N, K), 127, dtype=np.int8)
+    packed = q8.pack_weight(T(w))
+    ws = torch.empty(1 << 26, dtype=torch.uint8, device=DEV)
+    xt = T(x)
+    a0 = q8.linear_packed_acc32(xt, 0, packed, workspace=ws)
+    a1 = q8.linear_packed_acc32(xt, 127, packed, workspace=ws)
+    ref1 = oracle.linear_acc(x, 127, w)
+    assert abs(int(ref1.min())) > 1 << 24
+    np.testing.assert_array_equal(H(a1), ref1)
+    np.testing.assert_array_equal(H(a0), oracle.linear_acc(x, 0, w))
+
+
+def test_conv_packed_buffer_rewritten_after_packing_is_caught():
+    """The host records a packed weight's bound when it packs it and picks
+    the single-chunk kernel from that record; a buffer rewritten afterwards
+    with a weight that needs shorter chunks is caught on the device: the
+    kernel runs nothing and sets the error word (0x107)."""
+    N, IC, Hi, Wi, K, OC = 1, 256, 16, 64, 3, 128
+    x = np.full((N, IC, Hi, Wi), -128, dtype=np.int8)
+    w_small = synth.int8_uniform(9, "w", (OC, K * K * IC), -2, 2)
+    w_big = w_small.copy()
+    w_big[5] = 127
+    Ho, Wo = synth.output_hw(Hi, Wi, K, K, 2, 2, 1, 1, 1, 1)
+    pa = q8.pack_conv2d_transposed_weight(T(w_small), in_channels=IC, kernel_size=K)
+    pb = q8.pack_conv2d_transposed_weight(T(w_big), in_channels=IC, kernel_size=K)
+    pa.data.copy_(pb.data)          # behind the library's back
+    q8.conv2d_transposed_packed_acc32(T(x), 127, pa, (Ho, Wo), stride=2, padding=1)
+    torch.cuda.synchronize()
+    assert q8.device_error(clear=True) == 0x107
+    acc = H(q8.conv2d_transposed_packed_acc32(T(x), 127, pb, (Ho, Wo), stride=2, padding=1))
+    np.testing.assert_array_equal(acc, oracle.conv2d_transposed_acc(x, 127, w_big, K, K, Ho, Wo,
+                                                                    (2, 2), (1, 1), (1, 1)))
+
