@@ -10,12 +10,14 @@
 // w in [-128, 127], both exact in bf16, and every product (|p| <= 32640) is
 // exact in the f32 accumulator.  The K loop is cut into chunks whose f32
 // partial sums stay within 2^24 in magnitude and are therefore exact
-// integers: at most 2048 / b k-blocks of 64, b = max(128 + zp, 127 - zp)
-// being the largest |x - zp| (8 k-blocks = 512 products for b = 255, 16 for
-// zp = 0).  Each chunk's TMEM accumulator is drained by the epilogue warps
-// into int32 registers (exact conversion) while the MMA warp already fills
-// the other TMEM buffer.  Integer addition of the chunk sums is exact
-// (modulo 2^32, like the pages' i32 accumulator).
+// integers: at most 2^24 / (b * W) k-blocks of 64, b = max(128 + zp,
+// 127 - zp) being the largest |x - zp| and W the largest sum of |w| over one
+// k-block of one weight row (64 * 128 when the weight's own bound is not
+// known: 8 k-blocks for b = 255, 16 for zp = 0).  Each chunk's TMEM
+// accumulator is drained by the epilogue warps into int32 registers (exact
+// conversion) while the MMA warp already fills the other TMEM buffer.
+// Integer addition of the chunk sums is exact (modulo 2^32, like the pages'
+// i32 accumulator).
 //
 // Transposed convolution is an implicit GEMM per stride phase: outputs with
 // oh % stride_h == ph and ow % stride_w == pw all use the same taps, those
@@ -27,14 +29,16 @@
 // outside the input are filled with zeros by the TMA unit, which is exactly
 // "taps outside the input contribute nothing" because the stored values are
 // x - input_zero_point.  The direct convolution (mode 2) reads each tap's
-// window through a box with element strides (stride_w, stride_h).
+// window through a box with element strides (stride_w, stride_h).  Above 64
+// output channels per group the convolutions exchange the operands (modes
+// 3 to 6, see the kernel): 128 output channels on the MMA's M side, 256
+// output pixels on N.
 //
 // Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one thread)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2..   E epilogue warps (8, 12 or 16): warp w reads TMEM lanes
-//               32*(w%4)..+31 and BN / (E/4) of the tile's columns, keeping
-//               the int32 running sums in registers
+//               32*(w%4)..+31 and BN / (E/4) of the tile's columns
 // With CTA pairs (CG = 2, a cluster of two CTAs on neighbouring SMs) one
 // 256 x BN tile is computed by the 2-SM MMA: each CTA loads its own 128 rows
 // of A and half of the BN rows of B, the leader CTA's MMA thread issues the
