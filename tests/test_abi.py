@@ -180,3 +180,28 @@ def test_conv2d_guards_and_sizes():
     assert lib.q8_conv2d_workspace_bytes(ctypes.byref(s)) == 2 * 10 * 12 * 128 * 2 + 2 * 9 * 32 * 64 * 2
     bad = q8.conv2d_shape((2, 96, 10, 12), (64, 9 * 48), 3, 3, 10, 10, 1, 1, 1, 2)  # W_out % 4
     assert lib.q8_conv2d_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+def test_packed_acc32_guards():
+    """The int32-accumulator forms from packed convolution weights refuse
+    bad arguments on the host, before anything is enqueued."""
+    st = q8.conv_t_shape((1, 64, 8, 8), (96, 9 * 64), 3, 3, 16, 16, 2, 1, 1)
+    sd = q8.conv2d_shape((1, 64, 8, 8), (96, 9 * 64), 3, 3, 8, 8, 1, 1, 1, 1)
+    need_t = lib.q8_conv2d_transposed_packed_workspace_bytes(ctypes.byref(st))
+    need_d = lib.q8_conv2d_packed_workspace_bytes(ctypes.byref(sd))
+    assert need_t > 0 and need_d > 0
+    for fn, s, need in ((lib.q8_conv2d_transposed_packed_acc32, st, need_t),
+                        (lib.q8_conv2d_packed_acc32, sd, need_d)):
+        assert fn(None, ctypes.byref(s), 0, FAKE, FAKE, FAKE, need, None) == q8.Q8_ERR_NULL
+        assert fn(FAKE, ctypes.byref(s), 0, None, FAKE, FAKE, need, None) == q8.Q8_ERR_NULL
+        assert fn(FAKE, ctypes.byref(s), 0, FAKE, None, FAKE, need, None) == q8.Q8_ERR_NULL
+        assert fn(FAKE, None, 0, FAKE, FAKE, FAKE, need, None) == q8.Q8_ERR_NULL
+        assert fn(FAKE, ctypes.byref(s), 128, FAKE, FAKE, FAKE, need, None) == q8.Q8_ERR_ARG
+        assert fn(FAKE, ctypes.byref(s), 0, FAKE, FAKE, FAKE, need - 1, None) == \
+            q8.Q8_ERR_WORKSPACE
+        assert fn(FAKE, ctypes.byref(s), 0, FAKE, FAKE, None, need, None) == q8.Q8_ERR_WORKSPACE
+        assert fn(FAKE, ctypes.byref(s), 0, FAKE, FAKE, ctypes.c_void_p(0x10010), need,
+                  None) == q8.Q8_ERR_ALIGN
+    bad = q8.conv_t_shape((1, 64, 8, 8), (96, 9 * 64), 3, 3, 16, 14, 2, 1, 1)   # W_out % 4
+    assert lib.q8_conv2d_transposed_packed_acc32(FAKE, ctypes.byref(bad), 0, FAKE, FAKE, FAKE,
+                                                 need_t, None) == q8.Q8_ERR_SHAPE
