@@ -247,6 +247,134 @@ class Path:
         rec(5)
 
 
+GEMV_CHAIN_COPIES = 24   # 24 x 16.8 MB of weights: 403 MB, more than 3x the 129 MB L2
+GEMV_CHAIN_REPS = 20
+
+
+def gemv_chain_measure(path, copies=GEMV_CHAIN_COPIES, reps=GEMV_CHAIN_REPS):
+    """q8ta_linear_gemv as a decode step runs it: `copies` gemvs back to back,
+    each on its own weight (like successive layers), no event or host work
+    between them, captured once in a CUDA graph (so the host's per-call cost
+    is not what is timed) and replayed `reps` times.  The weights total more
+    than 2x L2, so every call streams its weight from HBM.  Returns
+    (microseconds per call, whether a graph was used); checks that every
+    call's output equals the lone call's (same x, same weight values)."""
+    torch, q8 = path.torch, path.q8
+    gp = G.params
+    weights = [path.gw.clone() for _ in range(copies)]
+    outs = [torch.empty((1, GN), dtype=torch.int8, device=path.dev) for _ in range(copies)]
+
+    def chain():
+        for i in range(copies):
+            q8.linear_gemv(path.gx, gp["in_scale"], gp["in_zp"], weights[i], None, path.gws,
+                           path.gb, gp["out_scale"], gp["out_zp"], out=outs[i])
+
+    for _ in range(2):
+        chain()
+    torch.cuda.synchronize()
+    graph = None
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            chain()
+        graph = g
+    except RuntimeError:
+        torch.cuda.synchronize()
+        graph = None
+    run = graph.replay if graph is not None else chain
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+    for o in outs:
+        if not torch.equal(o, path.g_out):
+            raise RuntimeError("gemv chain: a chained call's output differs from the lone call's")
+    del weights, outs, graph
+    return us, run is not chain
+
+
+def small_op_latency(fn, reps=60, warm=10):
+    """Median microseconds of fn() over `reps` calls, each bracketed by CUDA
+    events on the launching stream (launch gaps included), after `warm`."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for a, b in evs:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+
+
+def small_configs_measure(dev):
+    """The two latency-bound workloads: quantize -> q8ta_linear 8x64x32 and
+    the 1x64x32x32 -> 1x32x64x64 transposed convolution (packed weights,
+    buffers allocated once).  Returns their ops entries."""
+    import torch
+    import int8_quantized_q8ta_gb300 as q8
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    w0 = synth.CONFIGS["linear_chain_8x64x32"]
+    d0, p0 = w0.dims, w0.params
+    x, w, ws, b = synth.linear_inputs(w0.seed, d0["M"], d0["K"], d0["N"], x_kind="fp32", p=p0)
+    x, ws, b = T(x), T(ws), T(b)
+    packed = q8.pack_weight(T(w))
+    xq = torch.empty((d0["M"], d0["K"]), dtype=torch.int8, device=dev)
+    operand = q8.operand_buffer(d0["M"], d0["K"], dev)
+    out0 = torch.empty((d0["M"], d0["N"]), dtype=torch.int8, device=dev)
+
+    def cfg0():
+        q8.quantize_to_operand(x, p0["in_scale"], p0["in_zp"], x_q=xq, operand=operand)
+        q8.linear_operand_packed(operand, p0["in_scale"], packed, ws, b, p0["out_scale"],
+                                 p0["out_zp"], out=out0)
+
+    w3 = synth.CONFIGS["conv_t_1x64x32x32_k4s2"]
+    d3, p3 = w3.dims, w3.params
+    cx, cw, cws, cb = synth.conv_t_inputs(w3.seed, d3, p3)
+    cx, cws, cb = T(cx), T(cws), T(cb)
+    Ho, Wo = synth.output_hw(d3["H_in"], d3["W_in"], d3["Kh"], d3["Kw"], d3["s"], d3["s"],
+                             d3["p"], d3["p"], d3["op"], d3["op"])
+    cpk = q8.pack_conv2d_transposed_weight(T(cw), d3["IC"], (d3["Kh"], d3["Kw"]))
+    shape = q8.conv_t_shape(tuple(cx.shape), tuple(cw.shape), d3["Kh"], d3["Kw"], Ho, Wo,
+                            d3["s"], d3["p"], d3["op"])
+    import ctypes
+    cws_buf = torch.empty(q8.lib().q8_conv2d_transposed_packed_workspace_bytes(
+        ctypes.byref(shape)), dtype=torch.uint8, device=dev)
+    out3 = torch.empty((d3["N"], d3["OC"], Ho, Wo), dtype=torch.int8, device=dev)
+
+    def cfg3():
+        q8.conv2d_transposed_packed(cx, p3["in_scale"], p3["in_zp"], cpk, cws, cb,
+                                    p3["out_scale"], p3["out_zp"], stride=d3["s"],
+                                    padding=d3["p"], output_padding=d3["op"], out=out3,
+                                    workspace=cws_buf)
+
+    us0 = small_op_latency(cfg0)
+    us3 = small_op_latency(cfg3)
+    macs3 = conv_valid_macs(d3, Ho, Wo)
+    return {
+        "linear_chain_8x64x32": {
+            "us": us0, "launches": 2, "TOPS": 2 * d0["M"] * d0["N"] * d0["K"] / us0 / 1e6,
+            "method": "median of 60 calls after 10, each bracketed by CUDA events "
+                      "(quantize->operand launch + GEMM launch; launch gaps included)"},
+        "q8ta_conv2d_transposed_1x64x32x32": {
+            "us": us3, "launches": 2, "outputs/s": d3["N"] * d3["OC"] * Ho * Wo / us3 * 1e6,
+            "TOPS_valid_taps": 2 * macs3 / us3 / 1e6,
+            "method": "median of 60 calls after 10, each bracketed by CUDA events "
+                      "(input relayout + GEMM; packed weight)"},
+    }
+
+
 def e2e_measure(paths, h, steps):
     """The step through the public API with host buffers: every activation is
     copied in from pinned host memory and every output copied back to pinned
@@ -311,61 +439,70 @@ def e2e_measure(paths, h, steps):
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle baseline (bounded sample of the same workload)
+# CPU oracle baseline: the whole step scaled down by the same factor in every op
 # ---------------------------------------------------------------------------
-def cpu_oracle_step_estimate(h, budget_s=12.0):
-    """Time the oracle on a bounded sample of each op on all host cores and
-    scale each op to its full size.  Returns (seconds per full step, cores,
-    sample description)."""
+ORACLE_SCALE = 64   # the oracle's step is 1/64 of the full step's work in every op
+
+
+def oracle_scaled_step(h, threads=None, scale=ORACLE_SCALE):
+    """Run the oracle, as it stands, on 1/scale of every op of the step and
+    time it: quantize numel/scale elements; the chain's quantize and linear
+    on M/scale rows; the gemv on N/scale weight rows; the transposed
+    convolution on (images x output channels)/scale whole output planes.
+    The work is exactly OPS_STEP/scale int8 MACs x 2, so the rate needs no
+    extrapolation.  Returns (seconds, threads used, description, per-op
+    seconds)."""
     import oracle
     oracle.build()
-    cores = os.cpu_count() or 1
+    threads = threads or (os.cpu_count() or 1)
     qp, lp, gp, cp = Q.params, L.params, G.params, C.params
-    # sample sizes (units of work that scale linearly)
-    q_n = 1 << 22                        # elements of the quantize
-    l_rows = max(cores, 8)               # rows of the 2048-row prefill
-    c_oc = 2                             # output channels of one conv image
-    xq_l = oracle.quantize_per_tensor(h["lx"][:l_rows], lp["in_scale"], lp["in_zp"])
+    q_n = QN // scale
+    l_rows = LM // scale
+    g_rows = GN // scale
+    planes = CD["N"] * CD["OC"] // scale
     Ho, Wo = CHo, CWo
 
-    def run_quant(i):
-        n = q_n // cores
-        oracle.quantize_per_tensor(h["xq"][i * n:(i + 1) * n], qp["in_scale"], qp["in_zp"])
+    def chunks(n, parts):
+        step = (n + parts - 1) // parts
+        return [(a, min(n, a + step)) for a in range(0, n, step)]
 
-    def run_lin(i):
-        oracle.linear(xq_l[i:i + 1], lp["in_scale"], lp["in_zp"], h["lw"], h["lws"], h["lb"],
+    def run_quant(ab):
+        oracle.quantize_per_tensor(h["xq"][ab[0]:ab[1]], qp["in_scale"], qp["in_zp"])
+
+    def run_chain(r):
+        xq = oracle.quantize_per_tensor(h["lx"][r:r + 1], lp["in_scale"], lp["in_zp"])
+        oracle.linear(xq, lp["in_scale"], lp["in_zp"], h["lw"], h["lws"], h["lb"],
                       lp["out_scale"], lp["out_zp"])
 
-    def run_gemv(i):
-        if i == 0:
-            oracle.linear(h["gx"], gp["in_scale"], gp["in_zp"], h["gw"], h["gws"], h["gb"],
-                          gp["out_scale"], gp["out_zp"])
+    def run_gemv(ab):
+        a, b = ab
+        oracle.linear(h["gx"], gp["in_scale"], gp["in_zp"], h["gw"][a:b], h["gws"][a:b],
+                      h["gb"][a:b], gp["out_scale"], gp["out_zp"])
 
     def run_conv(i):
-        if i < c_oc:
-            oracle.conv2d_transposed(h["cx"][:1], cp["in_scale"], cp["in_zp"], h["cw"][i:i + 1],
-                                     CD["Kh"], CD["Kw"], h["cws"][i:i + 1], h["cb"][i:i + 1],
-                                     cp["out_scale"], cp["out_zp"], Ho, Wo, (CD["s"], CD["s"]),
-                                     (CD["p"], CD["p"]))
+        n, oc = divmod(i, CD["OC"])
+        oracle.conv2d_transposed(h["cx"][n:n + 1], cp["in_scale"], cp["in_zp"],
+                                 h["cw"][oc:oc + 1], CD["Kh"], CD["Kw"], h["cws"][oc:oc + 1],
+                                 h["cb"][oc:oc + 1], cp["out_scale"], cp["out_zp"], Ho, Wo,
+                                 (CD["s"], CD["s"]), (CD["p"], CD["p"]))
 
-    def timed(fn, n_items):
-        t0 = time.perf_counter()
-        with cf.ThreadPoolExecutor(max_workers=cores) as ex:   # ctypes releases the GIL
-            list(ex.map(fn, range(n_items)))
-        return time.perf_counter() - t0
-
-    t_q = timed(run_quant, cores) * (QN / (q_n // cores * cores))
-    t_l = timed(run_lin, l_rows) * (LM / l_rows)
-    t_g = timed(run_gemv, 1)
-    t_c = timed(run_conv, c_oc) * (CD["N"] * CD["OC"] / c_oc)
-    # the chain's quantize of [2048, 4096] at the quantize's measured rate
-    t_cq = t_q * (LM * LK) / QN
-    total = t_q + t_cq + t_l + t_g + t_c
-    sample = (f"quantize {q_n} of {QN} elements; linear {l_rows} of {LM} rows; gemv full; "
-              f"conv_t 1 of {CD['N']} images x {c_oc} of {CD['OC']} channels; "
-              f"each scaled linearly to the full op")
-    return total, cores, sample, dict(quantize=t_q, chain_quantize=t_cq, linear=t_l, gemv=t_g,
-                                      conv_t=t_c)
+    parts = {}
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:   # ctypes releases the GIL
+        def timed(name, fn, items):
+            t0 = time.perf_counter()
+            list(ex.map(fn, items))
+            parts[name] = time.perf_counter() - t0
+        timed("quantize", run_quant, chunks(q_n, threads))
+        timed("chain_quantize_linear", run_chain, range(l_rows))
+        timed("gemv", run_gemv, chunks(g_rows, min(threads, max(1, g_rows // 8))))
+        # output planes spread over the images, as the full op's are
+        timed("conv_t", run_conv, [(k * CD["N"] * CD["OC"]) // planes for k in range(planes)])
+    total = sum(parts.values())
+    sample = (f"1/{scale} of every op of the step, timed whole: quantize {q_n} of {QN} "
+              f"elements; quantize->linear {l_rows} of {LM} rows; gemv {g_rows} of {GN} weight "
+              f"rows; conv_t {planes} of {CD['N'] * CD['OC']} (image, channel) output planes; "
+              f"{threads} thread(s), one oracle call per row block or plane")
+    return total, threads, sample, parts
 
 
 def traffic_from_profile(key="tc_gemm_linear_2048x4096x11008"):
@@ -446,6 +583,13 @@ def run_ours(args, rank, world, local_rank):
     if dist:
         ms_step = max_over_ranks(ms_step, dev)
 
+    extra_ops = {}
+    chained = args.only in ("all", "gemv") and not args.no_extra_ops
+    if chained:
+        chain_us, chain_graph = gemv_chain_measure(path)
+    if args.only == "all" and not args.no_extra_ops:
+        extra_ops = small_configs_measure(dev)
+
     names = ["quantize", "chain_prep", "linear", "gemv", "conv_t"]
     per = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
            for i, n in enumerate(names)}
@@ -460,12 +604,24 @@ def run_ours(args, rank, world, local_rank):
         "q8ta_linear_2048x4096x11008": {"us": us["linear"],
                                         "TOPS": OPS_LINEAR / us["linear"] / 1e6,
                                         "frac_bf16_peak": OPS_LINEAR / us["linear"] / 1e6 / bf16},
-        "q8ta_linear_gemv_1x4096x4096": {"us": us["gemv"], "GB/s": BYTES_GEMV / us["gemv"] / 1e3,
-                                         "frac_hbm": BYTES_GEMV / us["gemv"] / 1e3 / hbm},
+        "q8ta_linear_gemv_1x4096x4096": {
+            "us": us["gemv"], "GB/s": BYTES_GEMV / us["gemv"] / 1e3,
+            "frac_hbm": BYTES_GEMV / us["gemv"] / 1e3 / hbm,
+            "note": "one launch bracketed by events inside the step pass (its launch and "
+                    "DRAM ramp are not overlapped)"},
         "q8ta_conv2d_transposed_8x256x64x64": {
             "us": us["conv_t"], "outputs/s": CONV_OUTPUTS / us["conv_t"] * 1e6,
             "TOPS_valid_taps": OPS_CONV / us["conv_t"] / 1e6},
     }
+    if chained:
+        ops["q8ta_linear_gemv_1x4096x4096_chained"] = {
+            "us_per_call": chain_us, "GB/s": BYTES_GEMV / chain_us / 1e3,
+            "frac_hbm": BYTES_GEMV / chain_us / 1e3 / hbm,
+            "method": f"{GEMV_CHAIN_COPIES} calls back to back on distinct weight copies "
+                      f"({GEMV_CHAIN_COPIES * GN * GK / 1e6:.0f} MB, > 2x L2), "
+                      f"{'one CUDA graph' if chain_graph else 'eager launches'} replayed "
+                      f"{GEMV_CHAIN_REPS}x; events only around the replays"}
+    ops.update(extra_ops)
     achieved = OPS_LINEAR / us["linear"] / 1e6
     roofline = {"kernel": "tc_gemm_kernel (q8ta_linear 2048x4096x11008)", "bound": "tensor",
                 "achieved": achieved, "peak": bf16,
@@ -505,34 +661,40 @@ def run_ours(args, rank, world, local_rank):
                                  "kernels (two alternating device buffer sets); weights "
                                  "resident"}
     if rank == 0 and not args.no_cpu_baseline and args.only == "all":
-        t_cpu, cores, sample, parts = cpu_oracle_step_estimate(h)
-        result["cpu_baseline"] = {"value": OPS_STEP / t_cpu / 1e12, "unit": result["unit"],
-                                  "cores": cores, "kind": "oracle", "sample": sample,
-                                  "seconds_per_full_step": t_cpu,
-                                  "seconds_by_op": parts}
+        t_cpu, cores, sample, parts = oracle_scaled_step(h)
+        t_one, _, _, parts_one = oracle_scaled_step(h, threads=1)
+        result["cpu_baseline"] = {"value": OPS_STEP / ORACLE_SCALE / t_cpu / 1e12,
+                                  "unit": result["unit"], "cores": cores, "kind": "oracle",
+                                  "sample": sample, "seconds_per_sample": t_cpu,
+                                  "seconds_by_op": parts,
+                                  "single_thread": {
+                                      "value": OPS_STEP / ORACLE_SCALE / t_one / 1e12,
+                                      "cores": 1, "seconds_per_sample": t_one,
+                                      "seconds_by_op": parts_one}}
     return result
 
 
 def run_reference(args):
-    """The oracle as it stands, on the host cores, on bounded samples of the
-    same workload; each step is one bounded sample."""
+    """The oracle as it stands, on the host cores; each step is the full step
+    scaled down by ORACLE_SCALE in every op (see oracle_scaled_step)."""
     h = host_inputs()
     for _ in range(args.warmup):
-        cpu_oracle_step_estimate(h)
+        oracle_scaled_step(h)
     ts, last = [], None
     for _ in range(args.steps):
-        t, cores, sample, parts = cpu_oracle_step_estimate(h)
+        t, cores, sample, parts = oracle_scaled_step(h)
         ts.append(t)
         last = (cores, sample)
     t = statistics.median(ts)
-    v = OPS_STEP / t / 1e12
+    v = OPS_STEP / ORACLE_SCALE / t / 1e12
     unit = "int8 TOPS (2 x int8 MACs of linear + gemv + conv_t valid taps, per step)"
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic",
-            "config": {"workload": "q8ta hot path (same as the CUDA arm), CPU oracle on "
-                                   "bounded samples scaled to the full step"},
+            "config": {"workload": f"q8ta hot path (the CUDA arm's step) scaled by 1/{ORACLE_SCALE} "
+                                   "in every op; CPU oracle on all host cores",
+                       "step": "one step = 1/64 of the full step's work, timed whole"},
             "cpu_baseline": {"value": v, "unit": unit, "cores": last[0], "kind": "oracle",
                              "sample": last[1]},
             "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -548,6 +710,8 @@ def main():
                     default="all", help="run one op per step (for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-ops", action="store_true",
+                    help="skip the chained gemv and the two small workloads (for launch lists)")
     args = ap.parse_args()
     if args.warmup < 3 and args.only == "all":
         args.warmup = 3

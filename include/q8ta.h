@@ -37,7 +37,16 @@
  *     v = t + bias[n]; u = v * inv_output_scale;
  *     q = clamp(rint(u) + output_zero_point, -128, 127)        [linear]
  * - Scales must be finite and > 0; zero points must lie in [-128, 127]
- *   (they are zero points of int8 tensors); otherwise Q8_ERR_ARG.
+ *   (they are zero points of int8 tensors); otherwise Q8_ERR_ARG.  These
+ *   scalar checks are this library's own, not the pages': the pages state
+ *   no range for scales or zero points.  Below, each guard list says which
+ *   guards the pages state ("page") and which are this library's ("lib").
+ * - Per-device state: the device error word and the scratch array of
+ *   q8_linear_noalloc live in this library's device globals, whose device
+ *   addresses are looked up once per device and kept for the life of the
+ *   process.  Do not call the library across a cudaDeviceReset (or any
+ *   other destruction of the device's primary context): the kept addresses
+ *   would then be stale.
  */
 #ifndef Q8TA_H_
 #define Q8TA_H_
@@ -90,9 +99,9 @@ q8_status q8_device_error(uint32_t* code, int clear);
 /*
  * out[i] = clamp(rint(x[i] * inv_scale) + zero_point, -128, 127).
  * x: float32[numel]; out: int8[numel].
- * Guards (as on the page): x, out non-NULL; numel % 4 == 0 (the page's
- * packed-word binding); numel >= 0 (0 is a no-op, and then the pointers
- * may be NULL).
+ * Guards: page -- x, out non-NULL; numel % 4 == 0 (the page's packed-word
+ * binding; [quantize] Implementation).  lib -- numel >= 0 (0 is a no-op,
+ * and then the pointers may be NULL); the scale and zero-point ranges.
  */
 q8_status q8_quantize_per_tensor(const float* x, int64_t numel, double scale,
                                  int32_t zero_point, int8_t* out, q8_stream_t stream);
@@ -101,7 +110,8 @@ q8_status q8_quantize_per_tensor(const float* x, int64_t numel, double scale,
  * dequantize_per_tensor: int8 -> fp32, the op that closes the
  * quantize -> q8ta_* -> dequantize subgraph named in the Problem paragraphs
  * of [linear] and [conv_t].  out[i] = ((float)q[i] - (float)zero_point) *
- * (float)scale, one f32 rounding per step.  Same guards as quantize.
+ * (float)scale, one f32 rounding per step.  Same guards as quantize (the
+ * pages print no guard for this op; numel % 4 mirrors quantize's).
  */
 q8_status q8_dequantize_per_tensor(const int8_t* q, int64_t numel, double scale,
                                    int32_t zero_point, float* out, q8_stream_t stream);
@@ -124,8 +134,12 @@ q8_status q8_dequantize_per_tensor(const int8_t* q, int64_t numel, double scale,
  *                 requantization, i.e. out = max(out, output_zero_point));
  *                 anything else gives Q8_ERR_UNSUPPORTED
  *   out           int8 [M, N] row-major
- * Guards (as on the page): N % 4 == 0, (M*K) % 4 == 0, (N*K) % 4 == 0,
- * M, N, K >= 1.
+ * Guards: page ([linear] Implementation) -- N % 4 == 0, (M*K) % 4 == 0,
+ * (N*K) % 4 == 0, activation "none" (the page's fail-loud follow-up "relu"
+ * is supported here instead of refused), and for q8_linear_gemv M == 1.
+ * lib -- M, N, K >= 1; M, N <= INT32_MAX and K <= INT32_MAX / 2 (32-bit
+ * tile coordinates); no product of two sizes overflows int64; the scale
+ * and zero-point ranges.
  *
  * The contraction runs on the tcgen05 tensor cores with bf16 operands that
  * hold the int8 values exactly; workspace holds the bf16 operand copies:
@@ -267,10 +281,12 @@ typedef struct q8_conv2d_transposed_shape {
  * read).  For groups == 1 the weight layout is the page's reshape
  * weight[oc, (kh*Kw+kw)*IC + ic] = original[ic, oc, kh, kw]; group j of a
  * grouped weight holds original[j*ICg + icl, oc - j*OC/groups, kh, kw].
- * Guards: the page's stride >= 1, W_out % 4 == 0 and weight_row_stride >=
- * Kh*Kw*IC/groups; activation "none" or "relu"; groups dividing IC and OC,
- * dilation >= 1 (the page's fail-loud follow-ups, supported here); every
- * size >= 1 and pad >= 0.  weight_sums is accepted and ignored.
+ * Guards: page ([conv_t] Implementation) -- stride >= 1, W_out % 4 == 0,
+ * weight_row_stride >= Kh*Kw*IC/groups, activation "none"; the page's
+ * fail-loud follow-ups (activation "relu", groups != 1, dilation != 1) are
+ * supported here: activation "none" or "relu", groups dividing IC and OC,
+ * dilation >= 1.  lib -- every size >= 1, pad >= 0, the scale and
+ * zero-point ranges.  weight_sums is accepted and ignored.
  * workspace: q8_conv2d_transposed_workspace_bytes(shape) bytes, 256-byte
  * aligned (an NHWC bf16 copy of x - input_zero_point, channels padded per
  * group to a multiple of 64, then the packed weight); the size functions
@@ -356,7 +372,8 @@ typedef struct q8_conv2d_shape {
  * H_out and W_out are the caller's (normally (H_in + 2*pad_h -
  * dilation_h*(Kh-1) - 1) / stride_h + 1); outputs whose window lies wholly
  * in the padding hold the requantized bias.
- * Guards: as q8_conv2d_transposed, with stride_h, stride_w <= 8
+ * Guards: as q8_conv2d_transposed (the pages name this op but print no
+ * guard of its own), plus lib -- stride_h, stride_w <= 8
  * (Q8_ERR_UNSUPPORTED above: the input is read through TMA boxes with
  * element strides).  Workspace and packed forms as for the transposed op.
  */

@@ -170,6 +170,15 @@ cudaError_t launch_dequantize(const int8_t* q, int64_t numel, float scale, float
 // 2^32 like the accumulator itself.
 // One warp per output row; each lane keeps UNR 16-byte weight loads in
 // flight; a block's 4 warps produce 4 consecutive outputs = one 32-bit word.
+//
+// Before waiting for the previous kernel on the stream, the block asks for
+// its whole weight slab (4 rows, contiguous) to be brought into L2 with one
+// bulk prefetch, and lets the next kernel's blocks be scheduled.  Weights
+// are what the gemv streams; a prefetch into L2 can never hand stale data
+// to the loads that follow the wait, because L2 is where the GPU's memory is
+// coherent (a write by the previous kernel updates the line there).  In a
+// run of gemvs (one per layer of a decode step) this makes each call's
+// weight stream from HBM while the previous call is still running.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void dp4a_acc(uint32_t w, uint32_t x, int& dot, int& wsum) {
   dot = __dp4a(static_cast<int>(w), static_cast<int>(x), dot);
@@ -185,17 +194,23 @@ __global__ void __launch_bounds__(128) gemv_kernel(const int8_t* __restrict__ x,
   __shared__ int8_t res[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 4 + warp;
-  // The weight row is requested into L2 before waiting for the previous
-  // kernel: L2 is where the GPU's memory is coherent, so a prefetch can never
-  // return stale data to the loads below, and the row's DRAM latency overlaps
-  // the previous kernel's tail.
-  if (n < N) {
+  if constexpr (VEC == 16) {
+    // the block's rows n0 .. n0 + 3 are one contiguous, 16-byte aligned run
+    // (K % 16 == 0): one bulk prefetch of at most 4 * K bytes
+    if (threadIdx.x == 0) {
+      const int n0 = blockIdx.x * 4;
+      const uint32_t bytes = static_cast<uint32_t>(min(4, N - n0)) * static_cast<uint32_t>(K);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(w + static_cast<int64_t>(n0) * K),
+                   "r"(bytes)
+                   : "memory");
+    }
+  } else if (n < N) {
     const int8_t* wr = w + static_cast<int64_t>(n) * K;
     for (int off = lane * 128; off < K; off += 32 * 128)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(wr + off));
   }
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   int dot = 0, wsum = 0;
   if (n < N) {
     const int8_t* wr = w + static_cast<int64_t>(n) * K;

@@ -5,10 +5,11 @@ whose host runtime owns the device memory pool, a latency-critical loop that
 cannot afford cudaMalloc/cudaFree, a deployment with a memory budget fixed at
 start-up).  q8_linear_noalloc serves them from a fixed library-owned scratch
 array.  This test calls it through the C ABI and checks its output against
-q8_linear's (with a caller workspace) on two calls in a row with different
-inputs, so a second call that saw the first call's leftover scratch contents
-would show up; it also checks that an over-size problem is refused before
-anything is launched.  It sits in a file of its own that pytest collects
+q8_linear's (with a caller workspace) and against the CPU oracle on two
+calls in a row with different inputs, so a second call that saw the first
+call's leftover scratch contents would show up; it also checks that an
+over-size problem is refused before anything is launched (real device
+buffers, output left untouched).  It sits in a file of its own that pytest collects
 last, and it builds the library if needed, so it also runs alone in a fresh
 process.
 """
@@ -18,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -41,6 +43,12 @@ def _case(seed, M, K, N, izp):
     return T(x), T(w), T(ws), T(b), izp
 
 
+def _oracle(x, w, ws, b, izp, act="none"):
+    c = lambda t: t.cpu().numpy()  # noqa: E731
+    return torch.from_numpy(oracle.linear(c(x), 0.03, izp, c(w), c(ws), c(b), 0.1, 1,
+                                          activation=act)).to(DEV)
+
+
 def _noalloc(x, w, ws, b, izp, out, act=b"none"):
     M, K = x.shape
     N = w.shape[0]
@@ -60,22 +68,26 @@ def test_noalloc_matches_q8_linear_on_two_calls():
         ref = q8.linear(x, 0.03, izp, w, None, ws, b, 0.1, 1)
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
+        assert torch.equal(out, _oracle(x, w, ws, b, izp))
     # the relu activation through the same scratch
     out = torch.empty((M, N), dtype=torch.int8, device=DEV)
     assert _noalloc(x, w, ws, b, izp, out, b"relu") == q8.Q8_OK
     ref = q8.linear(x, 0.03, izp, w, None, ws, b, 0.1, 1, activation="relu")
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+    assert torch.equal(out, _oracle(x, w, ws, b, izp, "relu"))
     assert q8.device_error(clear=True) == 0
 
 
 def test_noalloc_refuses_oversize_and_serves_gemv():
-    # 2 * (M + N) * K bf16 bytes = 2 * (2048 + 4096) * 4096 > 16 MiB: refused, nothing launched
-    big = q8.lib().q8_linear_noalloc(ctypes.c_void_p(0x10000), 2048, 4096, 0.03, 0,
-                                     ctypes.c_void_p(0x10000), 4096, None,
-                                     ctypes.c_void_p(0x10000), None, 0.1, 0, b"none",
-                                     ctypes.c_void_p(0x10000), None)
-    assert big == q8.Q8_ERR_WORKSPACE
+    # 2 * (M + N) * ceil64(K) bf16 bytes = 2 * 2048 * 4160 > 16 MiB while the
+    # int8 inputs hold only 8.5 MB: refused before any launch, out untouched
+    M, K, N = 1024, 4160, 1024
+    x, w, ws, b, izp = _case(4, M, K, N, 0)
+    out = torch.full((M, N), 55, dtype=torch.int8, device=DEV)
+    assert _noalloc(x, w, ws, b, izp, out) == q8.Q8_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((out == 55).all())
     # M == 1 needs no scratch
     x, w, ws, b, izp = _case(3, 1, 4096, 1024, 0)
     out = torch.empty((1, 1024), dtype=torch.int8, device=DEV)
@@ -83,3 +95,5 @@ def test_noalloc_refuses_oversize_and_serves_gemv():
     ref = q8.linear_gemv(x, 0.03, izp, w, None, ws, b, 0.1, 1)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+    assert torch.equal(out, _oracle(x, w, ws, b, izp))
+    assert q8.device_error(clear=True) == 0
