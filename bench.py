@@ -3,10 +3,11 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
   1. quantize_per_tensor        fp32 [64Mi] -> int8                (HBM bound)
-  2. quantize -> linear operand fp32 [2048, 4096] -> int8 x_q + bf16 operand
-  3. q8ta_linear GEMM           2048 x 4096 x 11008, packed weight (tensor cores)
-  4. q8ta_linear_gemv           1 x 4096 x 4096                    (HBM bound)
-  5. q8ta_conv2d_transposed     [8,256,64,64] -> [8,128,128,128], K=3 s=2 p=1 op=1
+  2. quantize -> q8ta_linear   fp32 [2048, 4096] -> int8 x_q, then the GEMM
+                                2048 x 4096 x 11008 with a packed weight, in ONE
+                                kernel (the GEMM's warps quantize x; tensor cores)
+  3. q8ta_linear_gemv           1 x 4096 x 4096                    (HBM bound)
+  4. q8ta_conv2d_transposed     [8,256,64,64] -> [8,128,128,128], K=3 s=2 p=1 op=1
 
 value = int8 TOPS of the step: (2*M*N*K of the linear + 2*K*N of the gemv +
 2 * valid-tap MACs of the transposed convolution) / step time.  Per-op
@@ -73,7 +74,6 @@ CONV_OUTPUTS = CD["N"] * CD["OC"] * CHo * CWo
 # algorithmic bytes (each input read once, each output written once)
 BYTES_QUANT = QN * (4 + 1)
 BYTES_GEMV = GN * GK + GK + GN + 2 * GN * 4
-BYTES_CHAIN_PREP = LM * LK * (4 + 1 + 2)
 
 
 def measured_peaks():
@@ -193,30 +193,28 @@ class Path:
             dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
+    LAUNCHES = {"quantize": 1, "linear": 1, "gemv": 1, "conv_t": 2}
+
     def launches_per_step(self):
-        n = {"quantize": 1, "chain_prep": 1, "linear": 1, "gemv": 1, "conv_t": 2}
         if self.only == "all":
-            return sum(n.values())
-        return {"quantize": 1, "linear": 2, "gemv": 1, "conv_t": 2}[self.only]
+            return sum(self.LAUNCHES.values())
+        return self.LAUNCHES[self.only]
 
     # the four ops of a step, their activation inputs and outputs (attribute names)
     OPS = ("quantize", "linear", "gemv", "conv_t")
     INPUTS = {"quantize": "xq", "linear": "lx", "gemv": "gx", "conv_t": "cx"}
     OUTPUTS = {"quantize": "q_out", "linear": "l_out", "gemv": "g_out", "conv_t": "c_out"}
 
-    def run_op(self, name, rec=None):
+    def run_op(self, name):
         """Enqueue one op on the current stream (the linear op is the fused
-        quantize -> operand launch and the GEMM; rec(i) marks between them)."""
+        quantize -> q8ta_linear kernel)."""
         q8, qp, lp, gp, cp = self.q8, Q.params, L.params, G.params, C.params
         if name == "quantize":
             q8.quantize_per_tensor(self.xq, qp["in_scale"], qp["in_zp"], out=self.q_out)
         elif name == "linear":
-            q8.quantize_to_operand(self.lx, lp["in_scale"], lp["in_zp"], x_q=self.l_xq,
-                                   operand=self.operand)
-            if rec:
-                rec()
-            q8.linear_operand_packed(self.operand, lp["in_scale"], self.packed, self.lws, self.lb,
-                                     lp["out_scale"], lp["out_zp"], out=self.l_out)
+            q8.quantize_linear_fused(self.lx, lp["in_scale"], lp["in_zp"], self.packed, self.lws,
+                                     self.lb, lp["out_scale"], lp["out_zp"], x_q=self.l_xq,
+                                     out=self.l_out, operand=self.operand)
         elif name == "gemv":
             q8.linear_gemv(self.gx, gp["in_scale"], gp["in_zp"], self.gw, None, self.gws, self.gb,
                            gp["out_scale"], gp["out_zp"], out=self.g_out)
@@ -228,23 +226,13 @@ class Path:
                                         workspace=self.c_ws)
 
     def step(self, ev=None):
-        """Enqueue one step; ev (list of 6 CUDA events) brackets each op."""
+        """Enqueue one step; ev (a list of len(OPS) + 1 CUDA events) brackets each op."""
         rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
-        rec(0)
-        if self.only in ("all", "quantize"):
-            self.run_op("quantize")
-        rec(1)
-        if self.only in ("all", "linear"):
-            self.run_op("linear", rec=lambda: rec(2))
-        else:
-            rec(2)
-        rec(3)
-        if self.only in ("all", "gemv"):
-            self.run_op("gemv")
-        rec(4)
-        if self.only in ("all", "conv_t"):
-            self.run_op("conv_t")
-        rec(5)
+        for i, op in enumerate(self.OPS):
+            rec(i)
+            if self.only in ("all", op):
+                self.run_op(op)
+        rec(len(self.OPS))
 
 
 GEMV_CHAIN_COPIES = 24   # 24 x 16.8 MB of weights: 403 MB, more than 3x the 129 MB L2
@@ -318,6 +306,34 @@ def small_op_latency(fn, reps=60, warm=10):
     return statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
 
 
+def graph_per_call_us(fn, calls=32, reps=20):
+    """Device microseconds per call of fn() with the host out of the way:
+    `calls` calls captured in one CUDA graph, replayed `reps` times."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(calls):
+                fn()
+    except RuntimeError:
+        torch.cuda.synchronize()
+        return None
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (calls * reps)
+
+
 def small_configs_measure(dev):
     """The two latency-bound workloads: quantize -> q8ta_linear 8x64x32 and
     the 1x64x32x32 -> 1x32x64x64 transposed convolution (packed weights,
@@ -335,9 +351,8 @@ def small_configs_measure(dev):
     out0 = torch.empty((d0["M"], d0["N"]), dtype=torch.int8, device=dev)
 
     def cfg0():
-        q8.quantize_to_operand(x, p0["in_scale"], p0["in_zp"], x_q=xq, operand=operand)
-        q8.linear_operand_packed(operand, p0["in_scale"], packed, ws, b, p0["out_scale"],
-                                 p0["out_zp"], out=out0)
+        q8.quantize_linear_fused(x, p0["in_scale"], p0["in_zp"], packed, ws, b, p0["out_scale"],
+                                 p0["out_zp"], x_q=xq, out=out0, operand=operand)
 
     w3 = synth.CONFIGS["conv_t_1x64x32x32_k4s2"]
     d3, p3 = w3.dims, w3.params
@@ -359,19 +374,23 @@ def small_configs_measure(dev):
                                     padding=d3["p"], output_padding=d3["op"], out=out3,
                                     workspace=cws_buf)
 
-    us0 = small_op_latency(cfg0)
-    us3 = small_op_latency(cfg3)
+    us0, g0 = small_op_latency(cfg0), graph_per_call_us(cfg0)
+    us3, g3 = small_op_latency(cfg3), graph_per_call_us(cfg3)
     macs3 = conv_valid_macs(d3, Ho, Wo)
+    how = ("us: median of 60 calls after 10, each bracketed by CUDA events (host launch cost "
+           "and gaps included); us_graph: 32 calls captured in one CUDA graph, replayed 20x, "
+           "device time per call")
     return {
         "linear_chain_8x64x32": {
-            "us": us0, "launches": 2, "TOPS": 2 * d0["M"] * d0["N"] * d0["K"] / us0 / 1e6,
-            "method": "median of 60 calls after 10, each bracketed by CUDA events "
-                      "(quantize->operand launch + GEMM launch; launch gaps included)"},
+            "us": us0, "us_graph": g0, "launches": 1,
+            "TOPS": 2 * d0["M"] * d0["N"] * d0["K"] / us0 / 1e6,
+            "method": "fused quantize -> q8ta_linear kernel; " + how},
         "q8ta_conv2d_transposed_1x64x32x32": {
-            "us": us3, "launches": 2, "outputs/s": d3["N"] * d3["OC"] * Ho * Wo / us3 * 1e6,
+            "us": us3, "us_graph": g3, "launches": 2,
+            "outputs/s": d3["N"] * d3["OC"] * Ho * Wo / us3 * 1e6,
+            "outputs/s_graph": d3["N"] * d3["OC"] * Ho * Wo / g3 * 1e6 if g3 else None,
             "TOPS_valid_taps": 2 * macs3 / us3 / 1e6,
-            "method": "median of 60 calls after 10, each bracketed by CUDA events "
-                      "(input relayout + GEMM; packed weight)"},
+            "method": "input relayout + GEMM, packed weight; " + how},
     }
 
 
@@ -505,7 +524,7 @@ def oracle_scaled_step(h, threads=None, scale=ORACLE_SCALE):
     return total, threads, sample, parts
 
 
-def traffic_from_profile(key="tc_gemm_linear_2048x4096x11008"):
+def traffic_from_profile(key):
     """DRAM read+write bytes per launch of a GEMM from the committed ncu
     summary (profiles/traffic.json), valid only while the kernel's source
     files are unchanged since the capture; otherwise None."""
@@ -572,7 +591,8 @@ def run_ours(args, rank, world, local_rank):
     # Per-op times come from a second pass with an event between ops (an
     # event on the stream also stops one kernel from starting under the
     # previous one's tail, so these times include each op's own ramp).
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(Path.OPS) + 1)]
+           for _ in range(K)]
     for k in range(K):
         path.step(evs[k])
     torch.cuda.synchronize()
@@ -590,7 +610,7 @@ def run_ours(args, rank, world, local_rank):
     if args.only == "all" and not args.no_extra_ops:
         extra_ops = small_configs_measure(dev)
 
-    names = ["quantize", "chain_prep", "linear", "gemv", "conv_t"]
+    names = list(Path.OPS)
     per = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
            for i, n in enumerate(names)}
     hbm, bf16, peak_src = measured_peaks()
@@ -599,11 +619,11 @@ def run_ours(args, rank, world, local_rank):
     ops = {
         "quantize_64Mi": {"us": us["quantize"], "GB/s": BYTES_QUANT / us["quantize"] / 1e3,
                           "frac_hbm": BYTES_QUANT / us["quantize"] / 1e3 / hbm},
-        "chain_quantize_to_operand_2048x4096": {
-            "us": us["chain_prep"], "GB/s": BYTES_CHAIN_PREP / us["chain_prep"] / 1e3},
-        "q8ta_linear_2048x4096x11008": {"us": us["linear"],
-                                        "TOPS": OPS_LINEAR / us["linear"] / 1e6,
-                                        "frac_bf16_peak": OPS_LINEAR / us["linear"] / 1e6 / bf16},
+        "quantize_q8ta_linear_2048x4096x11008": {
+            "us": us["linear"], "TOPS": OPS_LINEAR / us["linear"] / 1e6,
+            "frac_bf16_peak": OPS_LINEAR / us["linear"] / 1e6 / bf16,
+            "note": "one kernel: quantize of the fp32 activations (writing x_q) fused with the "
+                    "GEMM; TOPS counts the GEMM's 2*M*N*K only"},
         "q8ta_linear_gemv_1x4096x4096": {
             "us": us["gemv"], "GB/s": BYTES_GEMV / us["gemv"] / 1e3,
             "frac_hbm": BYTES_GEMV / us["gemv"] / 1e3 / hbm,
@@ -623,11 +643,12 @@ def run_ours(args, rank, world, local_rank):
                       f"{GEMV_CHAIN_REPS}x; events only around the replays"}
     ops.update(extra_ops)
     achieved = OPS_LINEAR / us["linear"] / 1e6
-    roofline = {"kernel": "tc_gemm_kernel (q8ta_linear 2048x4096x11008)", "bound": "tensor",
+    roofline = {"kernel": "tc_gemm_kernel<240,12,7,2,2> (quantize -> q8ta_linear 2048x4096x11008, "
+                          "fused)", "bound": "tensor",
                 "achieved": achieved, "peak": bf16,
                 "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)",
                 "unit": "TFLOP/s", "frac": achieved / bf16,
-                "traffic": traffic_from_profile(),
+                "traffic": traffic_from_profile("tc_gemm_fused_linear_2048x4096x11008"),
                 "algorithmic_flops_per_launch": OPS_LINEAR}
 
     result = {

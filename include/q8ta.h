@@ -86,7 +86,9 @@ int q8_version(void);
  * issuing work and return, leaving the CUDA context usable (codes 0x101 ..
  * 0x106: which wait ran out).  Code 0x107: a convolution launched from a
  * packed weight whose buffer was rewritten after packing (the host's copy of
- * its k-block bound no longer held); that launch wrote nothing.  This call
+ * its k-block bound no longer held); that launch wrote nothing.  Codes
+ * 0x108 / 0x109: q8_quantize_linear_fused waited too long for an operand
+ * chunk / met an operand trailer that q8_linear_operand_init never prepared.  This call
  * synchronizes the current device, copies the word to *code (host pointer)
  * and, if clear != 0, resets it to 0.  Q8_OK is returned when the copy
  * succeeded, whatever the word holds.
@@ -246,11 +248,55 @@ q8_status q8_quantize_linear_packed(const float* x_f32, int64_t M, int64_t K, do
                                     const char* activation, int8_t* x_q, int8_t* out,
                                     void* workspace, size_t workspace_bytes, q8_stream_t stream);
 
+/*
+ * Fused quantize -> q8ta_linear in ONE kernel (the pages' delegated
+ * quantize_per_tensor -> q8ta_linear subgraph, [linear] Problem paragraph):
+ * the GEMM's own warps quantize fp32 x [M, K] exactly as
+ * q8_quantize_per_tensor does (input_scale, input_zero_point), write x_q
+ * (int8 [M, K], may be NULL) and the bf16 operand into `operand`, chunk by
+ * chunk along K, and the tensor cores start on each chunk as soon as every
+ * CTA has written its share of it.  Results equal q8_quantize_linear_packed.
+ *   operand: q8_linear_operand_bytes(M, K) bytes, 256-byte aligned, whose
+ *     trailer q8_linear_operand_init prepared once (before the first fused
+ *     call on it; each call leaves it ready for the next).  A buffer that
+ *     was never initialized runs nothing and sets device error 0x109.
+ *   Calls sharing an operand buffer must be ordered on one stream.
+ * The kernel's CTAs wait on one another (bounded, device error 0x108 on
+ * expiry): its persistent grid is sized to fit the GPU at once, so do not
+ * run other long-lived kernels concurrently on the same GPU.
+ * Guards: those of q8_quantize_linear_packed.
+ */
+q8_status q8_linear_operand_init(void* operand, int64_t M, int64_t K, size_t operand_bytes,
+                                 q8_stream_t stream);
+q8_status q8_quantize_linear_fused(const float* x_f32, int64_t M, int64_t K, double input_scale,
+                                   int32_t input_zero_point, const void* packed_weight, int64_t N,
+                                   const float* weight_scales, const float* bias,
+                                   double output_scale, int32_t output_zero_point,
+                                   const char* activation, int8_t* x_q, int8_t* out,
+                                   void* operand, size_t operand_bytes, q8_stream_t stream);
+
 /* Test and debugging form of q8_linear_packed: writes the exact int32
  * accumulators acc[m,n] (int32 [M, N]) instead of the int8 output. */
 q8_status q8_linear_packed_acc32(const int8_t* x, int64_t M, int64_t K, int32_t input_zero_point,
                                  const void* packed_weight, int64_t N, int32_t* acc,
                                  void* workspace, size_t workspace_bytes, q8_stream_t stream);
+
+/*
+ * Failure-detection test hook (no counterpart on the pages).  Runs
+ * q8_linear_packed_acc32 with every pipeline-barrier wait limited to
+ * wait_limit_ns (1 ms .. 1 s; else Q8_ERR_ARG) and with the kernel's TMA
+ * producer leaving out its skip_fill-th ring fill (0-based), so that the
+ * matching wait runs out.  The kernel then records a code in the device
+ * error word (0x101 .. 0x106, q8_device_error), stops, waits (bounded) for
+ * its own copies and tensor-core work in flight, frees its tensor memory
+ * and returns: nothing hangs and the CUDA context stays usable.  acc is
+ * left partly written.  For tests only.
+ */
+q8_status q8_debug_linear_packed_stall(const int8_t* x, int64_t M, int64_t K,
+                                       int32_t input_zero_point, const void* packed_weight,
+                                       int64_t N, int32_t* acc, void* workspace,
+                                       size_t workspace_bytes, uint64_t wait_limit_ns,
+                                       int64_t skip_fill, q8_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* q8ta_conv2d_transposed                                            [conv_t] */

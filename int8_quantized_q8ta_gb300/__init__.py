@@ -32,7 +32,8 @@ EXPORTS = (
     "q8_linear_packed_weight_bytes", "q8_linear_pack_weight",
     "q8_linear_operand_bytes", "q8_linear_prepare_operand", "q8_quantize_to_linear_operand",
     "q8_linear_operand_packed", "q8_linear_packed", "q8_quantize_linear_packed",
-    "q8_linear_packed_acc32",
+    "q8_linear_operand_init", "q8_quantize_linear_fused",
+    "q8_linear_packed_acc32", "q8_debug_linear_packed_stall",
     "q8_conv2d_transposed_workspace_bytes", "q8_conv2d_transposed",
     "q8_conv2d_transposed_acc32", "q8_conv2d_transposed_packed_weight_bytes",
     "q8_conv2d_transposed_packed_workspace_bytes", "q8_conv2d_transposed_pack_weight",
@@ -99,6 +100,11 @@ def _load() -> ctypes.CDLL:
         "q8_quantize_linear_packed": (ctypes.c_int, [P, I64, I64, D, I32, P, I64, P, P, D, I32, C,
                                                      P, P, P, S, P]),
         "q8_linear_packed_acc32": (ctypes.c_int, [P, I64, I64, I32, P, I64, P, P, S, P]),
+        "q8_linear_operand_init": (ctypes.c_int, [P, I64, I64, S, P]),
+        "q8_quantize_linear_fused": (ctypes.c_int, [P, I64, I64, D, I32, P, I64, P, P, D, I32, C,
+                                                    P, P, P, S, P]),
+        "q8_debug_linear_packed_stall": (ctypes.c_int, [P, I64, I64, I32, P, I64, P, P, S,
+                                                        ctypes.c_uint64, I64, P]),
         "q8_conv2d_transposed_workspace_bytes": (S, [SP]),
         "q8_conv2d_transposed": (ctypes.c_int, [P, SP, D, I32, P, P, P, P, D, I32, C, P, P, S, P]),
         "q8_conv2d_transposed_acc32": (ctypes.c_int, [P, SP, I32, P, P, P, S, P]),
@@ -335,8 +341,43 @@ class Operand:
 
 
 def operand_buffer(M: int, K: int, device) -> Operand:
-    return Operand(torch.empty(_lib.q8_linear_operand_bytes(M, K), dtype=torch.uint8,
-                               device=device), M, K)
+    """An operand buffer for M x K activations, its trailer prepared for the
+    fused quantize -> linear kernel as well (q8_linear_operand_init)."""
+    data = torch.empty(_lib.q8_linear_operand_bytes(M, K), dtype=torch.uint8, device=device)
+    _check(_lib.q8_linear_operand_init(_ptr(data), M, K, data.numel(), _stream(data)),
+           "q8_linear_operand_init")
+    return Operand(data, M, K)
+
+
+def quantize_linear_fused(x_f32, input_scale, input_zero_point, packed: PackedWeight,
+                          weight_scales, bias, output_scale, output_zero_point, activation="none",
+                          x_q=None, out=None, operand: Optional[Operand] = None,
+                          want_x_q: bool = True):
+    """fp32 x -> quantize_per_tensor -> q8ta_linear in one kernel (the GEMM's
+    warps quantize x into the operand, chunk by chunk along K).  Returns
+    (x_q, out, operand); pass the operand back in to reuse it."""
+    _need(x_f32, torch.float32, "x_f32")
+    _need(weight_scales, torch.float32, "weight_scales")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    M, K = x_f32.shape
+    if K != packed.K:
+        raise ValueError(f"x has K={K}, packed weight has K={packed.K}")
+    if x_q is None and want_x_q:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=x_f32.device)
+    if x_q is not None:
+        _need(x_q, torch.int8, "x_q")
+    out = torch.empty((M, packed.N), dtype=torch.int8, device=x_f32.device) if out is None else out
+    _need(out, torch.int8, "out")
+    operand = operand_buffer(M, K, x_f32.device) if operand is None else operand
+    if (operand.M, operand.K) != (M, K):
+        raise ValueError(f"operand is for {operand.M}x{operand.K}, x is {M}x{K}")
+    _check(_lib.q8_quantize_linear_fused(
+        _ptr(x_f32), M, K, float(input_scale), int(input_zero_point), _ptr(packed.data), packed.N,
+        _ptr(weight_scales), _ptr(bias), float(output_scale), int(output_zero_point),
+        activation.encode(), _ptr(x_q), _ptr(out), _ptr(operand.data), operand.data.numel(),
+        _stream(x_f32)), "q8_quantize_linear_fused")
+    return x_q, out, operand
 
 
 def prepare_operand(x, input_zero_point, operand: Optional[Operand] = None) -> Operand:
@@ -394,6 +435,25 @@ def linear_packed_acc32(x, input_zero_point, packed: PackedWeight, out=None, wor
     _check(_lib.q8_linear_packed_acc32(_ptr(x), M, K, int(input_zero_point), _ptr(packed.data),
                                        packed.N, _ptr(out), _ptr(ws), nbytes, _stream(x)),
            "q8_linear_packed_acc32")
+    return out
+
+
+def debug_linear_packed_stall(x, input_zero_point, packed: PackedWeight, wait_limit_ns,
+                              skip_fill, out=None, workspace=None):
+    """Failure-detection test: linear_packed_acc32 with a short barrier-wait
+    limit and one TMA ring fill left out, so a bounded wait runs out (the
+    device error word then holds its code).  Returns the (partly written)
+    accumulator tensor."""
+    _need(x, torch.int8, "x")
+    M, K = x.shape
+    out = torch.zeros((M, packed.N), dtype=torch.int32, device=x.device) if out is None else out
+    _need(out, torch.int32, "out")
+    nbytes = _lib.q8_linear_operand_bytes(M, K)
+    ws = _workspace(nbytes, x.device, workspace)
+    _check(_lib.q8_debug_linear_packed_stall(_ptr(x), M, K, int(input_zero_point),
+                                             _ptr(packed.data), packed.N, _ptr(out), _ptr(ws),
+                                             nbytes, int(wait_limit_ns), int(skip_fill),
+                                             _stream(x)), "q8_debug_linear_packed_stall")
     return out
 
 

@@ -230,7 +230,8 @@ q8_status q8_quantize_to_linear_operand(const float* x_f32, int64_t M, int64_t K
 static q8_status run_operand_packed(const void* operand, int64_t M, int64_t K, double input_scale,
                                     const void* packed, int64_t N, const float* ws,
                                     const float* bias, double output_scale, int32_t ozp,
-                                    int relu, int8_t* out, int32_t* acc_out, q8_stream_t stream) {
+                                    int relu, int8_t* out, int32_t* acc_out, q8_stream_t stream,
+                                    uint64_t wait_ns = 0, int stall_fill = 0) {
   if (reinterpret_cast<uintptr_t>(packed) % q8::kWorkspaceAlign != 0 ||
       reinterpret_cast<uintptr_t>(operand) % q8::kWorkspaceAlign != 0)
     return Q8_ERR_ALIGN;
@@ -248,6 +249,8 @@ static q8_status run_operand_packed(const void* operand, int64_t M, int64_t K, d
   L.a_bound_dev = operand_bound_word(const_cast<void*>(operand), M, K);
   L.a_bound_host = 255;
   L.w_bound_dev = operand_bound_word(const_cast<void*>(packed), N, K);
+  L.wait_ns = wait_ns;
+  L.stall_fill = stall_fill;
   return cuda_status(q8::launch_tc_linear(L, cs(stream)));
 }
 
@@ -303,6 +306,51 @@ q8_status q8_quantize_linear_packed(const float* x_f32, int64_t M, int64_t K, do
                             output_scale, output_zero_point, relu, out, nullptr, stream);
 }
 
+q8_status q8_linear_operand_init(void* operand, int64_t M, int64_t K, size_t operand_bytes,
+                                 q8_stream_t stream) {
+  if (M < 1 || K < 1 || !mul_ok(M, K) || M > INT32_MAX || K > INT32_MAX / 2) return Q8_ERR_SHAPE;
+  q8_status st = check_operand(operand, operand_bytes, M, K);
+  if (st != Q8_OK) return st;
+  return cuda_status(q8::launch_fused_trailer_init(
+      reinterpret_cast<uint32_t*>(operand_bound_word(operand, M, K)), cs(stream)));
+}
+
+q8_status q8_quantize_linear_fused(const float* x_f32, int64_t M, int64_t K, double input_scale,
+                                   int32_t input_zero_point, const void* packed_weight, int64_t N,
+                                   const float* weight_scales, const float* bias,
+                                   double output_scale, int32_t output_zero_point,
+                                   const char* activation, int8_t* x_q, int8_t* out,
+                                   void* operand, size_t operand_bytes, q8_stream_t stream) {
+  if (!x_f32) return Q8_ERR_NULL;
+  int relu = 0;
+  q8_status st = check_linear(reinterpret_cast<const int8_t*>(x_f32), M, K, input_scale,
+                              input_zero_point, packed_weight, N, weight_scales, output_scale,
+                              output_zero_point, activation, out, &relu);
+  if (st != Q8_OK) return st;
+  st = check_operand(operand, operand_bytes, M, K);
+  if (st != Q8_OK) return st;
+  if (reinterpret_cast<uintptr_t>(packed_weight) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
+  q8::TcLinear L{};
+  L.a = static_cast<const __nv_bfloat16*>(operand);
+  L.b = static_cast<const __nv_bfloat16*>(packed_weight);
+  L.M = M;
+  L.N = N;
+  L.Kp = round_up(K, kTileK);
+  L.ws = weight_scales;
+  L.bias = bias;
+  L.rq = make_rq(input_scale, output_scale, output_zero_point, relu);
+  L.out = out;
+  L.a_bound_host = a_bound_of(input_zero_point);
+  L.w_bound_dev = operand_bound_word(const_cast<void*>(packed_weight), N, K);
+  L.qx = x_f32;
+  L.qxq = x_q;
+  L.qinv = recip_f32(input_scale);
+  L.qzp = input_zero_point;
+  L.qK = K;
+  L.qsync = reinterpret_cast<uint32_t*>(operand_bound_word(operand, M, K));
+  return cuda_status(q8::launch_tc_linear(L, cs(stream)));
+}
+
 q8_status q8_linear_packed_acc32(const int8_t* x, int64_t M, int64_t K, int32_t input_zero_point,
                                  const void* packed_weight, int64_t N, int32_t* acc,
                                  void* workspace, size_t workspace_bytes, q8_stream_t stream) {
@@ -314,6 +362,25 @@ q8_status q8_linear_packed_acc32(const int8_t* x, int64_t M, int64_t K, int32_t 
   if (st != Q8_OK) return st;
   return run_operand_packed(workspace, M, K, 1.0, packed_weight, N, nullptr, nullptr, 1.0, 0, 0,
                             nullptr, acc, stream);
+}
+
+// Failure-detection test: q8_linear_packed_acc32 with a short barrier-wait
+// limit and one TMA ring fill left out, so the kernel's bounded wait runs out.
+q8_status q8_debug_linear_packed_stall(const int8_t* x, int64_t M, int64_t K,
+                                       int32_t input_zero_point, const void* packed_weight,
+                                       int64_t N, int32_t* acc, void* workspace,
+                                       size_t workspace_bytes, uint64_t wait_limit_ns,
+                                       int64_t skip_fill, q8_stream_t stream) {
+  static const float kOne = 1.0f;
+  q8_status st = check_linear(x, M, K, 1.0, input_zero_point, packed_weight, N, &kOne, 1.0, 0,
+                              "none", acc);
+  if (st != Q8_OK) return st;
+  if (wait_limit_ns < 1000000ull || wait_limit_ns > 1000000000ull) return Q8_ERR_ARG;
+  if (skip_fill < 0 || skip_fill >= (int64_t{1} << 30)) return Q8_ERR_ARG;
+  st = q8_linear_prepare_operand(x, M, K, input_zero_point, workspace, workspace_bytes, stream);
+  if (st != Q8_OK) return st;
+  return run_operand_packed(workspace, M, K, 1.0, packed_weight, N, nullptr, nullptr, 1.0, 0, 0,
+                            nullptr, acc, stream, wait_limit_ns, static_cast<int>(skip_fill) + 1);
 }
 
 }  // extern "C"

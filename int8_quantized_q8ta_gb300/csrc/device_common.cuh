@@ -98,6 +98,34 @@ __device__ __forceinline__ uint32_t pack4(int8_t a, int8_t b, int8_t c, int8_t d
          ((uint32_t)(uint8_t)d << 24);
 }
 
+// quantize_per_tensor of one value ("Add quantize_per_tensor op", Solution
+// paragraph): clamp(rint(x * inv) + zp, -128, 127) on ALU instructions
+// (round_add_clamp_i, equal to the float form for every x; zp in [-128, 127]).
+__device__ __forceinline__ int8_t quantize_one(float x, float inv, int32_t zp) {
+  return static_cast<int8_t>(round_add_clamp_i(__fmul_rn(x, inv), zp, -128));
+}
+
+// Operand preparation for the tensor-core GEMM: int8 values, and the
+// differences x - zp in [-255, 255], are exact in bf16 (8 significant bits).
+// On integer and FP32 ALU instructions only (no conversion instruction): for
+// |v| < 2^22, bits(1.5 * 2^23) + v is the encoding of 1.5 * 2^23 + v, so one
+// exact f32 subtraction gives (float)v; with at most 8 significant bits its
+// low 16 encoding bits are zero, and the high 16 are its bf16 encoding.
+__device__ __forceinline__ uint32_t bf16_bits_hi(int v) {
+  return __float_as_uint(__fsub_rn(__int_as_float(0x4B400000 + v), 12582912.0f));
+}
+__device__ __forceinline__ uint32_t bf16x2_from_ints(int lo, int hi) {
+  return __byte_perm(bf16_bits_hi(lo), bf16_bits_hi(hi), 0x7632);
+}
+
+// Destination layout of the GEMM operands ("K-blocked"): dst[kb][r][kk] with
+// kb = k / 64 and kk = k % 64, so the 128 x 64 (or BN x 64) tile the tensor
+// cores read for one k-block is a single contiguous run in memory.
+__device__ __forceinline__ int64_t kblocked_index16(int64_t r, int64_t k0, int64_t rows) {
+  // index of the 16-byte chunk holding elements k0 .. k0 + 7 of row r
+  return (((k0 >> 6) * rows + r) * 64 + (k0 & 63)) / 8;
+}
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of the library is launched
 // with programmatic stream serialization: it may start while the previous

@@ -101,8 +101,24 @@ struct TcLinear {
   // Largest sum of |w| over one k-block of one weight row (a device word
   // written when the weight was packed), or null for the worst case 64 * 128.
   const int32_t* w_bound_dev;
+  // Failure-detection test hooks (see TcParams): the barrier-wait time limit
+  // in ns (0: the default) and a ring fill the producer skips (f + 1; 0: none).
+  uint64_t wait_ns;
+  int stall_fill;
+  // Fused quantize -> linear (qx non-null): the kernel itself quantizes fp32
+  // x [M, qK] with (qinv, qzp) into the operand `a` (and into qxq when
+  // non-null) before multiplying it; qsync is the operand's trailer, which
+  // q8_linear_operand_init prepared (see tc_gemm_kernel.cuh, kFusedMagic).
+  const float* qx;
+  int8_t* qxq;
+  float qinv;
+  int qzp;
+  int64_t qK;
+  uint32_t* qsync;
 };
 cudaError_t launch_tc_linear(const TcLinear& p, cudaStream_t s);
+// Writes the synchronization words of a fused-quantize operand trailer.
+cudaError_t launch_fused_trailer_init(uint32_t* trailer, cudaStream_t s);
 
 struct TcConvT {
   // One group's implicit GEMM of a transposed (direct == false) or direct

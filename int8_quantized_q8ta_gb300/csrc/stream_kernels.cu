@@ -58,12 +58,7 @@ static int resident_grid(Kernel kernel, int (&cache)[64], int64_t work_items, in
 // Vector path: one float4 in, one packed 32-bit word out per item; U items
 // per thread per round are loaded before any is converted.
 // ---------------------------------------------------------------------------
-// clamp(rint(x * inv) + zp, -128, 127) on ALU instructions
-// (round_add_clamp_i, equal to the float form for every x; zp in [-128, 127]).
-__device__ __forceinline__ int8_t quantize_one(float x, float inv, int32_t zp) {
-  return static_cast<int8_t>(round_add_clamp_i(__fmul_rn(x, inv), zp, -128));
-}
-
+// (quantize_one: device_common.cuh)
 template <int U>
 __global__ void __launch_bounds__(256) quantize_vec_kernel(const float4* __restrict__ x, int64_t n4,
                                                            float inv, int32_t zp,
@@ -303,24 +298,7 @@ cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w
 // Operand preparation for the tensor-core GEMM.  int8 values, and the
 // differences x - zp in [-255, 255], are exact in bf16 (8 significant bits).
 // ---------------------------------------------------------------------------
-// On integer and FP32 ALU instructions only (no conversion instruction): for
-// |v| < 2^22, bits(1.5 * 2^23) + v is the encoding of 1.5 * 2^23 + v, so one
-// exact f32 subtraction gives (float)v; with at most 8 significant bits its
-// low 16 encoding bits are zero, and the high 16 are its bf16 encoding.
-__device__ __forceinline__ uint32_t bf16_bits_hi(int v) {
-  return __float_as_uint(__fsub_rn(__int_as_float(0x4B400000 + v), 12582912.0f));
-}
-__device__ __forceinline__ uint32_t bf16x2_from_ints(int lo, int hi) {
-  return __byte_perm(bf16_bits_hi(lo), bf16_bits_hi(hi), 0x7632);
-}
-
-// Destination layout of the GEMM operands ("K-blocked"): dst[kb][r][kk] with
-// kb = k / 64 and kk = k % 64, so the 128 x 64 (or BN x 64) tile the tensor
-// cores read for one k-block is a single contiguous run in memory.
-__device__ __forceinline__ int64_t kblocked_index16(int64_t r, int64_t k0, int64_t rows) {
-  // index of the 16-byte chunk holding elements k0 .. k0 + 7 of row r
-  return (((k0 >> 6) * rows + r) * 64 + (k0 & 63)) / 8;
-}
+// (bf16x2_from_ints, kblocked_index16: device_common.cuh)
 
 // One thread converts 8 consecutive elements (16 bytes of output) of a row.
 __global__ void __launch_bounds__(256) rows_to_bf16_kernel(const int8_t* __restrict__ src,

@@ -70,7 +70,28 @@ enum : uint32_t {
   kErrWaitDrain = 0x105,
   kErrWaitEpi = 0x106,
   kErrChunks = 0x107,  // a single-chunk kernel met a tile of several chunks
+  kErrWaitQuant = 0x108,  // a fused-quantize chunk of the operand never became ready
+  kErrFusedInit = 0x109,  // fused quantize: the operand's trailer was never initialized
 };
+
+// Fused quantize -> linear: the operand's 256-byte trailer holds, as 32-bit
+// words, [0] the |x - zp| bound, [1] the count of CTAs that finished the
+// launch, [2..3] kFusedMagic (written by the trailer's initialization) and
+// [4 + c] the count of CTAs that wrote their share of operand chunk c.
+// Chunk c holds k-blocks [0, 2) for c = 0 and [2^c, 2^(c+1)) after that:
+// the first chunks are small, so the first MMAs start early, and later ones
+// are converted while the earlier ones are multiplied.
+constexpr uint64_t kFusedMagic = 0x51a8d7e3c0f1b2a4ull;
+constexpr int kFusedWordDone = 1;
+constexpr int kFusedWordMagic = 2;
+constexpr int kFusedWordChunk0 = 4;
+constexpr int kFusedMaxChunks = 60;
+__host__ __device__ constexpr int fused_chunk_count(int kb_total) {
+  // chunks 0 .. c with 2^c <= kb_total - 1 (one chunk for up to 2 k-blocks)
+  int n = 1;
+  while (n < 31 && (1 << n) < kb_total) ++n;
+  return n;
+}
 
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 constexpr int kBM = 128;
@@ -128,6 +149,23 @@ struct TcParams {
   const int32_t* a_bound_dev;  // largest |x - zp| of A, on the device (or null)
   int a_bound_host;            // the same, when a_bound_dev is null
   const int32_t* w_bound_dev;  // largest sum of |w| over one k-block of one row (or null)
+  // failure detection: every barrier wait gives up after wait_ns (0: the
+  // default kWaitLimitNs); stall_fill = f + 1 makes the TMA producer skip
+  // its f-th ring fill (a test of the timeout path; 0: none)
+  uint64_t wait_ns;
+  int stall_fill;
+  // fused quantize -> linear (MODE 0 with qx != null): the epilogue warps of
+  // all CTAs first quantize fp32 x into the operand (and x_q), chunk by
+  // chunk; a producer loads an operand chunk only once every CTA has
+  // signalled it in the trailer (see kFusedMagic)
+  const float* qx;     // fp32 activations [M, qK], row-major
+  int8_t* qxq;         // int8 quantize output [M, qK], or null
+  uint4* qdst;         // the operand the A tensor map reads, K-blocked
+  uint32_t* qsync;     // the operand's trailer
+  float qinv;          // (float)(1 / input_scale)
+  int qzp;             // input zero point
+  int qK;              // K (the operand is zero-padded to kb_total * 64)
+  int qvec;            // x (and x_q) rows allow 16-byte (8-byte) vector access
 };
 
 // Ring stages per exact f32 chunk (see kWorstWBound), from A's and W's bounds.
@@ -227,14 +265,18 @@ struct Ctl {
 
 // Bounded wait.  Returns false when this CTA is aborting (this wait timed
 // out, or another role's did).
+__device__ __forceinline__ uint64_t wait_limit(const TcParams& p) {
+  return p.wait_ns != 0 ? p.wait_ns : kWaitLimitNs;
+}
+
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                         uint32_t code, uint32_t* err) {
+                                         uint32_t code, uint32_t* err, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
       atomicCAS(err, 0u, code);
       return false;
@@ -243,11 +285,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // Bounded wait used while shutting down: ignores the abort flag.
-__device__ __forceinline__ void wait_bar_final(uint32_t bar, uint32_t parity, uint32_t* err) {
+__device__ __forceinline__ void wait_bar_final(uint32_t bar, uint32_t parity, uint32_t* err,
+                                               uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       atomicCAS(err, 0u, kErrWaitDrain);
       return;
     }
@@ -258,18 +301,137 @@ __device__ __forceinline__ void wait_bar_final(uint32_t bar, uint32_t parity, ui
 // bar.sync, so one aborted warp cannot strand the others).  Shared-memory
 // writes made before the call are visible to every epilogue thread after it.
 __device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uint32_t* abort_flag,
-                                         uint32_t* err) {
+                                         uint32_t* err, uint64_t limit_ns) {
   // every epilogue warp arrives once per rendezvous
   __syncwarp();
   bool ok = true;
   if ((threadIdx.x & 31) == 0) {
     mbar_arrive(smem_u32(&ctl->epi_bar));
-    ok = wait_bar(smem_u32(&ctl->epi_bar), phase, abort_flag, kErrWaitEpi, err);
+    ok = wait_bar(smem_u32(&ctl->epi_bar), phase, abort_flag, kErrWaitEpi, err, limit_ns);
   }
   phase ^= 1u;
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   __syncwarp();
   return ok;
+}
+
+// ---- fused quantize -> linear ---------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Generic-proxy stores made before this fence are ordered before later
+// async-proxy (TMA) accesses, and the other way round.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Named barrier 1 over the converter (epilogue) warps only.
+__device__ __forceinline__ void converters_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Bounded wait until every CTA of the launch has signalled operand chunk c.
+static __device__ __noinline__ bool wait_chunk(const TcParams& p, int c, volatile uint32_t* abort_flag) {
+  const uint32_t* word = p.qsync + kFusedWordChunk0 + c;
+  const uint32_t target = gridDim.x;
+  if (ld_acquire_gpu(word) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (ld_acquire_gpu(word) >= target) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > wait_limit(p)) {
+      *abort_flag = 1u;
+      atomicCAS(p.err, 0u, kErrWaitQuant);
+      return false;
+    }
+    __nanosleep(32);
+  }
+}
+
+// This CTA's share of quantize_per_tensor fused with the operand
+// preparation, chunk by chunk: every thread of the grid's converter warps
+// takes items of 8 consecutive elements of a row (item i of chunk c is row
+// i / segs, elements kb0 * 64 + (i % segs) * 8 ..), keeps IU items' loads
+// in flight, and writes x_q (when asked) and the bf16 of q - zp (0 past K).
+// After each chunk the CTA orders its stores before the TMA unit's reads
+// and adds one to the chunk's counter.
+template <int IU>
+__device__ __noinline__ void fused_quantize(const TcParams& p, int t, int nt) {
+  const uint32_t GT = gridDim.x * static_cast<uint32_t>(nt);
+  const uint32_t gt = blockIdx.x * static_cast<uint32_t>(nt) + static_cast<uint32_t>(t);
+  const int nch = fused_chunk_count(p.kb_total);
+  const int64_t M = p.M, K = p.qK;
+  for (int c = 0; c < nch; ++c) {
+    const int kb0 = c == 0 ? 0 : (1 << c);
+    const int kb1 = min(p.kb_total, c == 0 ? 2 : (2 << c));
+    const uint32_t segs = static_cast<uint32_t>(kb1 - kb0) * 8u;
+    const int64_t dr = GT / segs;
+    const uint32_t ds = GT % segs;
+    int64_t r = gt / segs;
+    uint32_t sg = gt % segs;
+    while (r < M) {
+      float4 va[IU], vb[IU];
+      int64_t rr[IU];
+      int64_t kk[IU];
+#pragma unroll
+      for (int u = 0; u < IU; ++u) {
+        rr[u] = r;
+        kk[u] = (static_cast<int64_t>(kb0) * 8 + sg) * 8;
+        if (p.qvec && r < M && kk[u] + 8 <= K) {
+          const float4* xp = reinterpret_cast<const float4*>(p.qx + r * K + kk[u]);
+          va[u] = __ldcs(xp);
+          vb[u] = __ldcs(xp + 1);
+        }
+        r += dr;
+        sg += ds;
+        if (sg >= segs) {
+          sg -= segs;
+          ++r;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < IU; ++u) {
+        if (rr[u] >= M) break;
+        const int64_t row = rr[u], k0 = kk[u];
+        int v[8];
+        if (p.qvec && k0 + 8 <= K) {
+          int8_t q[8];
+          q[0] = quantize_one(va[u].x, p.qinv, p.qzp); q[1] = quantize_one(va[u].y, p.qinv, p.qzp);
+          q[2] = quantize_one(va[u].z, p.qinv, p.qzp); q[3] = quantize_one(va[u].w, p.qinv, p.qzp);
+          q[4] = quantize_one(vb[u].x, p.qinv, p.qzp); q[5] = quantize_one(vb[u].y, p.qinv, p.qzp);
+          q[6] = quantize_one(vb[u].z, p.qinv, p.qzp); q[7] = quantize_one(vb[u].w, p.qinv, p.qzp);
+          if (p.qxq != nullptr)
+            *reinterpret_cast<uint2*>(p.qxq + row * K + k0) =
+                make_uint2(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]));
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = static_cast<int>(q[j]) - p.qzp;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            v[j] = 0;
+            if (k0 + j < K) {
+              const int8_t q = quantize_one(p.qx[row * K + k0 + j], p.qinv, p.qzp);
+              if (p.qxq != nullptr) p.qxq[row * K + k0 + j] = q;
+              v[j] = static_cast<int>(q) - p.qzp;
+            }
+          }
+        }
+        uint4 o;
+        o.x = bf16x2_from_ints(v[0], v[1]);
+        o.y = bf16x2_from_ints(v[2], v[3]);
+        o.z = bf16x2_from_ints(v[4], v[5]);
+        o.w = bf16x2_from_ints(v[6], v[7]);
+        p.qdst[kblocked_index16(row, k0, M)] = o;
+      }
+    }
+    fence_proxy_async_global();
+    converters_sync(nt);
+    if (t == 0) red_release_gpu_add(p.qsync + kFusedWordChunk0 + c, 1u);
+  }
 }
 
 // Exchanged operands (MODE 3 / 4): one epilogue thread holds one output
@@ -433,7 +595,8 @@ __device__ __noinline__ PixChunks pix_chunks(const TcParams& p, TileInfo ti, Pix
     const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
     bool got = true;
     if (lane == 0)
-      got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull, p.err);
+      got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull, p.err,
+                     wait_limit(p));
     got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
     if (!got) return {acc_it, false};
     tc_fence_after();
@@ -488,10 +651,13 @@ __device__ __noinline__ PixChunks pix_chunks(const TcParams& p, TileInfo ti, Pix
 // shares one 256-row tile through the 2-SM MMA (cta_group::2): each CTA
 // loads its 128 rows of A and half of B's BN rows, the leader CTA issues
 // the MMAs, and each CTA's TMEM holds the accumulators of its own rows.
-template <int BN, int EPI, int MODE, int KD, int CG>
+template <int BN, int EPI, int MODE_IN, int KD, int CG>
 __global__ void __launch_bounds__(cta_threads(EPI), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ TcParams p) {
+  // MODE_IN 7: the linear (MODE 0) with the fused quantize prologue
+  constexpr int MODE = MODE_IN == 7 ? 0 : MODE_IN;
+  constexpr bool kFusedQ = (MODE_IN == 7);
   constexpr int kEpiWarps = EPI;
   constexpr int kColGroups = EPI / 4;     // epilogue warps sharing one TMEM lane quarter
   constexpr uint32_t kABytes = kBM * kBK * 2;   // one k-block of A
@@ -583,6 +749,20 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       if (threadIdx.x == 0 && blockIdx.x == 0) atomicCAS(p.err, 0u, kErrChunks);
     }
   }
+  // Fused quantize: the chunk counters must start at zero, which the
+  // trailer's initialization (kFusedMagic) and every launch's last CTA
+  // guarantee; a trailer without the magic runs nothing (every CTA reads the
+  // same word, written before this launch).
+  constexpr bool fused = kFusedQ;
+  if constexpr (fused) {
+    const uint64_t magic = *reinterpret_cast<const volatile uint64_t*>(p.qsync + kFusedWordMagic);
+    if (magic != kFusedMagic) {
+      run = false;
+      if (threadIdx.x == 0 && blockIdx.x == 0) atomicCAS(p.err, 0u, kErrFusedInit);
+    } else if (threadIdx.x == 0 && blockIdx.x == 0) {
+      p.qsync[0] = static_cast<uint32_t>(p.a_bound_host);  // the operand's |x - zp| bound
+    }
+  }
 
   if (!run) {
     // nothing to do (see above)
@@ -591,6 +771,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       uint32_t fills = 0;
+      int chunks_ready = 0;  // fused quantize: operand chunks known complete
       bool ok = true;
       for (int u = unit0; u < p.total_units && ok; u += unit_step) {
         for (int j = 0; j < p.subtiles && ok; ++j) {
@@ -618,14 +799,29 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               const int c_w = a_w + tw * step_w, c_h = a_h + th * step_h;
               for (int blk = 0; blk < nblk; blk += KD) {
                 if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag,
-                              kErrWaitEmpty, p.err)) {
+                              kErrWaitEmpty, p.err, wait_limit(p))) {
                   ok = false;
                   break;
                 }
                 const uint32_t sa = base + stage * kStageBytes;
                 const uint32_t sb = sa + KD * kABytes;
                 const int b_row = (MODE == 0 ? ti.nb : ti.ocb) * BN + rank * (BN / CG);
-                if constexpr (kPair) {
+                if constexpr (fused) {
+                  // the stage's k-blocks blk .. blk + KD - 1 must be converted
+                  // by every CTA before the TMA unit reads them
+                  const int last = min(blk + KD, p.kb_total) - 1;
+                  const int need = last < 2 ? 0 : 31 - __clz(last);
+                  while (ok && chunks_ready <= need) {
+                    ok = wait_chunk(p, chunks_ready, abort_flag);
+                    if (ok) ++chunks_ready;
+                  }
+                  if (!ok) break;
+                  fence_proxy_async_global();
+                }
+                if (p.stall_fill != 0 && fills + 1u == static_cast<uint32_t>(p.stall_fill)) {
+                  // failure-detection test: this fill is never issued, so the
+                  // MMA's wait on its full barrier runs out (bounded)
+                } else if constexpr (kPair) {
                   // both CTAs' copies complete on the leader's full barrier
                   const uint32_t full = map_to_cta(smem_u32(&ctl->full[stage]), 0);
                   if (leader) mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), CG * kStageBytes);
@@ -667,7 +863,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       // for both, and the closing cluster barrier holds the peer until then).
       for (int s = 0; s < S && leader; ++s) {
         const uint32_t f = (fills > static_cast<uint32_t>(s)) ? (fills - s + S - 1) / S : 0;
-        if (f > 0) wait_bar_final(smem_u32(&ctl->full[s]), (f - 1) & 1u, p.err);
+        if (f > 0) wait_bar_final(smem_u32(&ctl->full[s]), (f - 1) & 1u, p.err, wait_limit(p));
       }
     }
   } else if (warp == 1) {
@@ -682,7 +878,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           for (int st0 = 0; st0 < ti.nstages && ok; st0 += chunk_st) {
             const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
             if (!wait_bar(smem_u32(&ctl->acc_empty[buf]), (use & 1u) ^ 1u, abort_flag,
-                          kErrWaitAccEmpty, p.err)) {
+                          kErrWaitAccEmpty, p.err, wait_limit(p))) {
               ok = false;
               break;
             }
@@ -690,7 +886,8 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
             const uint32_t d = tmem_base + buf * kAccStride;
             const int st_end = min(st0 + chunk_st, ti.nstages);
             for (int st = st0; st < st_end; ++st) {
-              if (!wait_bar(smem_u32(&ctl->full[stage]), phase, abort_flag, kErrWaitFull, p.err)) {
+              if (!wait_bar(smem_u32(&ctl->full[stage]), phase, abort_flag, kErrWaitFull, p.err,
+                            wait_limit(p))) {
                 ok = false;
                 break;
               }
@@ -735,7 +932,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
         umma_commit_pair(smem_u32(&ctl->drain), 0x1);
       else
         umma_commit(smem_u32(&ctl->drain));
-      wait_bar_final(smem_u32(&ctl->drain), 0u, p.err);
+      wait_bar_final(smem_u32(&ctl->drain), 0u, p.err, wait_limit(p));
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -750,6 +947,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     float px_ws = 0.0f, px_b = 0.0f;  // exchanged operands: this lane's channel
     const int ew = warp - 2;  // epilogue warp index
     bool ok = true;
+    if constexpr (fused) {
+      // fused quantize: this CTA's share of the operand, before any tile
+      fused_quantize<4>(p, et, 32 * kEpiWarps);
+    }
     for (int u = unit0; u < p.total_units && ok; u += unit_step) {
       // register staging: this thread's bytes of the unit's earlier column
       // phases, four output channels per word
@@ -777,7 +978,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               bool got = true;
               if (lane == 0)
                 got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull,
-                               p.err);
+                               p.err, wait_limit(p));
               got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
               if (!got) {
                 ok = false;
@@ -832,9 +1033,9 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
             bool got = true;
             if (lane == 0) {
               got = wait_bar(smem_u32(&ctl->acc_full[b0]), (acc_it >> 1) & 1u, abort_flag,
-                             kErrWaitAccFull, p.err) &&
+                             kErrWaitAccFull, p.err, wait_limit(p)) &&
                     wait_bar(smem_u32(&ctl->acc_full[b1]), ((acc_it + 1u) >> 1) & 1u, abort_flag,
-                             kErrWaitAccFull, p.err);
+                             kErrWaitAccFull, p.err, wait_limit(p));
             }
             got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
             if (!got) {
@@ -944,7 +1145,8 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
           const uint32_t buf = acc_it & 1u, use = acc_it >> 1;
           bool got = true;
           if (lane == 0)
-            got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull, p.err);
+            got = wait_bar(smem_u32(&ctl->acc_full[buf]), use & 1u, abort_flag, kErrWaitAccFull, p.err,
+                           wait_limit(p));
           got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
           if (!got) {
             ok = false;
@@ -1003,7 +1205,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
             ws_buf[et] = ld_ws;
             ws_buf[kMaxBN + et] = ld_b;
           }
-          if (p.acc_out == nullptr && !epi_sync(ctl, epi_phase, abort_flag, p.err)) {
+          if (p.acc_out == nullptr && !epi_sync(ctl, epi_phase, abort_flag, p.err, wait_limit(p))) {
             ok = false;
             break;
           }
@@ -1148,6 +1350,19 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       tmem_dealloc_pair(tmem_base, kTmemCols);
     else
       tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (fused && run && threadIdx.x == 0) {  // (fused: constexpr)
+    // The last CTA to finish (no producer polls the counters any more) puts
+    // them back to zero for the next launch on this operand.
+    __threadfence();
+    const uint32_t done = atomicAdd(p.qsync + kFusedWordDone, 1u);
+    if (done == gridDim.x - 1) {
+      __threadfence();
+      const int nch = fused_chunk_count(p.kb_total);
+      for (int c = 0; c < nch; ++c) p.qsync[kFusedWordChunk0 + c] = 0u;
+      p.qsync[kFusedWordDone] = 0u;
+      __threadfence();
+    }
   }
 }
 

@@ -37,6 +37,27 @@ int pick_pair_bn(int64_t M, int64_t N, int pairs) {
   return best;
 }
 
+// The instantiation for a tile width (MODE 0: prepared operand; MODE 7:
+// the same with the fused quantize prologue).
+template <int MODE>
+cudaError_t launch_linear_bn(bool pair, int bn, const CUtensorMap& ma, const CUtensorMap& mb,
+                             const TcParams& p, cudaStream_t s) {
+  if (pair) {
+    switch (bn) {
+      case 256: return launch_tc_kernel<256, 8, MODE, 2, 2>(ma, mb, p, s);
+      case 240: return launch_tc_kernel<240, 12, MODE, 2, 2>(ma, mb, p, s);
+      case 224: return launch_tc_kernel<224, 8, MODE, 2, 2>(ma, mb, p, s);
+      default: return launch_tc_kernel<192, 8, MODE, 2, 2>(ma, mb, p, s);
+    }
+  }
+  // 16 epilogue warps where their register share fits the column slice
+  switch (bn) {
+    case 64: return launch_tc_kernel<64, 16, MODE, 1, 1>(ma, mb, p, s);
+    case 128: return launch_tc_kernel<128, 16, MODE, 1, 1>(ma, mb, p, s);
+    default: return launch_tc_kernel<256, 8, MODE, 1, 1>(ma, mb, p, s);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_tc_linear(const TcLinear& L, cudaStream_t s) {
@@ -81,23 +102,41 @@ cudaError_t launch_tc_linear(const TcLinear& L, cudaStream_t s) {
   p.a_bound_dev = L.a_bound_dev;
   p.a_bound_host = L.a_bound_host;
   p.w_bound_dev = L.w_bound_dev;
+  p.wait_ns = L.wait_ns;
+  p.stall_fill = L.stall_fill;
+  if (L.qx != nullptr) {
+    if (L.qsync == nullptr || fused_chunk_count(static_cast<int>(L.Kp / kBK)) > kFusedMaxChunks)
+      return cudaErrorInvalidValue;
+    p.qx = L.qx;
+    p.qxq = L.qxq;
+    p.qdst = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(L.a));
+    p.qsync = L.qsync;
+    p.qinv = L.qinv;
+    p.qzp = L.qzp;
+    p.qK = static_cast<int>(L.qK);
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(L.qx), qa = reinterpret_cast<uintptr_t>(L.qxq);
+    p.qvec = (L.qK % 8 == 0) && (xa % 16 == 0) && (L.qxq == nullptr || qa % 8 == 0) ? 1 : 0;
+  }
   const uintptr_t oa = reinterpret_cast<uintptr_t>(L.out);
   p.store_mode = (L.N % 16 == 0 && oa % 16 == 0) ? 2 : (oa % 4 == 0 ? 1 : 0);
   if (p.total_units == 0) return cudaSuccess;
-  if (pair) {
-    switch (bn) {
-      case 256: return launch_tc_kernel<256, 8, 0, 2, 2>(ma, mb, p, s);
-      case 240: return launch_tc_kernel<240, 12, 0, 2, 2>(ma, mb, p, s);
-      case 224: return launch_tc_kernel<224, 8, 0, 2, 2>(ma, mb, p, s);
-      default: return launch_tc_kernel<192, 8, 0, 2, 2>(ma, mb, p, s);
-    }
-  }
-  // 16 epilogue warps where their register share fits the column slice
-  switch (bn) {
-    case 64: return launch_tc_kernel<64, 16, 0, 1, 1>(ma, mb, p, s);
-    case 128: return launch_tc_kernel<128, 16, 0, 1, 1>(ma, mb, p, s);
-    default: return launch_tc_kernel<256, 8, 0, 1, 1>(ma, mb, p, s);
-  }
+  return L.qx != nullptr ? launch_linear_bn<7>(pair, bn, ma, mb, p, s)
+                        : launch_linear_bn<0>(pair, bn, ma, mb, p, s);
+}
+
+__global__ void fused_trailer_init_kernel(uint32_t* t) {
+  pdl_wait();  // a launch before this one may still use the trailer
+  pdl_launch_dependents();
+  // [0] the worst-case |x - zp| bound until a launch writes the real one
+  if (threadIdx.x == 0) t[0] = 255u;
+  if (threadIdx.x == 1) t[kFusedWordDone] = 0u;
+  if (threadIdx.x == 2) *reinterpret_cast<uint64_t*>(t + kFusedWordMagic) = kFusedMagic;
+  if (threadIdx.x >= kFusedWordChunk0 && threadIdx.x < kFusedWordChunk0 + kFusedMaxChunks)
+    t[threadIdx.x] = 0u;
+}
+
+cudaError_t launch_fused_trailer_init(uint32_t* trailer, cudaStream_t s) {
+  return launch_pdl(fused_trailer_init_kernel, 1, 64, 0, s, trailer);
 }
 
 }  // namespace q8

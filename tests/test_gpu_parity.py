@@ -185,6 +185,12 @@ def test_linear_chain_2048x4096x11008_full():
                                       p["out_scale"], p["out_zp"]))
     n_bad, first = _mismatches(out2, ref)
     assert n_bad == 0, f"{n_bad} of {ref.size} outputs differ, first: {first}"
+    # the fused form (quantize inside the GEMM kernel, one launch)
+    xq3, out3, _ = q8.quantize_linear_fused(T(x), p["in_scale"], p["in_zp"], packed, T(ws),
+                                            T(b), p["out_scale"], p["out_zp"], operand=operand)
+    np.testing.assert_array_equal(H(xq3), xq_ref)
+    n_bad, first = _mismatches(H(out3), ref)
+    assert n_bad == 0, f"{n_bad} of {ref.size} outputs differ, first: {first}"
 
 
 def test_acc32_exact_at_the_chunk_bound():
