@@ -3,9 +3,10 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
   1. quantize_per_tensor        fp32 [64Mi] -> int8                (HBM bound)
-  2. quantize -> q8ta_linear   fp32 [2048, 4096] -> int8 x_q, then the GEMM
-                                2048 x 4096 x 11008 with a packed weight, in ONE
-                                kernel (the GEMM's warps quantize x; tensor cores)
+  2. quantize -> q8ta_linear   fp32 [2048, 4096] -> int8 x_q + the bf16 operand,
+                                then the GEMM 2048 x 4096 x 11008 with a packed
+                                weight (two kernels under programmatic dependent
+                                launch; tensor cores)
   3. q8ta_linear_gemv           1 x 4096 x 4096                    (HBM bound)
   4. q8ta_conv2d_transposed     [8,256,64,64] -> [8,128,128,128], K=3 s=2 p=1 op=1
 
@@ -71,6 +72,7 @@ CONV_MACS = conv_valid_macs(CD, CHo, CWo)
 OPS_CONV = 2 * CONV_MACS
 OPS_STEP = OPS_LINEAR + OPS_GEMV + OPS_CONV
 CONV_OUTPUTS = CD["N"] * CD["OC"] * CHo * CWo
+BYTES_CHAIN_PREP = LM * LK * (4 + 1 + 2)
 # algorithmic bytes (each input read once, each output written once)
 BYTES_QUANT = QN * (4 + 1)
 BYTES_GEMV = GN * GK + GK + GN + 2 * GN * 4
@@ -193,7 +195,7 @@ class Path:
             dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
-    LAUNCHES = {"quantize": 1, "linear": 1, "gemv": 1, "conv_t": 2}
+    LAUNCHES = {"quantize": 1, "linear": 2, "gemv": 1, "conv_t": 2}
 
     def launches_per_step(self):
         if self.only == "all":
@@ -205,16 +207,19 @@ class Path:
     INPUTS = {"quantize": "xq", "linear": "lx", "gemv": "gx", "conv_t": "cx"}
     OUTPUTS = {"quantize": "q_out", "linear": "l_out", "gemv": "g_out", "conv_t": "c_out"}
 
-    def run_op(self, name):
-        """Enqueue one op on the current stream (the linear op is the fused
-        quantize -> q8ta_linear kernel)."""
+    def run_op(self, name, mid=None):
+        """Enqueue one op on the current stream (the linear op is the
+        quantize -> operand kernel and the GEMM; mid() runs between them)."""
         q8, qp, lp, gp, cp = self.q8, Q.params, L.params, G.params, C.params
         if name == "quantize":
             q8.quantize_per_tensor(self.xq, qp["in_scale"], qp["in_zp"], out=self.q_out)
         elif name == "linear":
-            q8.quantize_linear_fused(self.lx, lp["in_scale"], lp["in_zp"], self.packed, self.lws,
-                                     self.lb, lp["out_scale"], lp["out_zp"], x_q=self.l_xq,
-                                     out=self.l_out, operand=self.operand)
+            q8.quantize_to_operand(self.lx, lp["in_scale"], lp["in_zp"], x_q=self.l_xq,
+                                   operand=self.operand)
+            if mid:
+                mid()
+            q8.linear_operand_packed(self.operand, lp["in_scale"], self.packed, self.lws, self.lb,
+                                     lp["out_scale"], lp["out_zp"], out=self.l_out)
         elif name == "gemv":
             q8.linear_gemv(self.gx, gp["in_scale"], gp["in_zp"], self.gw, None, self.gws, self.gb,
                            gp["out_scale"], gp["out_zp"], out=self.g_out)
@@ -225,14 +230,21 @@ class Path:
                                         output_padding=CD["op"], out=self.c_out,
                                         workspace=self.c_ws)
 
+    # per-op timing slots: events 0..5 bracket quantize, the linear's operand
+    # preparation, the linear GEMM, the gemv and the transposed convolution
+    TIMED = ("quantize", "chain_prep", "linear", "gemv", "conv_t")
+
     def step(self, ev=None):
-        """Enqueue one step; ev (a list of len(OPS) + 1 CUDA events) brackets each op."""
+        """Enqueue one step; ev (a list of 6 CUDA events) brackets each op."""
         rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
-        for i, op in enumerate(self.OPS):
-            rec(i)
+        slot = {"quantize": 0, "linear": 1, "gemv": 3, "conv_t": 4}
+        for op in self.OPS:
+            rec(slot[op])
             if self.only in ("all", op):
-                self.run_op(op)
-        rec(len(self.OPS))
+                self.run_op(op, mid=(lambda: rec(2)) if op == "linear" else None)
+            elif op == "linear":
+                rec(2)
+        rec(5)
 
 
 GEMV_CHAIN_COPIES = 24   # 24 x 16.8 MB of weights: 403 MB, more than 3x the 129 MB L2
@@ -304,6 +316,31 @@ def small_op_latency(fn, reps=60, warm=10):
         b.record()
     torch.cuda.synchronize()
     return statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+
+
+def fused_chain_ab(path, reps=10):
+    """The prefill chain both ways, interleaved, each call bracketed by CUDA
+    events: two kernels (quantize -> operand, then the GEMM) and the single
+    fused kernel (q8_quantize_linear_fused).  Returns median microseconds."""
+    torch, q8 = path.torch, path.q8
+    lp = L.params
+    def two():
+        path.run_op("linear")
+    def one():
+        q8.quantize_linear_fused(path.lx, lp["in_scale"], lp["in_zp"], path.packed, path.lws,
+                                 path.lb, lp["out_scale"], lp["out_zp"], x_q=path.l_xq,
+                                 out=path.l_out, operand=path.operand)
+    res = {"two_kernels": [], "one_kernel": []}
+    for it in range(reps + 2):
+        for name, fn in (("two_kernels", two), ("one_kernel", one)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= 2:
+                res[name].append(e0.elapsed_time(e1) * 1e3)
+    return {k: statistics.median(v) for k, v in res.items()}
 
 
 def graph_per_call_us(fn, calls=32, reps=20):
@@ -591,8 +628,7 @@ def run_ours(args, rank, world, local_rank):
     # Per-op times come from a second pass with an event between ops (an
     # event on the stream also stops one kernel from starting under the
     # previous one's tail, so these times include each op's own ramp).
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(Path.OPS) + 1)]
-           for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     for k in range(K):
         path.step(evs[k])
     torch.cuda.synchronize()
@@ -609,8 +645,14 @@ def run_ours(args, rank, world, local_rank):
         chain_us, chain_graph = gemv_chain_measure(path)
     if args.only == "all" and not args.no_extra_ops:
         extra_ops = small_configs_measure(dev)
+        ab = fused_chain_ab(path)
+        extra_ops["quantize_q8ta_linear_2048x4096x11008_two_vs_one_kernel"] = {
+            "us_two_kernels": ab["two_kernels"], "us_one_kernel": ab["one_kernel"],
+            "method": "the prefill chain alone, each call bracketed by CUDA events, median of 10 "
+                      "interleaved calls: quantize->operand + GEMM (the step's form) against "
+                      "the single kernel whose warps quantize x into the operand"}
 
-    names = list(Path.OPS)
+    names = list(Path.TIMED)
     per = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
            for i, n in enumerate(names)}
     hbm, bf16, peak_src = measured_peaks()
@@ -619,11 +661,12 @@ def run_ours(args, rank, world, local_rank):
     ops = {
         "quantize_64Mi": {"us": us["quantize"], "GB/s": BYTES_QUANT / us["quantize"] / 1e3,
                           "frac_hbm": BYTES_QUANT / us["quantize"] / 1e3 / hbm},
-        "quantize_q8ta_linear_2048x4096x11008": {
+        "chain_quantize_to_operand_2048x4096": {
+            "us": us["chain_prep"], "GB/s": BYTES_CHAIN_PREP / us["chain_prep"] / 1e3,
+            "frac_hbm": BYTES_CHAIN_PREP / us["chain_prep"] / 1e3 / hbm},
+        "q8ta_linear_2048x4096x11008": {
             "us": us["linear"], "TOPS": OPS_LINEAR / us["linear"] / 1e6,
-            "frac_bf16_peak": OPS_LINEAR / us["linear"] / 1e6 / bf16,
-            "note": "one kernel: quantize of the fp32 activations (writing x_q) fused with the "
-                    "GEMM; TOPS counts the GEMM's 2*M*N*K only"},
+            "frac_bf16_peak": OPS_LINEAR / us["linear"] / 1e6 / bf16},
         "q8ta_linear_gemv_1x4096x4096": {
             "us": us["gemv"], "GB/s": BYTES_GEMV / us["gemv"] / 1e3,
             "frac_hbm": BYTES_GEMV / us["gemv"] / 1e3 / hbm,
@@ -643,12 +686,12 @@ def run_ours(args, rank, world, local_rank):
                       f"{GEMV_CHAIN_REPS}x; events only around the replays"}
     ops.update(extra_ops)
     achieved = OPS_LINEAR / us["linear"] / 1e6
-    roofline = {"kernel": "tc_gemm_kernel<240,12,7,2,2> (quantize -> q8ta_linear 2048x4096x11008, "
-                          "fused)", "bound": "tensor",
+    roofline = {"kernel": "tc_gemm_kernel<240,12,0,2,2> (q8ta_linear 2048x4096x11008)",
+                "bound": "tensor",
                 "achieved": achieved, "peak": bf16,
                 "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)",
                 "unit": "TFLOP/s", "frac": achieved / bf16,
-                "traffic": traffic_from_profile("tc_gemm_fused_linear_2048x4096x11008"),
+                "traffic": traffic_from_profile("tc_gemm_linear_2048x4096x11008"),
                 "algorithmic_flops_per_launch": OPS_LINEAR}
 
     result = {

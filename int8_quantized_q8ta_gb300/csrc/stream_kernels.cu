@@ -206,39 +206,42 @@ __global__ void __launch_bounds__(128) gemv_kernel(const int8_t* __restrict__ x,
   }
   pdl_launch_dependents();
   pdl_wait();
+  // the row's scale and bias are requested now, so their latency hides
+  // under the weight stream instead of following the reduction
+  float wsn = 0.0f, bn = 0.0f;
+  if (n < N && lane == 0) {
+    wsn = __ldg(ws + n);
+    bn = bias ? __ldg(bias + n) : 0.0f;
+  }
   int dot = 0, wsum = 0;
   if (n < N) {
     const int8_t* wr = w + static_cast<int64_t>(n) * K;
     if constexpr (VEC == 16) {
+      // rounds of 8 x 16 bytes per lane (4 KB per warp), every load of a
+      // round issued before any is used; K % 16 == 0 on this path
       constexpr int UNR = 8;
       const int nv = K / 16;
       const int4* w4 = reinterpret_cast<const int4*>(wr);
       const int4* x4 = reinterpret_cast<const int4*>(x);
-      int i = lane;
-      for (; i + 32 * (UNR - 1) < nv; i += 32 * UNR) {
+      for (int base = 0; base < nv; base += 32 * UNR) {
         int4 wv[UNR];
 #pragma unroll
-        for (int u = 0; u < UNR; ++u) wv[u] = __ldcs(w4 + i + 32 * u);
+        for (int u = 0; u < UNR; ++u) {
+          const int idx = base + lane + 32 * u;
+          wv[u] = idx < nv ? __ldcs(w4 + idx) : make_int4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
-          const int4 xv = __ldg(x4 + i + 32 * u);
-          dp4a_acc(wv[u].x, xv.x, dot, wsum);
-          dp4a_acc(wv[u].y, xv.y, dot, wsum);
-          dp4a_acc(wv[u].z, xv.z, dot, wsum);
-          dp4a_acc(wv[u].w, xv.w, dot, wsum);
+          const int idx = base + lane + 32 * u;
+          if (idx < nv) {
+            const int4 xv = __ldg(x4 + idx);
+            dp4a_acc(wv[u].x, xv.x, dot, wsum);
+            dp4a_acc(wv[u].y, xv.y, dot, wsum);
+            dp4a_acc(wv[u].z, xv.z, dot, wsum);
+            dp4a_acc(wv[u].w, xv.w, dot, wsum);
+          }
         }
       }
-      for (; i < nv; i += 32) {
-        const int4 wv = __ldcs(w4 + i), xv = __ldg(x4 + i);
-        dp4a_acc(wv.x, xv.x, dot, wsum);
-        dp4a_acc(wv.y, xv.y, dot, wsum);
-        dp4a_acc(wv.z, xv.z, dot, wsum);
-        dp4a_acc(wv.w, xv.w, dot, wsum);
-      }
-      // K % 16 tail in 4-byte words (K % 4 == 0 is a guard of the op)
-      const uint32_t* w1 = reinterpret_cast<const uint32_t*>(wr);
-      const uint32_t* x1 = reinterpret_cast<const uint32_t*>(x);
-      for (int j = nv * 4 + lane; j < K / 4; j += 32) dp4a_acc(__ldcs(w1 + j), __ldg(x1 + j), dot, wsum);
     } else if constexpr (VEC == 4) {
       const uint32_t* w1 = reinterpret_cast<const uint32_t*>(wr);
       const uint32_t* x1 = reinterpret_cast<const uint32_t*>(x);
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(128) gemv_kernel(const int8_t* __restrict__ x,
     if (lane == 0) {
       const int32_t acc = static_cast<int32_t>(static_cast<uint32_t>(dot) -
                                                static_cast<uint32_t>(izp) * static_cast<uint32_t>(wsum));
-      res[warp] = requant_one(acc, ws[n], bias ? bias[n] : 0.0f, rq);
+      res[warp] = requant_one(acc, wsn, bn, rq);
     }
   }
   __syncthreads();

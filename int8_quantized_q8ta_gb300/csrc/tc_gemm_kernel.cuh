@@ -77,20 +77,19 @@ enum : uint32_t {
 // Fused quantize -> linear: the operand's 256-byte trailer holds, as 32-bit
 // words, [0] the |x - zp| bound, [1] the count of CTAs that finished the
 // launch, [2..3] kFusedMagic (written by the trailer's initialization) and
-// [4 + c] the count of CTAs that wrote their share of operand chunk c.
-// Chunk c holds k-blocks [0, 2) for c = 0 and [2^c, 2^(c+1)) after that:
-// the first chunks are small, so the first MMAs start early, and later ones
-// are converted while the earlier ones are multiplied.
+// [4 + c] the count of CTAs that wrote their share of operand chunk c, a
+// chunk being qckb consecutive k-blocks of every row (at most 60 chunks).
 constexpr uint64_t kFusedMagic = 0x51a8d7e3c0f1b2a4ull;
 constexpr int kFusedWordDone = 1;
 constexpr int kFusedWordMagic = 2;
 constexpr int kFusedWordChunk0 = 4;
 constexpr int kFusedMaxChunks = 60;
-__host__ __device__ constexpr int fused_chunk_count(int kb_total) {
-  // chunks 0 .. c with 2^c <= kb_total - 1 (one chunk for up to 2 k-blocks)
-  int n = 1;
-  while (n < 31 && (1 << n) < kb_total) ++n;
-  return n;
+// k-blocks per chunk: 2 (one ring stage of the pair GEMM), doubled until
+// the chunk count fits kFusedMaxChunks
+__host__ __device__ constexpr int fused_chunk_kb(int kb_total) {
+  int kb = 2;
+  while ((kb_total + kb - 1) / kb > kFusedMaxChunks) kb *= 2;
+  return kb;
 }
 
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
@@ -166,6 +165,9 @@ struct TcParams {
   int qzp;             // input zero point
   int qK;              // K (the operand is zero-padded to kb_total * 64)
   int qvec;            // x (and x_q) rows allow 16-byte (8-byte) vector access
+  int qckb;            // k-blocks per operand chunk (fused_chunk_kb, a power of two)
+  int qseg_log2;       // log2(qckb * 8): 8-element items per row and chunk
+  int qnch;            // operand chunks
 };
 
 // Ring stages per exact f32 chunk (see kWorstWBound), from A's and W's bounds.
@@ -257,6 +259,7 @@ struct Ctl {
   uint64_t epi_bar;            // epilogue-warps rendezvous (one arrival per epilogue warp)
   uint32_t tmem_base;
   uint32_t abort_flag;
+  uint32_t qwarps[kFusedMaxChunks];  // fused quantize: this CTA's warps done with each chunk
   // column scales and biases of the current tile:
   //   linear: shared by all epilogue warps, two buffers by tile parity, [2][2][BN]
   //   conv:   one slice per epilogue warp, [warp][2][BN / (warps / 4)] = 8 * BN
@@ -316,32 +319,43 @@ __device__ __forceinline__ bool epi_sync(Ctl* ctl, uint32_t& phase, volatile uin
 }
 
 // ---- fused quantize -> linear ---------------------------------------------
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
   uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void red_relaxed_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 // Generic-proxy stores made before this fence are ordered before later
 // async-proxy (TMA) accesses, and the other way round.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-// Named barrier 1 over the converter (epilogue) warps only.
-__device__ __forceinline__ void converters_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_u32(p)), "r"(v)
+               : "memory");
+  return old;
 }
 
-// Bounded wait until every CTA of the launch has signalled operand chunk c.
+// Bounded wait until every CTA of the launch has signalled operand chunk c:
+// relaxed polling, then one acquire fence (the counter's increments follow a
+// release fence on the writers' side).
 static __device__ __noinline__ bool wait_chunk(const TcParams& p, int c, volatile uint32_t* abort_flag) {
   const uint32_t* word = p.qsync + kFusedWordChunk0 + c;
   const uint32_t target = gridDim.x;
-  if (ld_acquire_gpu(word) >= target) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (ld_acquire_gpu(word) >= target) return true;
+    if (ld_relaxed_gpu(word) >= target) {
+      fence_acq_rel_gpu();
+      return true;
+    }
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > wait_limit(p)) {
       *abort_flag = 1u;
@@ -353,85 +367,114 @@ static __device__ __noinline__ bool wait_chunk(const TcParams& p, int c, volatil
 }
 
 // This CTA's share of quantize_per_tensor fused with the operand
-// preparation, chunk by chunk: every thread of the grid's converter warps
-// takes items of 8 consecutive elements of a row (item i of chunk c is row
-// i / segs, elements kb0 * 64 + (i % segs) * 8 ..), keeps IU items' loads
-// in flight, and writes x_q (when asked) and the bf16 of q - zp (0 past K).
-// After each chunk the CTA orders its stores before the TMA unit's reads
-// and adds one to the chunk's counter.
+// preparation.  The work is a list of items of 8 consecutive elements of
+// one row, chunk after chunk: item I is (chunk c, index i) = (I / P, I % P),
+// P = M * segs, segs = qckb * 8 items per row and chunk; index i is row
+// i / segs, elements (c * segs + i % segs) * 8 .. + 7.  Thread g of the
+// grid's converter threads takes items g, g + GT, g + 2 GT, ... (GT of
+// them in the grid), loads IU items before converting any, writes x_q
+// (when asked) and the bf16 of q - zp (0 past K), and never waits on a
+// barrier: after each batch its warp counts, in shared memory, the chunks
+// all its lanes have passed, and the warp that completes a chunk for the
+// CTA adds one to the chunk's counter in the trailer (a release at GPU
+// scope, after the stores were ordered before the TMA unit's reads).
+__device__ __forceinline__ void fused_report(const TcParams& p, uint32_t* qwarps, uint32_t nwarps,
+                                             int& done, int upto) {
+  bool fenced = false;  // one GPU-scope release fence covers every count that follows
+  for (; done < upto; ++done) {
+    const uint32_t prev = atom_add_acq_rel_cta(qwarps + done, 1u);
+    if (prev == nwarps - 1) {
+      if (!fenced) {
+        fence_acq_rel_gpu();
+        fenced = true;
+      }
+      red_relaxed_gpu_add(p.qsync + kFusedWordChunk0 + done, 1u);
+    }
+  }
+}
+
 template <int IU>
-__device__ __noinline__ void fused_quantize(const TcParams& p, int t, int nt) {
-  const uint32_t GT = gridDim.x * static_cast<uint32_t>(nt);
-  const uint32_t gt = blockIdx.x * static_cast<uint32_t>(nt) + static_cast<uint32_t>(t);
-  const int nch = fused_chunk_count(p.kb_total);
-  const int64_t M = p.M, K = p.qK;
-  for (int c = 0; c < nch; ++c) {
-    const int kb0 = c == 0 ? 0 : (1 << c);
-    const int kb1 = min(p.kb_total, c == 0 ? 2 : (2 << c));
-    const uint32_t segs = static_cast<uint32_t>(kb1 - kb0) * 8u;
-    const int64_t dr = GT / segs;
-    const uint32_t ds = GT % segs;
-    int64_t r = gt / segs;
-    uint32_t sg = gt % segs;
-    while (r < M) {
-      float4 va[IU], vb[IU];
-      int64_t rr[IU];
-      int64_t kk[IU];
+__device__ __noinline__ void fused_quantize(const TcParams& p, uint32_t* qwarps, int t, int nt) {
+  const int lane = t & 31;
+  const uint32_t nwarps = static_cast<uint32_t>(nt >> 5);
+  const int sh = p.qseg_log2;
+  const int64_t M = p.M, K = p.qK, Kp = static_cast<int64_t>(p.kb_total) * 64;
+  const int64_t P = M << sh;
+  const int64_t GT = static_cast<int64_t>(gridDim.x) * nt;
+  const int64_t gc = GT / P, gi = GT - gc * P;
+  const int64_t I = static_cast<int64_t>(blockIdx.x) * nt + t;
+  int64_t c = I / P, i = I - c * P;
+  int done = 0;  // chunks this warp has reported
+  while (__shfl_sync(0xffffffffu, (c < p.qnch ? static_cast<int>(c) : p.qnch), 0) < p.qnch) {
+    float4 va[IU], vb[IU];
+    int cu[IU];
+    int64_t iu[IU];
 #pragma unroll
-      for (int u = 0; u < IU; ++u) {
-        rr[u] = r;
-        kk[u] = (static_cast<int64_t>(kb0) * 8 + sg) * 8;
-        if (p.qvec && r < M && kk[u] + 8 <= K) {
-          const float4* xp = reinterpret_cast<const float4*>(p.qx + r * K + kk[u]);
+    for (int u = 0; u < IU; ++u) {
+      cu[u] = (c < p.qnch ? static_cast<int>(c) : p.qnch);
+      iu[u] = i;
+      if (c < p.qnch) {
+        const int64_t row = i >> sh;
+        const int64_t k0 = ((c << sh) + (i - (row << sh))) * 8;
+        if (p.qvec && k0 + 8 <= K) {
+          const float4* xp = reinterpret_cast<const float4*>(p.qx + row * K + k0);
           va[u] = __ldcs(xp);
           vb[u] = __ldcs(xp + 1);
         }
-        r += dr;
-        sg += ds;
-        if (sg >= segs) {
-          sg -= segs;
-          ++r;
-        }
       }
-#pragma unroll
-      for (int u = 0; u < IU; ++u) {
-        if (rr[u] >= M) break;
-        const int64_t row = rr[u], k0 = kk[u];
-        int v[8];
-        if (p.qvec && k0 + 8 <= K) {
-          int8_t q[8];
-          q[0] = quantize_one(va[u].x, p.qinv, p.qzp); q[1] = quantize_one(va[u].y, p.qinv, p.qzp);
-          q[2] = quantize_one(va[u].z, p.qinv, p.qzp); q[3] = quantize_one(va[u].w, p.qinv, p.qzp);
-          q[4] = quantize_one(vb[u].x, p.qinv, p.qzp); q[5] = quantize_one(vb[u].y, p.qinv, p.qzp);
-          q[6] = quantize_one(vb[u].z, p.qinv, p.qzp); q[7] = quantize_one(vb[u].w, p.qinv, p.qzp);
-          if (p.qxq != nullptr)
-            *reinterpret_cast<uint2*>(p.qxq + row * K + k0) =
-                make_uint2(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]));
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = static_cast<int>(q[j]) - p.qzp;
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            v[j] = 0;
-            if (k0 + j < K) {
-              const int8_t q = quantize_one(p.qx[row * K + k0 + j], p.qinv, p.qzp);
-              if (p.qxq != nullptr) p.qxq[row * K + k0 + j] = q;
-              v[j] = static_cast<int>(q) - p.qzp;
-            }
-          }
-        }
-        uint4 o;
-        o.x = bf16x2_from_ints(v[0], v[1]);
-        o.y = bf16x2_from_ints(v[2], v[3]);
-        o.z = bf16x2_from_ints(v[4], v[5]);
-        o.w = bf16x2_from_ints(v[6], v[7]);
-        p.qdst[kblocked_index16(row, k0, M)] = o;
+      c += gc;
+      i += gi;
+      if (i >= P) {
+        i -= P;
+        ++c;
       }
     }
+#pragma unroll
+    for (int u = 0; u < IU; ++u) {
+      if (cu[u] >= p.qnch) break;
+      const int64_t row = iu[u] >> sh;
+      const int64_t k0 = ((static_cast<int64_t>(cu[u]) << sh) + (iu[u] - (row << sh))) * 8;
+      if (k0 >= Kp) continue;  // the last chunk's k-blocks past the operand
+      int v[8];
+      if (p.qvec && k0 + 8 <= K) {
+        int8_t q[8];
+        q[0] = quantize_one(va[u].x, p.qinv, p.qzp); q[1] = quantize_one(va[u].y, p.qinv, p.qzp);
+        q[2] = quantize_one(va[u].z, p.qinv, p.qzp); q[3] = quantize_one(va[u].w, p.qinv, p.qzp);
+        q[4] = quantize_one(vb[u].x, p.qinv, p.qzp); q[5] = quantize_one(vb[u].y, p.qinv, p.qzp);
+        q[6] = quantize_one(vb[u].z, p.qinv, p.qzp); q[7] = quantize_one(vb[u].w, p.qinv, p.qzp);
+        if (p.qxq != nullptr)
+          *reinterpret_cast<uint2*>(p.qxq + row * K + k0) =
+              make_uint2(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = static_cast<int>(q[j]) - p.qzp;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[j] = 0;
+          if (k0 + j < K) {
+            const int8_t q = quantize_one(p.qx[row * K + k0 + j], p.qinv, p.qzp);
+            if (p.qxq != nullptr) p.qxq[row * K + k0 + j] = q;
+            v[j] = static_cast<int>(q) - p.qzp;
+          }
+        }
+      }
+      uint4 o;
+      o.x = bf16x2_from_ints(v[0], v[1]);
+      o.y = bf16x2_from_ints(v[2], v[3]);
+      o.z = bf16x2_from_ints(v[4], v[5]);
+      o.w = bf16x2_from_ints(v[6], v[7]);
+      p.qdst[kblocked_index16(row, k0, M)] = o;
+    }
+    // every item of this warp below lane 0's next one is done: the chunks
+    // before that item's chunk are complete for the warp
     fence_proxy_async_global();
-    converters_sync(nt);
-    if (t == 0) red_release_gpu_add(p.qsync + kFusedWordChunk0 + c, 1u);
+    __syncwarp();
+    const int passed = __shfl_sync(0xffffffffu, (c < p.qnch ? static_cast<int>(c) : p.qnch), 0);
+    if (lane == 0) fused_report(p, qwarps, nwarps, done, passed);
+    done = passed;
   }
+  // chunks past this warp's last item (or all of them, for a warp with none)
+  if (lane == 0) fused_report(p, qwarps, nwarps, done, p.qnch);
 }
 
 // Exchanged operands (MODE 3 / 4): one epilogue thread holds one output
@@ -715,6 +758,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     mbar_init(smem_u32(&ctl->drain), 1);
     mbar_init(smem_u32(&ctl->epi_bar), kEpiWarps);
     ctl->abort_flag = 0u;
+    for (int c = 0; c < kFusedMaxChunks; ++c) ctl->qwarps[c] = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -809,8 +853,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                 if constexpr (fused) {
                   // the stage's k-blocks blk .. blk + KD - 1 must be converted
                   // by every CTA before the TMA unit reads them
-                  const int last = min(blk + KD, p.kb_total) - 1;
-                  const int need = last < 2 ? 0 : 31 - __clz(last);
+                  const int need = (min(blk + KD, p.kb_total) - 1) / p.qckb;
                   while (ok && chunks_ready <= need) {
                     ok = wait_chunk(p, chunks_ready, abort_flag);
                     if (ok) ++chunks_ready;
@@ -949,7 +992,8 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     bool ok = true;
     if constexpr (fused) {
       // fused quantize: this CTA's share of the operand, before any tile
-      fused_quantize<4>(p, et, 32 * kEpiWarps);
+      // 8 items in flight per thread where the registers allow (<= 448 threads)
+      fused_quantize<(cta_threads(EPI) <= 448 ? 8 : 4)>(p, ctl->qwarps, et, 32 * kEpiWarps);
     }
     for (int u = unit0; u < p.total_units && ok; u += unit_step) {
       // register staging: this thread's bytes of the unit's earlier column
@@ -1358,8 +1402,7 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
     const uint32_t done = atomicAdd(p.qsync + kFusedWordDone, 1u);
     if (done == gridDim.x - 1) {
       __threadfence();
-      const int nch = fused_chunk_count(p.kb_total);
-      for (int c = 0; c < nch; ++c) p.qsync[kFusedWordChunk0 + c] = 0u;
+      for (int c = 0; c < p.qnch; ++c) p.qsync[kFusedWordChunk0 + c] = 0u;
       p.qsync[kFusedWordDone] = 0u;
       __threadfence();
     }

@@ -105,8 +105,12 @@ cudaError_t launch_tc_linear(const TcLinear& L, cudaStream_t s) {
   p.wait_ns = L.wait_ns;
   p.stall_fill = L.stall_fill;
   if (L.qx != nullptr) {
-    if (L.qsync == nullptr || fused_chunk_count(static_cast<int>(L.Kp / kBK)) > kFusedMaxChunks)
-      return cudaErrorInvalidValue;
+    const int kb = static_cast<int>(L.Kp / kBK);
+    p.qckb = fused_chunk_kb(kb);
+    p.qseg_log2 = 0;
+    while ((1 << p.qseg_log2) < p.qckb * 8) ++p.qseg_log2;
+    p.qnch = (kb + p.qckb - 1) / p.qckb;
+    if (L.qsync == nullptr || p.qnch > kFusedMaxChunks) return cudaErrorInvalidValue;
     p.qx = L.qx;
     p.qxq = L.qxq;
     p.qdst = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(L.a));
