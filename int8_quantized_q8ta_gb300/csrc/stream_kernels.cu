@@ -453,67 +453,74 @@ cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, f
 // dst[n][j*CBg + c/64][h][w][c%64] for channel c of group j (CBg = ICgp/64
 // blocks per group); the padding channels ICg <= c < ICgp hold exactly 0, not
 // -zp, so the (64 channels x w x h) box of one k-block is contiguous along w.
-// A thread takes 8 channels x 4 columns of one (n, h) row: 8 loads of 4
-// bytes (consecutive threads take consecutive column quads of one channel,
-// so a warp reads whole 32-byte sectors) and 4 stores of 16 bytes (the
-// 8-channel pieces of 4 columns).  No shared memory, no block barrier.
-template <typename Idx>
+// One block per (n, channel block, h, 64 columns): 256 threads load the 64
+// channels' 64-byte row pieces (16 bytes each, consecutive threads along a
+// row), transpose them through shared memory and store the slab's 64
+// columns x 64 channels of bf16 as 8 KB of consecutive 16-byte pieces (a
+// warp writes 512 contiguous bytes per instruction).
+template <bool VEC>
 __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __restrict__ x,
-                                                                Idx NH, int64_t groups, int64_t ICg,
-                                                                Idx H, int64_t W, int32_t zp,
+                                                                int64_t groups, int64_t ICg,
+                                                                int64_t H, int64_t W, int32_t zp,
                                                                 uint4* __restrict__ dst,
                                                                 int64_t ICgp) {
+  // 64 channels x 64 column bytes, rows padded to 17 words (conflict-free)
+  __shared__ uint32_t tile[64][17];
   pdl_wait();
   pdl_launch_dependents();
-  const Idx W4 = static_cast<Idx>((W + 3) / 4);
-  const Idx CBg = static_cast<Idx>(ICgp / 64);
-  const Idx CB = CBg * static_cast<Idx>(groups);
-  const int64_t C = groups * ICg;
-  const Idx total = NH * CB * 8 * W4;
-  const bool vec = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 4 == 0);
-  for (Idx i = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<Idx>(gridDim.x) * blockDim.x) {
-    const int64_t w4 = i % W4;
-    Idx rest = i / W4;
-    const int cseg = static_cast<int>(rest % 8);
-    rest /= 8;
-    const int64_t cb = rest % CB;
-    const Idx nhi = rest / CB;
-    const int64_t n = nhi / H, h = nhi - (nhi / H) * H;
-    const int64_t g = cb / CBg;
-    const int64_t cl0 = (cb - g * CBg) * 64 + 8 * cseg;   // channel within the group
-    const int64_t wb = 4 * w4;
-    uint32_t raw[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      raw[j] = 0u;
-      if (cl0 + j < ICg) {
-        const int8_t* src = x + ((n * C + g * ICg + cl0 + j) * H + h) * W + wb;
-        if (vec) {
-          raw[j] = __ldcs(reinterpret_cast<const unsigned int*>(src));
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (wb + q < W) raw[j] |= static_cast<uint32_t>(static_cast<uint8_t>(src[q])) << (8 * q);
-        }
+  const int64_t CBg = ICgp / 64, CB = CBg * groups, C = groups * ICg;
+  const int64_t WB = (W + 63) / 64;
+  int64_t b = blockIdx.x;
+  const int64_t wb = b % WB;
+  b /= WB;
+  const int64_t h = b % H;
+  b /= H;
+  const int64_t cb = b % CB;
+  const int64_t n = b / CB;
+  const int64_t g = cb / CBg;
+  const int64_t cl0 = (cb - g * CBg) * 64;  // first channel of the block, within its group
+  const int64_t w0 = wb * 64;
+  const int t = threadIdx.x;
+  {
+    // load: channel r, bytes 16q .. 16q + 15 of the 64-column piece
+    const int r = t >> 2, q = t & 3;
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    if (cl0 + r < ICg) {
+      const int8_t* src = x + ((n * C + g * ICg + cl0 + r) * H + h) * W + w0 + 16 * q;
+      if (VEC && w0 + 16 * q + 16 <= W) {
+        const uint4 u = __ldcs(reinterpret_cast<const uint4*>(src));
+        v[0] = u.x;
+        v[1] = u.y;
+        v[2] = u.z;
+        v[3] = u.w;
+      } else {
+        for (int e = 0; e < 16; ++e)
+          if (w0 + 16 * q + e < W)
+            v[e >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(src[e])) << (8 * (e & 3));
       }
     }
-    uint4* out = dst + (((n * CB + cb) * H + h) * W + wb) * 8 + cseg;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (wb + q >= W) break;
-      int d[8];
+    for (int k = 0; k < 4; ++k) tile[r][4 * q + k] = v[k];
+  }
+  __syncthreads();
+  // store: column wl, channels 8 s .. 8 s + 7 (16 bytes of bf16)
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        d[j] = (cl0 + j < ICg) ? static_cast<int>(static_cast<int8_t>((raw[j] >> (8 * q)) & 0xff)) - zp
-                               : 0;
-      uint4 o;
-      o.x = bf16x2_from_ints(d[0], d[1]);
-      o.y = bf16x2_from_ints(d[2], d[3]);
-      o.z = bf16x2_from_ints(d[4], d[5]);
-      o.w = bf16x2_from_ints(d[6], d[7]);
-      out[q * 8] = o;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int wl = 32 * pass + (t >> 3), s8 = t & 7;
+    if (w0 + wl >= W) continue;
+    int d[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = 8 * s8 + j;
+      const int v = static_cast<int8_t>((tile[c][wl >> 2] >> (8 * (wl & 3))) & 0xffu);
+      d[j] = (cl0 + c < ICg) ? v - zp : 0;
     }
+    uint4 o;
+    o.x = bf16x2_from_ints(d[0], d[1]);
+    o.y = bf16x2_from_ints(d[2], d[3]);
+    o.z = bf16x2_from_ints(d[4], d[5]);
+    o.w = bf16x2_from_ints(d[6], d[7]);
+    dst[(((n * CB + cb) * H + h) * W + w0 + wl) * 8 + s8] = o;
   }
 }
 
@@ -521,20 +528,14 @@ cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t groups,
                                      int64_t H, int64_t W, int32_t zp, __nv_bfloat16* dst,
                                      int64_t ICgp, cudaStream_t s) {
   if (N * H * W == 0) return cudaSuccess;
-  const int64_t items = N * H * groups * (ICgp / 64) * 8 * ((W + 3) / 4);
-  if (items + 256 < (int64_t(1) << 31)) {
-    static int occ[64];
-    const int grid = resident_grid(nchw_to_nhwc_bf16_kernel<uint32_t>, occ, items, 256);
-    return launch_pdl(nchw_to_nhwc_bf16_kernel<uint32_t>, grid, 256, 0, s, x,
-                      static_cast<uint32_t>(N * H), groups, ICg, static_cast<uint32_t>(H), W, zp,
-                      reinterpret_cast<uint4*>(dst), ICgp);
-  } else {
-    static int occ[64];
-    const int grid = resident_grid(nchw_to_nhwc_bf16_kernel<int64_t>, occ, items, 256);
-    return launch_pdl(nchw_to_nhwc_bf16_kernel<int64_t>, grid, 256, 0, s, x, N * H, groups, ICg, H,
-                      W, zp, reinterpret_cast<uint4*>(dst), ICgp);
-  }
-  return cudaGetLastError();
+  const int64_t blocks = N * groups * (ICgp / 64) * H * ((W + 63) / 64);
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  const bool vec = (W % 16 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
+  if (vec)
+    return launch_pdl(nchw_to_nhwc_bf16_kernel<true>, static_cast<int>(blocks), 256, 0, s, x,
+                      groups, ICg, H, W, zp, reinterpret_cast<uint4*>(dst), ICgp);
+  return launch_pdl(nchw_to_nhwc_bf16_kernel<false>, static_cast<int>(blocks), 256, 0, s, x, groups,
+                    ICg, H, W, zp, reinterpret_cast<uint4*>(dst), ICgp);
 }
 
 // Convolution weight [OC, ldw] (per row: taps x ICg used) -> bf16, per group j:
