@@ -21,9 +21,11 @@ cudaError_t launch_tc_conv_t(const TcConvT& C, cudaStream_t s) {
   if (S.p.total_units == 0) return cudaSuccess;
   // one CTA per tile: on the transposed-convolution workload the 2-SM MMA
   // measured no faster (its k-blocks are short and many)
-  if (S.pixn)
+  if (S.pixn) {
+    if (S.kd != 1) return cudaErrorInvalidValue;
     return S.single ? launch_tc_kernel<kPixTile, 16, 5, 1, 1>(S.ma, S.mb, S.p, s)
                     : launch_tc_kernel<kPixTile, 16, 3, 1, 1>(S.ma, S.mb, S.p, s);
+  }
   switch (S.bn * 4 + S.kd) {
     case 64 * 4 + 1: return launch_tc_kernel<64, 16, 1, 1, 1>(S.ma, S.mb, S.p, s);
     case 64 * 4 + 2: return launch_tc_kernel<64, 16, 1, 2, 1>(S.ma, S.mb, S.p, s);

@@ -17,9 +17,11 @@ cudaError_t launch_tc_conv2d(const TcConvT& C, cudaStream_t s) {
   ConvSetup S;
   if (!conv_setup(C, S)) return cudaErrorInvalidValue;
   if (S.p.total_units == 0) return cudaSuccess;
-  if (S.pixn)
+  if (S.pixn) {
+    if (S.kd != 1) return cudaErrorInvalidValue;
     return S.single ? launch_tc_kernel<kPixTile, 16, 6, 1, 1>(S.ma, S.mb, S.p, s)
                     : launch_tc_kernel<kPixTile, 16, 4, 1, 1>(S.ma, S.mb, S.p, s);
+  }
   switch (S.bn * 4 + S.kd) {
     case 64 * 4 + 1: return launch_tc_kernel<64, 16, 2, 1, 1>(S.ma, S.mb, S.p, s);
     case 64 * 4 + 2: return launch_tc_kernel<64, 16, 2, 2, 1>(S.ma, S.mb, S.p, s);

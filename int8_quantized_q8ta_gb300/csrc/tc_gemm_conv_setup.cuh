@@ -93,10 +93,22 @@ inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
   const int bh = tile_px / bw;
   if (bw * ew > 256 || bh * eh > 256) return false;
   const uint64_t icb = static_cast<uint64_t>(C.ICp / kBK);
-  // two k-blocks (channel blocks) per TMA box when they split evenly: the
-  // 128-wide tiles need bigger boxes to keep enough bytes in flight per SM;
-  // the exchanged tiles (48 KB per k-block) measured faster with one k-block
-  // per stage (four stages) than with two (two stages)
+  // the most taps of any sub-tile
+  int max_taps = static_cast<int>(C.Kh * C.Kw);
+  if (!direct) {
+    int th = 0, tw = 0;
+    for (int ph = 0; ph < C.stride_h; ++ph)
+      th = std::max(th, conv_t_phase_taps(ph, C.pad_h, C.stride_h, C.dil_h, C.Kh));
+    for (int pw = 0; pw < C.stride_w; ++pw)
+      tw = std::max(tw, conv_t_phase_taps(pw, C.pad_w, C.stride_w, C.dil_w, C.Kw));
+    max_taps = th * tw;
+  }
+  // Two k-blocks (channel blocks) per TMA box when they split evenly: the
+  // 128-wide tiles need bigger boxes to keep enough bytes in flight per SM.
+  // The exchanged tiles (48 KB per k-block) keep one k-block per stage: four
+  // 48 KB stages measured faster than two 96 KB ones (21.2 us against 22.1
+  // us for the 8x256x64x64 transposed convolution's GEMM): the feed is bound
+  // by bytes from L2, not by the count of boxes.
   const int kd = (!pixn && icb % 2 == 0) ? 2 : 1;
   {
     // the group's channel blocks of [N][cb_total][H_in][W_in][64] bf16
@@ -157,15 +169,6 @@ inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
   p.total_units = static_cast<int>(units);
   p.subtiles = direct ? 1 : static_cast<int>(C.stride_w);
   // the most ring stages of any sub-tile (taps x channel-block stages)
-  int max_taps = static_cast<int>(C.Kh * C.Kw);
-  if (!direct) {
-    int th = 0, tw = 0;
-    for (int ph = 0; ph < C.stride_h; ++ph)
-      th = std::max(th, conv_t_phase_taps(ph, C.pad_h, C.stride_h, C.dil_h, C.Kh));
-    for (int pw = 0; pw < C.stride_w; ++pw)
-      tw = std::max(tw, conv_t_phase_taps(pw, C.pad_w, C.stride_w, C.dil_w, C.Kw));
-    max_taps = th * tw;
-  }
   p.max_nstages = max_taps * static_cast<int>((icb + kd - 1) / kd);
   if (!direct && C.stride_h <= kMaxPhases) {
     // row phases with more taps first, so the heaviest units start earliest
@@ -176,6 +179,35 @@ inline bool conv_setup(const TcConvT& C, ConvSetup& S) {
     }
     std::stable_sort(order, order + C.stride_h, [&](int x, int y) { return taps[x] > taps[y]; });
     for (int i = 0; i < C.stride_h; ++i) p.ph_order[i] = static_cast<int8_t>(order[i]);
+  }
+  p.fd_oc = make_fastdiv(static_cast<uint32_t>(p.tiles_oc));
+  p.fd_w = make_fastdiv(static_cast<uint32_t>(p.tiles_w));
+  p.fd_h = make_fastdiv(static_cast<uint32_t>(p.tiles_h));
+  p.fd_n = make_fastdiv(static_cast<uint32_t>(p.Nimg));
+  p.phase_tab = 0;
+  if (!direct && C.stride_h <= kMaxPhases && C.stride_w <= kMaxPhases) {
+    // the first tap, tap count and first-tap input offset of each phase:
+    // the least k >= 0 with k * dil = phase + pad (mod stride), k0 = ((t / g)
+    // * inv) mod ts for t = (phase + pad) mod stride when g = gcd(dil,
+    // stride) divides t (else no tap), and the input offset
+    // (phase + pad - k0 * dil) / stride, an integer by construction
+    auto fill = [](int nph, int pad, int stride, int dil, int K, int g, int ts, int inv, int* r0,
+                   int* nt, int* d0) {
+      for (int ph = 0; ph < nph; ++ph) {
+        const int t = (ph + pad) % stride;
+        r0[ph] = 0;
+        nt[ph] = 0;
+        d0[ph] = 0;
+        if (t % g != 0) continue;
+        const int k0 = static_cast<int>((static_cast<int64_t>(t / g) * inv) % ts);
+        r0[ph] = k0;
+        nt[ph] = k0 < K ? (K - k0 + ts - 1) / ts : 0;
+        d0[ph] = (ph + pad - k0 * dil) / stride;
+      }
+    };
+    fill(p.sh, p.pad_h, p.sh, p.dil_h, p.Kh, p.gh, p.tsh, p.invh, p.ph_r, p.ph_nt, p.ph_d0);
+    fill(p.sw, p.pad_w, p.sw, p.dil_w, p.Kw, p.gw, p.tsw, p.invw, p.pw_r, p.pw_nt, p.pw_d0);
+    p.phase_tab = 1;
   }
   p.ws = C.ws;
   p.bias = C.bias;

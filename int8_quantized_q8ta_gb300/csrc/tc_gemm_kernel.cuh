@@ -137,6 +137,15 @@ struct TcParams {
   int staged;        // conv output: 2 = column phases held in registers, one
                      // store per channel; 0 = one byte store per output
   int8_t ph_order[kMaxPhases];  // row phases, most taps first (stride_h <= kMaxPhases)
+  // tile decomposition without integer division: divisors of the unit index
+  FastDiv fd_oc, fd_w, fd_h, fd_n;
+  // per stride phase (phase_tab: both strides <= kMaxPhases), the first
+  // tap, the tap count and the input offset of the first tap: row phase ph
+  // (ph_r, ph_nt, ph_d0) and column phase pw (pw_r, pw_nt, pw_d0), as
+  // decode_tile would compute them
+  int phase_tab;
+  int ph_r[kMaxPhases], ph_nt[kMaxPhases], ph_d0[kMaxPhases];
+  int pw_r[kMaxPhases], pw_nt[kMaxPhases], pw_d0[kMaxPhases];
   // epilogue
   const float* ws;
   const float* bias;
@@ -209,27 +218,42 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams& p, int u, int j,
     ti.nstages = (p.kb_total + KD - 1) / KD;
   } else if constexpr (MODE == 2) {
     // direct convolution: one output tile of image n, every tap
-    ti.ocb = u % p.tiles_oc;
-    u /= p.tiles_oc;
-    ti.wb = u % p.tiles_w;
-    u /= p.tiles_w;
-    ti.hb = (u % p.tiles_h) * CG + rank;
-    ti.n = u / p.tiles_h;
+    uint32_t q, r;
+    fast_divmod(static_cast<uint32_t>(u), p.fd_oc, q, r);
+    ti.ocb = static_cast<int>(r);
+    fast_divmod(q, p.fd_w, q, r);
+    ti.wb = static_cast<int>(r);
+    fast_divmod(q, p.fd_h, q, r);
+    ti.hb = static_cast<int>(r) * CG + rank;
+    ti.n = static_cast<int>(q);
     ti.nth = p.Kh;
     ti.ntw = p.Kw;
     ti.num_kb = p.Kh * p.Kw * p.icb;
     ti.nstages = p.Kh * p.Kw * ((p.icb + KD - 1) / KD);
   } else {
-    ti.ocb = u % p.tiles_oc;
-    u /= p.tiles_oc;
-    ti.wb = u % p.tiles_w;
-    u /= p.tiles_w;
-    ti.hb = (u % p.tiles_h) * CG + rank;
-    u /= p.tiles_h;
-    ti.n = u % p.Nimg;
-    const int phx = u / p.Nimg;
+    uint32_t q, r;
+    fast_divmod(static_cast<uint32_t>(u), p.fd_oc, q, r);
+    ti.ocb = static_cast<int>(r);
+    fast_divmod(q, p.fd_w, q, r);
+    ti.wb = static_cast<int>(r);
+    fast_divmod(q, p.fd_h, q, r);
+    ti.hb = static_cast<int>(r) * CG + rank;
+    fast_divmod(q, p.fd_n, q, r);
+    ti.n = static_cast<int>(r);
+    const int phx = static_cast<int>(q);
     ti.ph = (p.sh <= kMaxPhases) ? p.ph_order[phx] : phx;
     ti.pw = j;
+    if (p.phase_tab) {
+      ti.rh = p.ph_r[ti.ph];
+      ti.nth = p.ph_nt[ti.ph];
+      ti.dh0 = p.ph_d0[ti.ph];
+      ti.rw = p.pw_r[j];
+      ti.ntw = p.pw_nt[j];
+      ti.dw0 = p.pw_d0[j];
+      ti.num_kb = ti.nth * ti.ntw * p.icb;
+      ti.nstages = ti.nth * ti.ntw * ((p.icb + KD - 1) / KD);
+      return ti;
+    }
     // first taps: the least kh >= 0 with kh * dil_h = ph + pad_h (mod sh), if any
     const int th0 = (ti.ph + p.pad_h) % p.sh, tw0 = (ti.pw + p.pad_w) % p.sw;
     ti.nth = 0;
@@ -595,6 +619,40 @@ __device__ __forceinline__ void pix_store16(const TcParams& p, const TileInfo& t
             static_cast<int8_t>(requant_f(f[i], ws, b, p.rq));
     }
   }
+}
+
+// The single-chunk kernels' form of pix_store16: with stride 2 the two
+// column phases of a unit meet in registers instead of in the output.
+// Phase 0 keeps its four packed words of group G in ph0[4G .. 4G + 3] and
+// stores nothing; phase 1 (the same thread, next sub-tile) interleaves them
+// with its own bytes and writes whole sectors once.  (G is a compile-time
+// index, so ph0 stays in registers.)
+template <int kCols, int G>
+__device__ __forceinline__ void pix_store16_reg(const TcParams& p, const TileInfo& ti,
+                                                const PixRun& r, int col0, const float (&f)[16],
+                                                float ws, float b, uint32_t (&hold)[4],
+                                                uint32_t (&ph0)[kCols / 4]) {
+  if (r.vec && p.osw == 2) {
+    uint32_t q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      q[k] = rq_pack4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3], ws, b, p.rq);
+    if (ti.pw == 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ph0[4 * G + k] = q[k];
+      return;
+    }
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[2 * k] = __byte_perm(ph0[4 * G + k], q[k], 0x5140);
+      w[2 * k + 1] = __byte_perm(ph0[4 * G + k], q[k], 0x7362);
+    }
+    st_global_v8(r.dst + 32 * G, w);
+    return;
+  }
+  const uint32_t e[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // (no stride-2 sector merge here)
+  pix_store16<kCols>(p, ti, r, col0, G, f, ws, b, hold, e);
 }
 
 // The sector that phase 0 of a stride-2 unit wrote for group g (read before
@@ -1000,6 +1058,9 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
       // phases, four output channels per word
       constexpr int kHeld = (MODE != 0 && !kPixN && kColsPerWarp <= 64) ? kColsPerWarp / 4 : 1;
       uint32_t held[kHeld];
+      // single-chunk exchanged kernels: phase 0's packed bytes (see pix_store16_reg)
+      constexpr int kPh0 = (kPixN && kSingleOnly) ? kColsPerWarp / 4 : 4;
+      uint32_t ph0[kPh0];
       for (int j = 0; j < p.subtiles && ok; ++j) {
         const TileInfo ti = decode_tile<CM, CG, KD>(p, u, j, rank);
         if constexpr (kPixN) {
@@ -1031,6 +1092,38 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
               tc_fence_after();
             }
             uint32_t hold[4] = {0u, 0u, 0u, 0u};
+            if constexpr (kSingleOnly) {
+              // groups unrolled, so ph0 stays in registers
+              static_assert(!kSingleOnly || kColsPerWarp == 64, "four 16-column groups per thread");
+              uint32_t r[1][16];
+              const uint32_t taddr = tmem_base + lane_addr + buf * kAccStride + col0;
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                if (nchunks == 1) {
+                  tmem_ld_16cols(taddr + 16 * g, r[0]);
+                  tmem_ld_wait();
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) r[0][i] = 0u;
+                }
+                if (mine) {
+                  if (p.acc_out != nullptr) {
+                    int32_t a[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) a[i] = __float2int_rn(__uint_as_float(r[0][i]));
+                    pix_store16_acc(p, ti, run, col0, g, a);
+                  } else {
+                    float fv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) fv[i] = __uint_as_float(r[0][i]);
+                    if (g == 0) pix_store16_reg<kColsPerWarp, 0>(p, ti, run, col0, fv, px_ws, px_b, hold, ph0);
+                    if (g == 1) pix_store16_reg<kColsPerWarp, 1>(p, ti, run, col0, fv, px_ws, px_b, hold, ph0);
+                    if (g == 2) pix_store16_reg<kColsPerWarp, 2>(p, ti, run, col0, fv, px_ws, px_b, hold, ph0);
+                    if (g == 3) pix_store16_reg<kColsPerWarp, 3>(p, ti, run, col0, fv, px_ws, px_b, hold, ph0);
+                  }
+                }
+              }
+            } else
 #pragma unroll 1
             for (int g = 0; g < kColsPerWarp / 16; ++g) {
               uint32_t e[8];
