@@ -469,15 +469,17 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc_bf16_kernel(const int8_t* __
   pdl_wait();
   pdl_launch_dependents();
   const int64_t CBg = ICgp / 64, CB = CBg * groups, C = groups * ICg;
-  const int64_t WB = (W + 63) / 64;
-  int64_t b = blockIdx.x;
+  // the block index in 32 bits (the launch checks it fits): 32-bit division
+  // is a short sequence, 64-bit division a long one
+  const uint32_t WB = static_cast<uint32_t>((W + 63) / 64);
+  uint32_t b = blockIdx.x;
   const int64_t wb = b % WB;
   b /= WB;
-  const int64_t h = b % H;
-  b /= H;
-  const int64_t cb = b % CB;
-  const int64_t n = b / CB;
-  const int64_t g = cb / CBg;
+  const int64_t h = b % static_cast<uint32_t>(H);
+  b /= static_cast<uint32_t>(H);
+  const int64_t cb = b % static_cast<uint32_t>(CB);
+  const int64_t n = b / static_cast<uint32_t>(CB);
+  const int64_t g = static_cast<uint32_t>(cb) / static_cast<uint32_t>(CBg);
   const int64_t cl0 = (cb - g * CBg) * 64;  // first channel of the block, within its group
   const int64_t w0 = wb * 64;
   const int t = threadIdx.x;
