@@ -353,7 +353,8 @@ cudaError_t launch_rows_to_bf16(const int8_t* src, int64_t rows, int64_t K, int6
 template <int U, typename Idx>
 __global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
     const float* __restrict__ x, Idx rows, Idx K, float inv, int32_t zp,
-    int8_t* __restrict__ xq, uint4* __restrict__ dst, Idx Kp, int32_t* bound_word) {
+    int8_t* __restrict__ xq, uint4* __restrict__ dst, Idx Kp, int32_t* bound_word,
+    FastDiv fd_row) {
   pdl_wait();
   pdl_launch_dependents();
   if (bound_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
@@ -371,7 +372,12 @@ __global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const Idx i = base + static_cast<Idx>(u) * blockDim.x;
-      rr[u] = i / per_row;
+      // the row of item i: a multiply-shift division in 32 bits (fd_row
+      // divides by per_row), a plain one in 64
+      if constexpr (sizeof(Idx) == 4)
+        rr[u] = static_cast<Idx>(fast_div(static_cast<uint32_t>(i), fd_row));
+      else
+        rr[u] = i / per_row;
       kk[u] = (i - rr[u] * per_row) * 8;
       if (vec && i < total && kk[u] + 8 <= K) {
         const float4* xp = reinterpret_cast<const float4*>(x + static_cast<int64_t>(rr[u]) * K + kk[u]);
@@ -433,12 +439,13 @@ cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, f
     const int grid = resident_grid(quantize_rows_bf16_kernel<U, uint32_t>, occ, (items + U - 1) / U, 256);
     return launch_pdl(quantize_rows_bf16_kernel<U, uint32_t>, grid, 256, 0, s, x,
                       static_cast<uint32_t>(rows), static_cast<uint32_t>(K), inv, zp, xq,
-                      reinterpret_cast<uint4*>(dst), static_cast<uint32_t>(Kp), bound_word);
+                      reinterpret_cast<uint4*>(dst), static_cast<uint32_t>(Kp), bound_word,
+                      make_fastdiv(static_cast<uint32_t>(Kp / 8)));
   } else {
     static int occ[64];
     const int grid = resident_grid(quantize_rows_bf16_kernel<U, int64_t>, occ, (items + U - 1) / U, 256);
     return launch_pdl(quantize_rows_bf16_kernel<U, int64_t>, grid, 256, 0, s, x, rows, K, inv, zp,
-                      xq, reinterpret_cast<uint4*>(dst), Kp, bound_word);
+                      xq, reinterpret_cast<uint4*>(dst), Kp, bound_word, FastDiv{1u, 0u, 0u, 0u});
   }
   return cudaGetLastError();
 }
