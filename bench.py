@@ -180,6 +180,9 @@ class Path:
         self.operand = q8.operand_buffer(LM, LK, dev)
         self.l_out = torch.empty((LM, LN), dtype=torch.int8, device=dev)
         self.gx, self.gw = T(h["gx"]), T(h["gw"])
+        # the gemv weight is packed once too (a copy the library never sees
+        # written again, so each call reads it before the previous kernel ends)
+        self.g_packed = q8.pack_gemv_weight(self.gw)
         self.gws, self.gb = T(h["gws"]), T(h["gb"])
         self.g_out = torch.empty((1, GN), dtype=torch.int8, device=dev)
         self.cx, self.cw = T(h["cx"]), T(h["cw"])
@@ -221,8 +224,8 @@ class Path:
             q8.linear_operand_packed(self.operand, lp["in_scale"], self.packed, self.lws, self.lb,
                                      lp["out_scale"], lp["out_zp"], out=self.l_out)
         elif name == "gemv":
-            q8.linear_gemv(self.gx, gp["in_scale"], gp["in_zp"], self.gw, None, self.gws, self.gb,
-                           gp["out_scale"], gp["out_zp"], out=self.g_out)
+            q8.linear_gemv_packed(self.gx, gp["in_scale"], gp["in_zp"], self.g_packed, self.gws,
+                                  self.gb, gp["out_scale"], gp["out_zp"], out=self.g_out)
         else:
             q8.conv2d_transposed_packed(self.cx, cp["in_scale"], cp["in_zp"], self.c_packed,
                                         self.cws, self.cb, cp["out_scale"], cp["out_zp"],
@@ -251,7 +254,7 @@ GEMV_CHAIN_COPIES = 24   # 24 x 16.8 MB of weights: 403 MB, more than 3x the 129
 GEMV_CHAIN_REPS = 20
 
 
-def gemv_chain_measure(path, copies=GEMV_CHAIN_COPIES, reps=GEMV_CHAIN_REPS):
+def gemv_chain_measure(path, copies=GEMV_CHAIN_COPIES, reps=GEMV_CHAIN_REPS, packed=True):
     """q8ta_linear_gemv as a decode step runs it: `copies` gemvs back to back,
     each on its own weight (like successive layers), no event or host work
     between them, captured once in a CUDA graph (so the host's per-call cost
@@ -261,13 +264,20 @@ def gemv_chain_measure(path, copies=GEMV_CHAIN_COPIES, reps=GEMV_CHAIN_REPS):
     call's output equals the lone call's (same x, same weight values)."""
     torch, q8 = path.torch, path.q8
     gp = G.params
-    weights = [path.gw.clone() for _ in range(copies)]
+    if packed:
+        weights = [q8.pack_gemv_weight(path.gw) for _ in range(copies)]
+    else:
+        weights = [path.gw.clone() for _ in range(copies)]
     outs = [torch.empty((1, GN), dtype=torch.int8, device=path.dev) for _ in range(copies)]
 
     def chain():
         for i in range(copies):
-            q8.linear_gemv(path.gx, gp["in_scale"], gp["in_zp"], weights[i], None, path.gws,
-                           path.gb, gp["out_scale"], gp["out_zp"], out=outs[i])
+            if packed:
+                q8.linear_gemv_packed(path.gx, gp["in_scale"], gp["in_zp"], weights[i], path.gws,
+                                      path.gb, gp["out_scale"], gp["out_zp"], out=outs[i])
+            else:
+                q8.linear_gemv(path.gx, gp["in_scale"], gp["in_zp"], weights[i], None, path.gws,
+                               path.gb, gp["out_scale"], gp["out_zp"], out=outs[i])
 
     for _ in range(2):
         chain()
@@ -643,6 +653,7 @@ def run_ours(args, rank, world, local_rank):
     chained = args.only in ("all", "gemv") and not args.no_extra_ops
     if chained:
         chain_us, chain_graph = gemv_chain_measure(path)
+        plain_us, _ = gemv_chain_measure(path, packed=False)
     if args.only == "all" and not args.no_extra_ops:
         extra_ops = small_configs_measure(dev)
         ab = fused_chain_ab(path)
@@ -670,7 +681,7 @@ def run_ours(args, rank, world, local_rank):
         "q8ta_linear_gemv_1x4096x4096": {
             "us": us["gemv"], "GB/s": BYTES_GEMV / us["gemv"] / 1e3,
             "frac_hbm": BYTES_GEMV / us["gemv"] / 1e3 / hbm,
-            "note": "one launch bracketed by events inside the step pass (its launch and "
+            "note": "q8_linear_gemv_packed, one launch bracketed by events inside the step pass (its launch and "
                     "DRAM ramp are not overlapped)"},
         "q8ta_conv2d_transposed_8x256x64x64": {
             "us": us["conv_t"], "outputs/s": CONV_OUTPUTS / us["conv_t"] * 1e6,
@@ -680,7 +691,8 @@ def run_ours(args, rank, world, local_rank):
         ops["q8ta_linear_gemv_1x4096x4096_chained"] = {
             "us_per_call": chain_us, "GB/s": BYTES_GEMV / chain_us / 1e3,
             "frac_hbm": BYTES_GEMV / chain_us / 1e3 / hbm,
-            "method": f"{GEMV_CHAIN_COPIES} calls back to back on distinct weight copies "
+            "us_per_call_unpacked_weight": plain_us,
+            "method": f"{GEMV_CHAIN_COPIES} calls back to back on distinct packed weight copies "
                       f"({GEMV_CHAIN_COPIES * GN * GK / 1e6:.0f} MB, > 2x L2), "
                       f"{'one CUDA graph' if chain_graph else 'eager launches'} replayed "
                       f"{GEMV_CHAIN_REPS}x; events only around the replays"}

@@ -194,6 +194,27 @@ q8_status q8_linear_gemv(const int8_t* x, int64_t M, int64_t K, double input_sca
                          size_t workspace_bytes, q8_stream_t stream);
 
 /*
+ * The gemv from a packed weight (decode-shaped layers, whose weights are
+ * constants): q8_linear_gemv_pack_weight copies the int8 [N, K] weight into
+ * `packed` (q8_linear_gemv_packed_weight_bytes(N, K) bytes, 256-byte
+ * aligned, owned by the caller) and waits for the copy (load time).  A packed
+ * buffer is rewritten only by packing into it again.  q8_linear_gemv_packed
+ * then computes exactly what q8_linear_gemv computes, but reads its first
+ * 4 KB of each weight row before waiting for the previous kernel on the
+ * stream (which never writes a packed weight), so that in a run of layers
+ * each layer's weight streams in while the previous layer runs.  x is int8
+ * [1, K].  Guards: those of q8_linear_gemv.
+ */
+size_t q8_linear_gemv_packed_weight_bytes(int64_t N, int64_t K);
+q8_status q8_linear_gemv_pack_weight(const int8_t* weight, int64_t N, int64_t K, void* packed,
+                                     size_t packed_bytes, q8_stream_t stream);
+q8_status q8_linear_gemv_packed(const int8_t* x, int64_t K, double input_scale,
+                                int32_t input_zero_point, const void* packed_weight, int64_t N,
+                                const float* weight_scales, const float* bias, double output_scale,
+                                int32_t output_zero_point, const char* activation, int8_t* out,
+                                q8_stream_t stream);
+
+/*
  * Load-time weight packing.  A linear layer's weight is a constant, so the
  * bf16 copy the tensor cores read can be made once:
  *   q8_linear_pack_weight writes q8_linear_packed_weight_bytes(N, K) bytes

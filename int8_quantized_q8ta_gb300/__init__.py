@@ -29,6 +29,7 @@ EXPORTS = (
     "q8_status_string", "q8_version", "q8_device_error",
     "q8_quantize_per_tensor", "q8_dequantize_per_tensor",
     "q8_linear_workspace_bytes", "q8_linear", "q8_linear_noalloc", "q8_linear_gemv",
+    "q8_linear_gemv_packed_weight_bytes", "q8_linear_gemv_pack_weight", "q8_linear_gemv_packed",
     "q8_linear_packed_weight_bytes", "q8_linear_pack_weight",
     "q8_linear_operand_bytes", "q8_linear_prepare_operand", "q8_quantize_to_linear_operand",
     "q8_linear_operand_packed", "q8_linear_packed", "q8_quantize_linear_packed",
@@ -88,6 +89,9 @@ def _load() -> ctypes.CDLL:
                                           P]),
         "q8_linear_noalloc": (ctypes.c_int, [P, I64, I64, D, I32, P, I64, P, P, P, D, I32, C, P,
                                              P]),
+        "q8_linear_gemv_packed_weight_bytes": (S, [I64, I64]),
+        "q8_linear_gemv_pack_weight": (ctypes.c_int, [P, I64, I64, P, S, P]),
+        "q8_linear_gemv_packed": (ctypes.c_int, [P, I64, D, I32, P, I64, P, P, D, I32, C, P, P]),
         "q8_linear_packed_weight_bytes": (S, [I64, I64]),
         "q8_linear_pack_weight": (ctypes.c_int, [P, I64, I64, P, S, P]),
         "q8_linear_operand_bytes": (S, [I64, I64]),
@@ -281,6 +285,44 @@ def pack_weight(weight: torch.Tensor) -> PackedWeight:
     _check(_lib.q8_linear_pack_weight(_ptr(weight), N, K, _ptr(buf), nbytes, _stream(weight)),
            "q8_linear_pack_weight")
     return PackedWeight(buf, N, K)
+
+
+@dataclasses.dataclass
+class PackedGemvWeight:
+    """A q8ta_linear_gemv weight packed once at load time (see
+    q8_linear_gemv_pack_weight): ``data`` is a uint8 CUDA buffer."""
+    data: torch.Tensor
+    N: int
+    K: int
+
+
+def pack_gemv_weight(weight: torch.Tensor) -> PackedGemvWeight:
+    _need(weight, torch.int8, "weight")
+    N, K = weight.shape
+    nbytes = _lib.q8_linear_gemv_packed_weight_bytes(N, K)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=weight.device)
+    _check(_lib.q8_linear_gemv_pack_weight(_ptr(weight), N, K, _ptr(buf), nbytes,
+                                           _stream(weight)), "q8_linear_gemv_pack_weight")
+    return PackedGemvWeight(buf, N, K)
+
+
+def linear_gemv_packed(x, input_scale, input_zero_point, packed: PackedGemvWeight, weight_scales,
+                       bias, output_scale, output_zero_point, activation="none", out=None):
+    """q8ta_linear_gemv (M == 1) from a packed weight."""
+    _need(x, torch.int8, "x")
+    _need(weight_scales, torch.float32, "weight_scales")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    if x.numel() != packed.K:
+        raise ValueError(f"x has {x.numel()} elements, the packed weight K={packed.K}")
+    out = torch.empty((1, packed.N), dtype=torch.int8, device=x.device) if out is None else out
+    _need(out, torch.int8, "out")
+    _check(_lib.q8_linear_gemv_packed(_ptr(x), packed.K, float(input_scale),
+                                      int(input_zero_point), _ptr(packed.data), packed.N,
+                                      _ptr(weight_scales), _ptr(bias), float(output_scale),
+                                      int(output_zero_point), activation.encode(), _ptr(out),
+                                      _stream(x)), "q8_linear_gemv_packed")
+    return out
 
 
 def linear_packed(x, input_scale, input_zero_point, packed: PackedWeight, weight_scales, bias,

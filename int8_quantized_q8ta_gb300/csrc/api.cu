@@ -139,6 +139,41 @@ q8_status q8_linear_gemv(const int8_t* x, int64_t M, int64_t K, double input_sca
                                      out, cs(stream)));
 }
 
+size_t q8_linear_gemv_packed_weight_bytes(int64_t N, int64_t K) {
+  if (N < 1 || K < 1 || !mul_ok(N, K)) return 0;
+  return align_ws(static_cast<size_t>(N) * static_cast<size_t>(K));
+}
+
+q8_status q8_linear_gemv_pack_weight(const int8_t* weight, int64_t N, int64_t K, void* packed,
+                                     size_t packed_bytes, q8_stream_t stream) {
+  if (!weight || !packed) return Q8_ERR_NULL;
+  if (N < 1 || K < 1 || !mul_ok(N, K) || N > INT32_MAX || K > INT32_MAX / 2) return Q8_ERR_SHAPE;
+  if (packed_bytes < q8_linear_gemv_packed_weight_bytes(N, K)) return Q8_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(packed) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
+  // a copy of the row-major int8 weight, finished before this call returns,
+  // so that no kernel launched later ever sees it being written
+  cudaError_t e = cudaMemcpyAsync(packed, weight, static_cast<size_t>(N) * static_cast<size_t>(K),
+                                  cudaMemcpyDeviceToDevice, cs(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs(stream));
+  return cuda_status(e);
+}
+
+q8_status q8_linear_gemv_packed(const int8_t* x, int64_t K, double input_scale,
+                                int32_t input_zero_point, const void* packed_weight, int64_t N,
+                                const float* weight_scales, const float* bias, double output_scale,
+                                int32_t output_zero_point, const char* activation, int8_t* out,
+                                q8_stream_t stream) {
+  int relu = 0;
+  q8_status st = check_linear(x, 1, K, input_scale, input_zero_point, packed_weight, N,
+                              weight_scales, output_scale, output_zero_point, activation, out,
+                              &relu);
+  if (st != Q8_OK) return st;
+  if (reinterpret_cast<uintptr_t>(packed_weight) % q8::kWorkspaceAlign != 0) return Q8_ERR_ALIGN;
+  return cuda_status(q8::launch_gemv_packed(
+      x, K, input_zero_point, static_cast<const int8_t*>(packed_weight), N, weight_scales, bias,
+      make_rq(input_scale, output_scale, output_zero_point, relu), out, cs(stream)));
+}
+
 q8_status q8_linear(const int8_t* x, int64_t M, int64_t K, double input_scale,
                     int32_t input_zero_point, const int8_t* weight, int64_t N,
                     const int32_t* weight_sums, const float* weight_scales, const float* bias,

@@ -49,6 +49,13 @@ cudaError_t launch_dequantize(const int8_t* q, int64_t numel, float scale, float
 cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w, int64_t N,
                         const float* ws, const float* bias, Requant rq, int8_t* out,
                         cudaStream_t s);
+// The gemv from a packed weight: reads its first round of weights before
+// waiting for the previous kernel (a packed weight is never written by a
+// kernel that may still be running); falls back to launch_gemv when the
+// 16-byte path does not apply.
+cudaError_t launch_gemv_packed(const int8_t* x, int64_t K, int32_t izp, const int8_t* w, int64_t N,
+                               const float* ws, const float* bias, Requant rq, int8_t* out,
+                               cudaStream_t s);
 // dst[r, k] = bf16(src[r*ld + k] - zp) for k < K, 0 for K <= k < Kp.
 // When bound_word is non-null, one thread also stores there the largest
 // |x - zp| an int8 x can give, max(128 + zp, 127 - zp): the operand's bound

@@ -291,6 +291,110 @@ cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w
                     out);
 }
 
+// q8ta_linear_gemv from a packed (load-time) weight.  A packed weight is
+// written once, by q8_linear_gemv_pack_weight, which waits for its copy to
+// finish, and is never written again except by packing into it again; so
+// no kernel that may still be running writes it, and this kernel reads its
+// first round of weights (8 x 16 bytes per lane, 4 KB of the warp's row)
+// and sums them BEFORE waiting for the previous kernel on the stream.  After
+// the wait only x (and, for K > 4096, the further rounds) remain to be
+// read.  K % 16 == 0 with 16-byte aligned x and weight (the host picks the
+// plain kernel otherwise).
+__global__ void __launch_bounds__(128) gemv_packed_kernel(const int8_t* __restrict__ x, int K,
+                                                          int32_t izp,
+                                                          const int8_t* __restrict__ w, int N,
+                                                          const float* __restrict__ ws,
+                                                          const float* __restrict__ bias,
+                                                          Requant rq, int8_t* __restrict__ out) {
+  constexpr int UNR = 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 4 + warp;
+  const int nv = K / 16;
+  if (threadIdx.x == 0 && nv > 32 * UNR) {
+    // the rounds after the first: into L2 now
+    const int n0 = blockIdx.x * 4;
+    const uint32_t bytes = static_cast<uint32_t>(min(4, N - n0)) * static_cast<uint32_t>(K);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(w + static_cast<int64_t>(n0) * K),
+                 "r"(bytes)
+                 : "memory");
+  }
+  const int4* w4 = reinterpret_cast<const int4*>(w + static_cast<int64_t>(n < N ? n : 0) * K);
+  int4 wv[UNR];
+  int dot = 0, wsum = 0;
+#pragma unroll
+  for (int u = 0; u < UNR; ++u) {
+    const int idx = lane + 32 * u;
+    wv[u] = (n < N && idx < nv) ? __ldcs(w4 + idx) : make_int4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int u = 0; u < UNR; ++u) {
+    wsum = __dp4a(wv[u].x, 0x01010101, wsum);
+    wsum = __dp4a(wv[u].y, 0x01010101, wsum);
+    wsum = __dp4a(wv[u].z, 0x01010101, wsum);
+    wsum = __dp4a(wv[u].w, 0x01010101, wsum);
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  if (n >= N) return;
+  float wsn = 0.0f, bn = 0.0f;
+  if (lane == 0) {
+    wsn = __ldg(ws + n);
+    bn = bias ? __ldg(bias + n) : 0.0f;
+  }
+  const int4* x4 = reinterpret_cast<const int4*>(x);
+#pragma unroll
+  for (int u = 0; u < UNR; ++u) {
+    const int idx = lane + 32 * u;
+    if (idx < nv) {
+      const int4 xv = __ldg(x4 + idx);
+      dot = __dp4a(wv[u].x, xv.x, dot);
+      dot = __dp4a(wv[u].y, xv.y, dot);
+      dot = __dp4a(wv[u].z, xv.z, dot);
+      dot = __dp4a(wv[u].w, xv.w, dot);
+    }
+  }
+  for (int base = 32 * UNR; base < nv; base += 32 * UNR) {
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int idx = base + lane + 32 * u;
+      wv[u] = idx < nv ? __ldcs(w4 + idx) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int idx = base + lane + 32 * u;
+      if (idx < nv) {
+        const int4 xv = __ldg(x4 + idx);
+        dp4a_acc<true>(wv[u].x, xv.x, dot, wsum);
+        dp4a_acc<true>(wv[u].y, xv.y, dot, wsum);
+        dp4a_acc<true>(wv[u].z, xv.z, dot, wsum);
+        dp4a_acc<true>(wv[u].w, xv.w, dot, wsum);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    dot = static_cast<int>(static_cast<uint32_t>(dot) +
+                           static_cast<uint32_t>(__shfl_xor_sync(0xffffffffu, dot, o)));
+    wsum = static_cast<int>(static_cast<uint32_t>(wsum) +
+                            static_cast<uint32_t>(__shfl_xor_sync(0xffffffffu, wsum, o)));
+  }
+  if (lane == 0) {
+    const int32_t acc = static_cast<int32_t>(static_cast<uint32_t>(dot) -
+                                             static_cast<uint32_t>(izp) * static_cast<uint32_t>(wsum));
+    out[n] = requant_one(acc, wsn, bn, rq);
+  }
+}
+
+cudaError_t launch_gemv_packed(const int8_t* x, int64_t K, int32_t izp, const int8_t* w, int64_t N,
+                               const float* ws, const float* bias, Requant rq, int8_t* out,
+                               cudaStream_t s) {
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(w);
+  if (!(xa % 16 == 0 && wa % 16 == 0 && K % 16 == 0))
+    return launch_gemv(x, K, izp, w, N, ws, bias, rq, out, s);
+  return launch_pdl(gemv_packed_kernel, static_cast<int>((N + 3) / 4), 128, 0, s, x, (int)K, izp, w,
+                    (int)N, ws, bias, rq, out);
+}
+
 // ---------------------------------------------------------------------------
 // Operand preparation for the tensor-core GEMM.  int8 values, and the
 // differences x - zp in [-255, 255], are exact in bf16 (8 significant bits).

@@ -205,3 +205,29 @@ def test_packed_acc32_guards():
     bad = q8.conv_t_shape((1, 64, 8, 8), (96, 9 * 64), 3, 3, 16, 14, 2, 1, 1)   # W_out % 4
     assert lib.q8_conv2d_transposed_packed_acc32(FAKE, ctypes.byref(bad), 0, FAKE, FAKE, FAKE,
                                                  need_t, None) == q8.Q8_ERR_SHAPE
+
+
+def test_gemv_packed_guards():
+    assert lib.q8_linear_gemv_packed_weight_bytes(0, 64) == 0
+    assert lib.q8_linear_gemv_packed_weight_bytes(4, 64) == 256
+    assert lib.q8_linear_gemv_packed_weight_bytes(1000, 4100) == 4100000 + 96  # up to 256
+    pack = lib.q8_linear_gemv_pack_weight
+    assert pack(None, 4, 64, FAKE, 256, None) == q8.Q8_ERR_NULL
+    assert pack(FAKE, 0, 64, FAKE, 256, None) == q8.Q8_ERR_SHAPE
+    assert pack(FAKE, 4, 64, FAKE, 255, None) == q8.Q8_ERR_WORKSPACE
+    assert pack(FAKE, 4, 64, ctypes.c_void_p(0x10010), 256, None) == q8.Q8_ERR_ALIGN
+    g = lib.q8_linear_gemv_packed
+    ok = dict(x=FAKE, K=64, s_in=0.02, izp=0, w=FAKE, N=32, ws=FAKE, s_out=0.05, ozp=0,
+              act=b"none", out=FAKE)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return g(a["x"], a["K"], a["s_in"], a["izp"], a["w"], a["N"], a["ws"], None, a["s_out"],
+                 a["ozp"], a["act"], a["out"], None)
+    assert call(x=None) == q8.Q8_ERR_NULL
+    assert call(ws=None) == q8.Q8_ERR_NULL
+    assert call(N=30) == q8.Q8_ERR_SHAPE                       # N % 4
+    assert call(K=0) == q8.Q8_ERR_SHAPE
+    assert call(act=b"gelu") == q8.Q8_ERR_UNSUPPORTED
+    assert call(izp=200) == q8.Q8_ERR_ARG
+    assert call(w=ctypes.c_void_p(0x10010)) == q8.Q8_ERR_ALIGN  # packed buffers are 256-aligned

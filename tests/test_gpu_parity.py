@@ -106,6 +106,45 @@ def test_gemv_ragged(K, N, izp):
     np.testing.assert_array_equal(got_nb, oracle.linear(x, 0.02, izp, w, ws, None, 0.07, -2))
 
 
+# The gemv from a packed weight (its first 4 KB of each row read before the
+# launch dependency wait): K % 16 == 0 up to one round, several rounds
+# (K > 4096), and K % 16 != 0 (the host falls back to the plain kernel).
+@pytest.mark.parametrize("K,N,izp", [(16, 4, 0), (4096, 4096, 0), (64, 36, 127), (1028, 40, 3),
+                                     (4096 + 16, 8, -7), (8192, 20, -100), (16384, 12, 127),
+                                     (2048, 1004, 3), (100, 12, 5)])
+def test_gemv_packed_matches_oracle(K, N, izp):
+    p = dict(ws_lo=0.002, ws_hi=0.01, b_mean=0.0, b_var=0.1)
+    x, w, ws, b = synth.linear_inputs(2 * K + N, 1, K, N, x_kind="int8", p=p)
+    packed = q8.pack_gemv_weight(T(w))
+    got = H(q8.linear_gemv_packed(T(x), 0.02, izp, packed, T(ws), T(b), 0.07, -2))
+    np.testing.assert_array_equal(got, oracle.linear(x, 0.02, izp, w, ws, b, 0.07, -2))
+    got = H(q8.linear_gemv_packed(T(x), 0.02, izp, packed, T(ws), None, 0.07, -2,
+                                  activation="relu"))
+    np.testing.assert_array_equal(got, oracle.linear(x, 0.02, izp, w, ws, None, 0.07, -2,
+                                                     activation="relu"))
+
+
+def test_gemv_packed_chain_of_layers():
+    """Layers back to back with no host sync, each reading the previous
+    layer's output as its input (the decode pattern the early weight read
+    serves): every layer's output equals the oracle's chain."""
+    K = N = 1024
+    p = dict(ws_lo=0.002, ws_hi=0.01, b_mean=0.0, b_var=0.1)
+    x0 = synth.int8_uniform(90, "cx", (1, K), -128, 127)
+    layers = [synth.linear_inputs(91 + i, 1, K, N, x_kind="int8", p=p)[1:] for i in range(6)]
+    packs = [(q8.pack_gemv_weight(T(w)), T(ws), T(b)) for w, ws, b in layers]
+    xt = T(x0)
+    outs = []
+    for pk, ws, b in packs:
+        xt = q8.linear_gemv_packed(xt, 0.05, 1, pk, ws, b, 0.05, 1)
+        outs.append(xt)
+    torch.cuda.synchronize()
+    x = x0
+    for (w, ws, b), o in zip(layers, outs):
+        x = oracle.linear(x, 0.05, 1, w, ws, b, 0.05, 1)
+        np.testing.assert_array_equal(o.cpu().numpy(), x)
+
+
 # --------------------------------------------------------------- linear
 
 # The last three rows pick the 224-, 240- and 256-column pair tiles on a
