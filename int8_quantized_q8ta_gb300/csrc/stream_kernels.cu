@@ -391,6 +391,10 @@ cudaError_t launch_gemv_packed(const int8_t* x, int64_t K, int32_t izp, const in
   const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(w);
   if (!(xa % 16 == 0 && wa % 16 == 0 && K % 16 == 0))
     return launch_gemv(x, K, izp, w, N, ws, bias, rq, out, s);
+  // (A variant staging the rows in shared memory through bulk copies, which
+  // holds no registers while it waits and so keeps more calls resident,
+  // measured 4.07 us per call in a chain of 24 against 3.76 us for this one:
+  // more calls' loads in flight delay the one that runs.)
   return launch_pdl(gemv_packed_kernel, static_cast<int>((N + 3) / 4), 128, 0, s, x, (int)K, izp, w,
                     (int)N, ws, bias, rq, out);
 }
