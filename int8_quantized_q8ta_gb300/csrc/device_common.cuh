@@ -8,6 +8,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "fastdiv.h"
+
 namespace q8 {
 
 // ---------------------------------------------------------------------------
@@ -84,41 +86,6 @@ __device__ __forceinline__ int32_t requant_i(int32_t acc, float ws, float b, con
 
 __device__ __forceinline__ int8_t requant_one(int32_t acc, float ws, float b, const Requant& rq) {
   return static_cast<int8_t>(requant_i(acc, ws, b, rq));
-}
-
-// Division of 32-bit unsigned integers by a divisor fixed for a launch, by
-// one multiply-high and two shifts: the method of Granlund and Montgomery,
-// "Division by Invariant Integers using Multiplication" (PLDI 1994),
-// Figure 4.1.  For d >= 2, with l = ceil(log2 d) and m = floor(2^32 (2^l - d)
-// / d) + 1, the quotient of any 32-bit n is (t + ((n - t) >> 1)) >> (l - 1),
-// t = umulhi(m, n); d = 1 is m = 0 and both shifts 0.
-struct FastDiv {
-  uint32_t d, m, s1, s2;
-};
-
-inline FastDiv make_fastdiv(uint32_t d) {
-  FastDiv f{d, 0u, 0u, 0u};
-  if (d <= 1) {
-    f.d = 1;
-    return f;
-  }
-  uint32_t l = 0;
-  while ((uint64_t{1} << l) < d) ++l;
-  f.m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1);
-  f.s1 = 1;
-  f.s2 = l - 1;
-  return f;
-}
-
-__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
-  const uint32_t t = __umulhi(f.m, n);
-  return (t + ((n - t) >> f.s1)) >> f.s2;
-}
-
-// q = n / f.d, r = n % f.d
-__device__ __forceinline__ void fast_divmod(uint32_t n, const FastDiv& f, uint32_t& q, uint32_t& r) {
-  q = fast_div(n, f);
-  r = n - q * f.d;
 }
 
 // Four values in [-128, 127] as bytes 0..3 of a word.
