@@ -44,7 +44,8 @@ P = dict(x_mean=0.0, x_var=3.0, ws_lo=0.001, ws_hi=0.005, b_mean=0.0, b_var=0.1)
 # one k-block to several chunks, ragged tails
 SHAPES = [(2, 4, 4, 0.03, 0), (8, 64, 32, 0.02, 3), (130, 200, 36, 0.05, -128),
           (257, 520, 260, 0.03, 127), (129, 1036, 516, 0.01, -5), (300, 4096, 136, 0.03, 1),
-          (640, 2052, 1024, 0.04, -7), (1000, 8192, 264, 0.03, 77), (256, 12, 192, 0.5, 2)]
+          (640, 2052, 1024, 0.04, -7), (1000, 8192, 264, 0.03, 77), (256, 12, 192, 0.5, 2),
+          (1, 64, 32, 0.02, 3), (3, 4, 8, 0.1, -1)]
 
 
 @pytest.mark.parametrize("M,K,N,scale,zp", SHAPES)
