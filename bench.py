@@ -251,17 +251,23 @@ class Path:
 
 
 GEMV_CHAIN_COPIES = 24   # 24 x 16.8 MB of weights: 403 MB, more than 3x the 129 MB L2
-GEMV_CHAIN_REPS = 20
+GEMV_CHAIN_PASSES = 4    # the graph runs the 24 calls 4 times: 96 gemvs in a row
+GEMV_CHAIN_REPS = 5      # graph replays per timed group
+GEMV_CHAIN_GROUPS = 5    # timed groups; the median group is reported
 
 
-def gemv_chain_measure(path, copies=GEMV_CHAIN_COPIES, reps=GEMV_CHAIN_REPS, packed=True):
-    """q8ta_linear_gemv as a decode step runs it: `copies` gemvs back to back,
-    each on its own weight (like successive layers), no event or host work
-    between them, captured once in a CUDA graph (so the host's per-call cost
-    is not what is timed) and replayed `reps` times.  The weights total more
-    than 2x L2, so every call streams its weight from HBM.  Returns
-    (microseconds per call, whether a graph was used); checks that every
-    call's output equals the lone call's (same x, same weight values)."""
+def gemv_chain_measure(path, copies=GEMV_CHAIN_COPIES, reps=GEMV_CHAIN_REPS, packed=True,
+                       passes=GEMV_CHAIN_PASSES, groups=GEMV_CHAIN_GROUPS):
+    """q8ta_linear_gemv as a decode step runs it: gemvs back to back, each
+    on its own weight (like successive layers), no event or host work
+    between them.  `passes` rounds over `copies` weights (passes x copies
+    calls, a decode step's worth) are captured once in a CUDA graph (so the
+    host's per-call cost is not what is timed); a timed group is `reps`
+    replays, and the median of `groups` groups is reported.  The weights
+    total more than 2x L2, so every call streams its weight from HBM.
+    Returns (microseconds per call, whether a graph was used); checks that
+    every call's output equals the lone call's (same x, same weight
+    values)."""
     torch, q8 = path.torch, path.q8
     gp = G.params
     if packed:
@@ -288,27 +294,37 @@ def gemv_chain_measure(path, copies=GEMV_CHAIN_COPIES, reps=GEMV_CHAIN_REPS, pac
         side.wait_stream(torch.cuda.current_stream())
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=side):
-            chain()
+            for _ in range(passes):
+                chain()
         graph = g
     except RuntimeError:
         torch.cuda.synchronize()
         graph = None
-    run = graph.replay if graph is not None else chain
+    if graph is not None:
+        run = graph.replay
+    else:
+        def run():
+            for _ in range(passes):
+                chain()
     for _ in range(3):
         run()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        run()
-    e1.record()
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+    per_group = []
+    for _ in range(groups):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        per_group.append(e0.elapsed_time(e1) * 1e3 / (reps * passes * copies))
+    us = float(np.median(per_group))
     for o in outs:
         if not torch.equal(o, path.g_out):
             raise RuntimeError("gemv chain: a chained call's output differs from the lone call's")
+    used_graph = graph is not None
     del weights, outs, graph
-    return us, run is not chain
+    return us, used_graph
 
 
 def small_op_latency(fn, reps=60, warm=10):
@@ -692,10 +708,13 @@ def run_ours(args, rank, world, local_rank):
             "us_per_call": chain_us, "GB/s": BYTES_GEMV / chain_us / 1e3,
             "frac_hbm": BYTES_GEMV / chain_us / 1e3 / hbm,
             "us_per_call_unpacked_weight": plain_us,
-            "method": f"{GEMV_CHAIN_COPIES} calls back to back on distinct packed weight copies "
-                      f"({GEMV_CHAIN_COPIES * GN * GK / 1e6:.0f} MB, > 2x L2), "
-                      f"{'one CUDA graph' if chain_graph else 'eager launches'} replayed "
-                      f"{GEMV_CHAIN_REPS}x; events only around the replays"}
+            "method": f"{GEMV_CHAIN_PASSES * GEMV_CHAIN_COPIES} calls back to back, "
+                      f"{GEMV_CHAIN_PASSES} passes over {GEMV_CHAIN_COPIES} distinct packed weight "
+                      f"copies ({GEMV_CHAIN_COPIES * GN * GK / 1e6:.0f} MB, > 2x L2, so every "
+                      f"call streams its weight from HBM), "
+                      f"{'one CUDA graph' if chain_graph else 'eager launches'}; median of "
+                      f"{GEMV_CHAIN_GROUPS} groups of {GEMV_CHAIN_REPS} replays, events only "
+                      f"around each group"}
     ops.update(extra_ops)
     achieved = OPS_LINEAR / us["linear"] / 1e6
     roofline = {"kernel": "tc_gemm_kernel<240,12,0,2,2> (q8ta_linear 2048x4096x11008)",

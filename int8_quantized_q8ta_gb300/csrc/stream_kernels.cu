@@ -163,18 +163,25 @@ cudaError_t launch_dequantize(const int8_t* q, int64_t numel, float scale, float
 // the zero point folded as sum x*w - zp * sum w (Constraints paragraph);
 // both sums are exact int32 dp4a dot products, so the fold is exact modulo
 // 2^32 like the accumulator itself.
-// One warp per output row (its lane 0 stores the row's byte); each lane
-// keeps 8 16-byte weight loads in flight; a block's 4 warps take 4
-// consecutive rows.
 //
-// Before waiting for the previous kernel on the stream, the block asks for
-// its whole weight slab (4 rows, contiguous) to be brought into L2 with one
-// bulk prefetch, and lets the next kernel's blocks be scheduled.  Weights
-// are what the gemv streams; a prefetch into L2 can never hand stale data
-// to the loads that follow the wait, because L2 is where the GPU's memory is
-// coherent (a write by the previous kernel updates the line there).  In a
-// run of gemvs (one per layer of a decode step) this makes each call's
-// weight stream from HBM while the previous call is still running.
+// gemv_rows_kernel (K % 16 == 0, 16-byte aligned x and weight): one warp per
+// output row, 16 rows per block; each lane keeps 8 16-byte weight loads in
+// flight (4 KB of the row per round), and each round's 4 KB of x is brought
+// into shared memory once per block instead of every warp reading all of x
+// from L2.  The kernel lets the next kernel on the stream launch first
+// thing, then, before waiting for the previous one:
+//  * the plain form asks for the block's weight slab (16 contiguous rows) to
+//    be brought into L2 with one bulk prefetch.  A prefetch into L2 can never
+//    hand stale data to the loads that follow the wait, because L2 is where
+//    the GPU's memory is coherent (a write by the previous kernel updates the
+//    line there);
+//  * the packed form (a load-time weight, written only by
+//    q8_linear_gemv_pack_weight, which waits for its copy: no kernel that may
+//    still run writes it) loads its first round into registers and sums it.
+// In a run of gemvs (one per layer of a decode step) each call's weight so
+// streams in while the previous call is still running.
+// gemv_kernel is the 4-byte and 1-byte fallback: 4 rows per block, x read
+// by every warp.
 // ---------------------------------------------------------------------------
 // FOLD: also sum the weights (the fold term zp * sum w)
 template <bool FOLD>
@@ -191,17 +198,8 @@ __global__ void __launch_bounds__(128) gemv_kernel(const int8_t* __restrict__ x,
                                                    int8_t* __restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 4 + warp;
-  if constexpr (VEC == 16) {
-    // the block's rows n0 .. n0 + 3 are one contiguous, 16-byte aligned run
-    // (K % 16 == 0): one bulk prefetch of at most 4 * K bytes
-    if (threadIdx.x == 0) {
-      const int n0 = blockIdx.x * 4;
-      const uint32_t bytes = static_cast<uint32_t>(min(4, N - n0)) * static_cast<uint32_t>(K);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(w + static_cast<int64_t>(n0) * K),
-                   "r"(bytes)
-                   : "memory");
-    }
-  } else if (n < N) {
+  static_assert(VEC == 4 || VEC == 1, "16-byte rows take gemv_rows_kernel");
+  if (n < N) {
     const int8_t* wr = w + static_cast<int64_t>(n) * K;
     for (int off = lane * 128; off < K; off += 32 * 128)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(wr + off));
@@ -218,33 +216,7 @@ __global__ void __launch_bounds__(128) gemv_kernel(const int8_t* __restrict__ x,
   int dot = 0, wsum = 0;
   if (n < N) {
     const int8_t* wr = w + static_cast<int64_t>(n) * K;
-    if constexpr (VEC == 16) {
-      // rounds of 8 x 16 bytes per lane (4 KB per warp), every load of a
-      // round issued before any is used; K % 16 == 0 on this path
-      constexpr int UNR = 8;
-      const int nv = K / 16;
-      const int4* w4 = reinterpret_cast<const int4*>(wr);
-      const int4* x4 = reinterpret_cast<const int4*>(x);
-      for (int base = 0; base < nv; base += 32 * UNR) {
-        int4 wv[UNR];
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-          const int idx = base + lane + 32 * u;
-          wv[u] = idx < nv ? __ldcs(w4 + idx) : make_int4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-          const int idx = base + lane + 32 * u;
-          if (idx < nv) {
-            const int4 xv = __ldg(x4 + idx);
-            dp4a_acc<FOLD>(wv[u].x, xv.x, dot, wsum);
-            dp4a_acc<FOLD>(wv[u].y, xv.y, dot, wsum);
-            dp4a_acc<FOLD>(wv[u].z, xv.z, dot, wsum);
-            dp4a_acc<FOLD>(wv[u].w, xv.w, dot, wsum);
-          }
-        }
-      }
-    } else if constexpr (VEC == 4) {
+    if constexpr (VEC == 4) {
       const uint32_t* w1 = reinterpret_cast<const uint32_t*>(wr);
       const uint32_t* x1 = reinterpret_cast<const uint32_t*>(x);
       for (int j = lane; j < K / 4; j += 32) dp4a_acc<FOLD>(__ldcs(w1 + j), __ldg(x1 + j), dot, wsum);
@@ -272,112 +244,105 @@ __global__ void __launch_bounds__(128) gemv_kernel(const int8_t* __restrict__ x,
   }
 }
 
-cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w, int64_t N,
-                        const float* ws, const float* bias, Requant rq, int8_t* out,
-                        cudaStream_t s) {
-  const int grid = static_cast<int>((N + 3) / 4);
-  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(w);
-  // 16-byte loads need every row start 16-byte aligned, hence K % 16 == 0.
-  // (Skipping the weight sums when the zero point is 0 measured slower in a
-  // chain of calls: 4.6 against 4.4 us per call, with fewer registers and
-  // more blocks resident per SM.)
-  if (xa % 16 == 0 && wa % 16 == 0 && K % 16 == 0)
-    return launch_pdl(gemv_kernel<16, true>, grid, 128, 0, s, x, (int)K, izp, w, (int)N, ws, bias,
-                      rq, out);
-  if (xa % 4 == 0 && wa % 4 == 0 && K % 4 == 0)
-    return launch_pdl(gemv_kernel<4, true>, grid, 128, 0, s, x, (int)K, izp, w, (int)N, ws, bias,
-                      rq, out);
-  return launch_pdl(gemv_kernel<1, true>, grid, 128, 0, s, x, (int)K, izp, w, (int)N, ws, bias, rq,
-                    out);
+// Sum over the warp's lanes modulo 2^32 (like the int32 accumulator it forms).
+__device__ __forceinline__ int warp_sum_u32(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    v = static_cast<int>(static_cast<uint32_t>(v) +
+                         static_cast<uint32_t>(__shfl_xor_sync(0xffffffffu, v, o)));
+  return v;
 }
 
-// q8ta_linear_gemv from a packed (load-time) weight.  A packed weight is
-// written once, by q8_linear_gemv_pack_weight, which waits for its copy to
-// finish, and is never written again except by packing into it again; so
-// no kernel that may still be running writes it, and this kernel reads its
-// first round of weights (8 x 16 bytes per lane, 4 KB of the warp's row)
-// and sums them BEFORE waiting for the previous kernel on the stream.  After
-// the wait only x (and, for K > 4096, the further rounds) remain to be
-// read.  K % 16 == 0 with 16-byte aligned x and weight (the host picks the
-// plain kernel otherwise).
-__global__ void __launch_bounds__(128) gemv_packed_kernel(const int8_t* __restrict__ x, int K,
-                                                          int32_t izp,
-                                                          const int8_t* __restrict__ w, int N,
-                                                          const float* __restrict__ ws,
-                                                          const float* __restrict__ bias,
-                                                          Requant rq, int8_t* __restrict__ out) {
-  constexpr int UNR = 8;
+constexpr int kGemvRows = 16;                   // rows (warps) per block
+constexpr int kGemvUnr = 8;                     // 16-byte loads per lane and round
+constexpr int kGemvRound = 32 * kGemvUnr;       // 16-byte words of a row per round
+
+// kPacked: the weight is a packed (load-time) one, read before the wait.
+template <bool kPacked>
+__global__ void __launch_bounds__(32 * kGemvRows, 2)
+    gemv_rows_kernel(const int8_t* __restrict__ x, int K, int32_t izp, const int8_t* __restrict__ w,
+                     int N, const float* __restrict__ ws, const float* __restrict__ bias,
+                     Requant rq, int8_t* __restrict__ out) {
+  constexpr int T = 32 * kGemvRows;
+  static_assert(kGemvRound <= T, "one round of x is at most one 16-byte word per thread");
+  __shared__ int4 xs[kGemvRound];
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = blockIdx.x * 4 + warp;
+  const int n = blockIdx.x * kGemvRows + warp;
+  const bool row_ok = n < N;
   const int nv = K / 16;
-  if (threadIdx.x == 0 && nv > 32 * UNR) {
-    // the rounds after the first: into L2 now
-    const int n0 = blockIdx.x * 4;
-    const uint32_t bytes = static_cast<uint32_t>(min(4, N - n0)) * static_cast<uint32_t>(K);
+  const bool one_round = nv <= kGemvRound;
+  if (threadIdx.x == 0 && (!kPacked || !one_round)) {
+    // into L2 now: the block's rows (packed: the rounds after the first),
+    // one contiguous, 16-byte aligned run
+    const int n0 = blockIdx.x * kGemvRows;
+    const uint32_t bytes = static_cast<uint32_t>(min(kGemvRows, N - n0)) * static_cast<uint32_t>(K);
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(w + static_cast<int64_t>(n0) * K),
                  "r"(bytes)
                  : "memory");
   }
-  const int4* w4 = reinterpret_cast<const int4*>(w + static_cast<int64_t>(n < N ? n : 0) * K);
-  int4 wv[UNR];
+  const int4* w4 = reinterpret_cast<const int4*>(w + static_cast<int64_t>(row_ok ? n : 0) * K);
+  int4 wv[kGemvUnr];
   int dot = 0, wsum = 0;
+  if constexpr (kPacked) {
 #pragma unroll
-  for (int u = 0; u < UNR; ++u) {
-    const int idx = lane + 32 * u;
-    wv[u] = (n < N && idx < nv) ? __ldcs(w4 + idx) : make_int4(0, 0, 0, 0);
-  }
+    for (int u = 0; u < kGemvUnr; ++u) {
+      const int idx = lane + 32 * u;
+      wv[u] = (row_ok && idx < nv) ? __ldcs(w4 + idx) : make_int4(0, 0, 0, 0);
+    }
 #pragma unroll
-  for (int u = 0; u < UNR; ++u) {
-    wsum = __dp4a(wv[u].x, 0x01010101, wsum);
-    wsum = __dp4a(wv[u].y, 0x01010101, wsum);
-    wsum = __dp4a(wv[u].z, 0x01010101, wsum);
-    wsum = __dp4a(wv[u].w, 0x01010101, wsum);
+    for (int u = 0; u < kGemvUnr; ++u) {
+      wsum = __dp4a(wv[u].x, 0x01010101, wsum);
+      wsum = __dp4a(wv[u].y, 0x01010101, wsum);
+      wsum = __dp4a(wv[u].z, 0x01010101, wsum);
+      wsum = __dp4a(wv[u].w, 0x01010101, wsum);
+    }
+    // a row of one round has its whole weight sum now: reduce it before the wait
+    if (one_round) wsum = warp_sum_u32(wsum);
   }
-  pdl_launch_dependents();
   pdl_wait();
-  if (n >= N) return;
   float wsn = 0.0f, bn = 0.0f;
-  if (lane == 0) {
+  if (row_ok && lane == 0) {
     wsn = __ldg(ws + n);
     bn = bias ? __ldg(bias + n) : 0.0f;
   }
   const int4* x4 = reinterpret_cast<const int4*>(x);
+  for (int base = 0; base < nv; base += kGemvRound) {
+    // rounds whose weights are loaded (and summed) after the wait
+    const bool late = !kPacked || base > 0;
+    if (base > 0) __syncthreads();  // every warp is done with the previous round's x
+    if (late) {
 #pragma unroll
-  for (int u = 0; u < UNR; ++u) {
-    const int idx = lane + 32 * u;
-    if (idx < nv) {
-      const int4 xv = __ldg(x4 + idx);
+      for (int u = 0; u < kGemvUnr; ++u) {
+        const int idx = base + lane + 32 * u;
+        wv[u] = (row_ok && idx < nv) ? __ldcs(w4 + idx) : make_int4(0, 0, 0, 0);
+      }
+    }
+    if (threadIdx.x < kGemvRound) {
+      // this round's x, one 16-byte word per thread (zero past K)
+      const int i = base + threadIdx.x;
+      xs[threadIdx.x] = i < nv ? __ldg(x4 + i) : make_int4(0, 0, 0, 0);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kGemvUnr; ++u) {
+      // past K, both the weight and x words are zero
+      const int4 xv = xs[lane + 32 * u];
       dot = __dp4a(wv[u].x, xv.x, dot);
       dot = __dp4a(wv[u].y, xv.y, dot);
       dot = __dp4a(wv[u].z, xv.z, dot);
       dot = __dp4a(wv[u].w, xv.w, dot);
-    }
-  }
-  for (int base = 32 * UNR; base < nv; base += 32 * UNR) {
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int idx = base + lane + 32 * u;
-      wv[u] = idx < nv ? __ldcs(w4 + idx) : make_int4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int idx = base + lane + 32 * u;
-      if (idx < nv) {
-        const int4 xv = __ldg(x4 + idx);
-        dp4a_acc<true>(wv[u].x, xv.x, dot, wsum);
-        dp4a_acc<true>(wv[u].y, xv.y, dot, wsum);
-        dp4a_acc<true>(wv[u].z, xv.z, dot, wsum);
-        dp4a_acc<true>(wv[u].w, xv.w, dot, wsum);
+      if (late) {
+        wsum = __dp4a(wv[u].x, 0x01010101, wsum);
+        wsum = __dp4a(wv[u].y, 0x01010101, wsum);
+        wsum = __dp4a(wv[u].z, 0x01010101, wsum);
+        wsum = __dp4a(wv[u].w, 0x01010101, wsum);
       }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    dot = static_cast<int>(static_cast<uint32_t>(dot) +
-                           static_cast<uint32_t>(__shfl_xor_sync(0xffffffffu, dot, o)));
-    wsum = static_cast<int>(static_cast<uint32_t>(wsum) +
-                            static_cast<uint32_t>(__shfl_xor_sync(0xffffffffu, wsum, o)));
-  }
+  if (!row_ok) return;
+  dot = warp_sum_u32(dot);
+  if (!kPacked || !one_round) wsum = warp_sum_u32(wsum);
   if (lane == 0) {
     const int32_t acc = static_cast<int32_t>(static_cast<uint32_t>(dot) -
                                              static_cast<uint32_t>(izp) * static_cast<uint32_t>(wsum));
@@ -385,18 +350,51 @@ __global__ void __launch_bounds__(128) gemv_packed_kernel(const int8_t* __restri
   }
 }
 
+// Measured in a chain of 24 calls (1 x 4096 x 4096, packed weight): one warp
+// per row in blocks of 4 rows, each warp reading all of x from L2, 3.85 us
+// per call; x through shared memory with 8 / 16 / 32 rows per block, 3.49 /
+// 3.40 / 3.48 us; 16 rows with the next kernel let in first thing, 3.29 us.
+// (A variant staging whole weight slabs in shared memory with bulk copies,
+// one block per SM and two calls resident, measured 4.4 us: after the
+// dependency wait its work ran behind the next call's copies.)
+static cudaError_t launch_gemv_rows(bool packed, const int8_t* x, int64_t K, int32_t izp,
+                                    const int8_t* w, int64_t N, const float* ws, const float* bias,
+                                    Requant rq, int8_t* out, cudaStream_t s) {
+  const int grid = static_cast<int>((N + kGemvRows - 1) / kGemvRows);
+  if (packed)
+    return launch_pdl(gemv_rows_kernel<true>, grid, 32 * kGemvRows, 0, s, x, (int)K, izp, w, (int)N,
+                      ws, bias, rq, out);
+  return launch_pdl(gemv_rows_kernel<false>, grid, 32 * kGemvRows, 0, s, x, (int)K, izp, w, (int)N,
+                    ws, bias, rq, out);
+}
+
+cudaError_t launch_gemv(const int8_t* x, int64_t K, int32_t izp, const int8_t* w, int64_t N,
+                        const float* ws, const float* bias, Requant rq, int8_t* out,
+                        cudaStream_t s) {
+  const int grid = static_cast<int>((N + 3) / 4);
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(w);
+  // 16-byte loads need every row start 16-byte aligned, hence K % 16 == 0.
+  // (In an earlier 4-row form, skipping the weight sums when the zero point
+  // is 0 measured slower in a chain of calls, 4.6 against 4.4 us per call:
+  // fewer registers, more blocks resident per SM.)
+  if (xa % 16 == 0 && wa % 16 == 0 && K % 16 == 0)
+    return launch_gemv_rows(false, x, K, izp, w, N, ws, bias, rq, out, s);
+  if (xa % 4 == 0 && wa % 4 == 0 && K % 4 == 0)
+    return launch_pdl(gemv_kernel<4, true>, grid, 128, 0, s, x, (int)K, izp, w, (int)N, ws, bias,
+                      rq, out);
+  return launch_pdl(gemv_kernel<1, true>, grid, 128, 0, s, x, (int)K, izp, w, (int)N, ws, bias, rq,
+                    out);
+}
+
+// q8ta_linear_gemv from a packed (load-time) weight: the same kernel, its
+// first round of weights read before the wait.
 cudaError_t launch_gemv_packed(const int8_t* x, int64_t K, int32_t izp, const int8_t* w, int64_t N,
                                const float* ws, const float* bias, Requant rq, int8_t* out,
                                cudaStream_t s) {
   const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(w);
   if (!(xa % 16 == 0 && wa % 16 == 0 && K % 16 == 0))
     return launch_gemv(x, K, izp, w, N, ws, bias, rq, out, s);
-  // (A variant staging the rows in shared memory through bulk copies, which
-  // holds no registers while it waits and so keeps more calls resident,
-  // measured 4.07 us per call in a chain of 24 against 3.76 us for this one:
-  // more calls' loads in flight delay the one that runs.)
-  return launch_pdl(gemv_packed_kernel, static_cast<int>((N + 3) / 4), 128, 0, s, x, (int)K, izp, w,
-                    (int)N, ws, bias, rq, out);
+  return launch_gemv_rows(true, x, K, izp, w, N, ws, bias, rq, out, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -107,11 +107,12 @@ def test_gemv_ragged(K, N, izp):
 
 
 # The gemv from a packed weight (its first 4 KB of each row read before the
-# launch dependency wait): K % 16 == 0 up to one round, several rounds
-# (K > 4096), and K % 16 != 0 (the host falls back to the plain kernel).
+# launch dependency wait, 16 rows per block): K % 16 == 0 up to one round,
+# several rounds (K > 4096, a ragged last round), N not a multiple of 16,
+# and K % 16 != 0 (the host falls back to the plain kernel).
 @pytest.mark.parametrize("K,N,izp", [(16, 4, 0), (4096, 4096, 0), (64, 36, 127), (1028, 40, 3),
                                      (4096 + 16, 8, -7), (8192, 20, -100), (16384, 12, 127),
-                                     (2048, 1004, 3), (100, 12, 5)])
+                                     (2048, 1004, 3), (100, 12, 5), (3 * 4096 + 48, 36, 1)])
 def test_gemv_packed_matches_oracle(K, N, izp):
     p = dict(ws_lo=0.002, ws_hi=0.01, b_mean=0.0, b_var=0.1)
     x, w, ws, b = synth.linear_inputs(2 * K + N, 1, K, N, x_kind="int8", p=p)
