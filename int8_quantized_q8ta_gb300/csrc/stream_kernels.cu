@@ -560,37 +560,41 @@ cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, f
 // dst[n][j*CBg + c/64][h][w][c%64] for channel c of group j (CBg = ICgp/64
 // blocks per group); the padding channels ICg <= c < ICgp hold exactly 0, not
 // -zp, so the (64 channels x w x h) box of one k-block is contiguous along w.
-// One block of 128 threads per (n, channel block, h, 64 columns):
+// One block of 128 threads per (n, channel block, h, 64 columns), the block
+// index split by multiply-shift divisions:
 //  * load: each thread reads 32 consecutive bytes of one channel's row (two
 //    16-byte loads) into shared memory, rows of 16 words (+1 pad);
 //  * store: each thread takes 4 columns x 8 channels, i.e. one word of each
-//    of 8 channel rows; byte c of word j is channel j at column c, so one
-//    byte permute per value sign-extends it, one add of 0x4B400000 - zp and
-//    one subtraction of 1.5 * 2^23 give the float of x - zp, whose high half
-//    is its bf16 (exact: at most 8 significant bits); the thread stores 4
-//    pieces of 16 bytes (8 channels of one pixel each), and a warp's store
-//    covers 4 whole 128-byte pixel rows.
+//    of 8 channel rows.  Flipping the top bit of every byte gives x + 128 as
+//    an unsigned byte; one byte permute puts byte c of a word under the
+//    constant high bytes of 1.5 * 2^23, which makes the float 1.5 * 2^23 +
+//    x + 128, and one subtraction of 1.5 * 2^23 + 128 + zp leaves exactly
+//    x - zp, whose high half is its bf16 (exact: at most 8 significant
+//    bits).  The thread stores 4 pieces of 16 bytes (8 channels of one pixel
+//    each), and a warp's store covers 4 whole 128-byte pixel rows.
+struct RelayoutDiv {
+  FastDiv wb, h, cb, cbg;  // by (W + 63) / 64, H, CB (channel blocks), CBg
+};
+
 template <bool VEC>
 __global__ void __launch_bounds__(128) nchw_to_nhwc_bf16_kernel(const int8_t* __restrict__ x,
                                                                 int64_t groups, int64_t ICg,
                                                                 int64_t H, int64_t W, int32_t zp,
                                                                 uint4* __restrict__ dst,
-                                                                int64_t ICgp) {
+                                                                int64_t ICgp, RelayoutDiv dv) {
   __shared__ uint32_t tile[64][17];  // [channel][4-column word]
   pdl_wait();
   pdl_launch_dependents();
   const int64_t CBg = ICgp / 64, CB = CBg * groups, C = groups * ICg;
-  // the block index in 32 bits (the launch checks it fits): 32-bit division
-  // is a short sequence, 64-bit division a long one
-  const uint32_t WB = static_cast<uint32_t>((W + 63) / 64);
-  uint32_t b = blockIdx.x;
-  const int64_t wb = b % WB;
-  b /= WB;
-  const int64_t h = b % static_cast<uint32_t>(H);
-  b /= static_cast<uint32_t>(H);
-  const int64_t cb = b % static_cast<uint32_t>(CB);
-  const int64_t n = b / static_cast<uint32_t>(CB);
-  const int64_t g = static_cast<uint32_t>(cb) / static_cast<uint32_t>(CBg);
+  // the block index in 32 bits (the launch checks it fits)
+  uint32_t q, r;
+  fast_divmod(blockIdx.x, dv.wb, q, r);
+  const int64_t wb = r;
+  fast_divmod(q, dv.h, q, r);
+  const int64_t h = r;
+  fast_divmod(q, dv.cb, q, r);
+  const int64_t cb = r, n = q;
+  const int64_t g = fast_div(static_cast<uint32_t>(cb), dv.cbg);
   const int64_t cl0 = (cb - g * CBg) * 64;  // first channel of the block, within its group
   const int64_t w0 = wb * 64;
   const int t = threadIdx.x;
@@ -619,25 +623,25 @@ __global__ void __launch_bounds__(128) nchw_to_nhwc_bf16_kernel(const int8_t* __
   if (w0 + 4 * cq >= W) return;
   uint32_t a[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) a[j] = tile[8 * cs + j][cq];
+  for (int j = 0; j < 8; ++j) a[j] = tile[8 * cs + j][cq] ^ 0x80808080u;  // bytes x + 128
   // channels past the group's last one are padding: exactly 0
   const int64_t left = ICg - (cl0 + 8 * cs);
   const int nvalid = left >= 8 ? 8 : (left <= 0 ? 0 : static_cast<int>(left));
-  const int base = 0x4B400000 - zp;
+  // 1.5 * 2^23 + 128 + zp: an integer below 2^24, exact in f32
+  const float bias = static_cast<float>(12582912 + 128 + zp);
   uint4* out = dst + (((n * CB + cb) * H + h) * W + w0 + 4 * cq) * 8 + cs;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     if (w0 + 4 * cq + c >= W) break;
-    // byte c of each word, sign-extended: a byte permute whose selector takes
-    // byte c, then replicates its sign bit into the three upper bytes (the
-    // PTX prmt sign mode, selector bit 3, which __byte_perm does not expose)
-    const uint32_t sel = static_cast<uint32_t>(c) | ((8u | c) << 4) | ((8u | c) << 8) | ((8u | c) << 12);
+    // bytes: [byte c of the word, 0x00, 0x40, 0x4B] = the bits of 1.5 * 2^23 + (x + 128)
+    const uint32_t sel = static_cast<uint32_t>(c) | 0x7650u;
     uint32_t f[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      int q;
-      asm("prmt.b32 %0, %1, 0, %2;" : "=r"(q) : "r"(a[j]), "r"(sel));
-      f[j] = j < nvalid ? __float_as_uint(__fsub_rn(__int_as_float(base + q), 12582912.0f)) : 0u;
+    for (int j = 0; j < 8; ++j)
+      f[j] = __float_as_uint(__fsub_rn(__uint_as_float(__byte_perm(a[j], 0x4B400000u, sel)), bias));
+    if (nvalid < 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = j < nvalid ? f[j] : 0u;
     }
     uint4 o;
     o.x = __byte_perm(f[0], f[1], 0x7632);
@@ -652,14 +656,17 @@ cudaError_t launch_nchw_to_nhwc_bf16(const int8_t* x, int64_t N, int64_t groups,
                                      int64_t H, int64_t W, int32_t zp, __nv_bfloat16* dst,
                                      int64_t ICgp, cudaStream_t s) {
   if (N * H * W == 0) return cudaSuccess;
-  const int64_t blocks = N * groups * (ICgp / 64) * H * ((W + 63) / 64);
+  const int64_t WB = (W + 63) / 64, CBg = ICgp / 64, CB = CBg * groups;
+  const int64_t blocks = N * CB * H * WB;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  const RelayoutDiv dv{make_fastdiv(static_cast<uint32_t>(WB)), make_fastdiv(static_cast<uint32_t>(H)),
+                       make_fastdiv(static_cast<uint32_t>(CB)), make_fastdiv(static_cast<uint32_t>(CBg))};
   const bool vec = (W % 16 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
   if (vec)
     return launch_pdl(nchw_to_nhwc_bf16_kernel<true>, static_cast<int>(blocks), 128, 0, s, x,
-                      groups, ICg, H, W, zp, reinterpret_cast<uint4*>(dst), ICgp);
+                      groups, ICg, H, W, zp, reinterpret_cast<uint4*>(dst), ICgp, dv);
   return launch_pdl(nchw_to_nhwc_bf16_kernel<false>, static_cast<int>(blocks), 128, 0, s, x, groups,
-                    ICg, H, W, zp, reinterpret_cast<uint4*>(dst), ICgp);
+                    ICg, H, W, zp, reinterpret_cast<uint4*>(dst), ICgp, dv);
 }
 
 // Convolution weight [OC, ldw] (per row: taps x ICg used) -> bf16, per group j:
