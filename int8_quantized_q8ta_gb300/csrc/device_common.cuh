@@ -120,6 +120,31 @@ __device__ __forceinline__ uint32_t bf16x2_from_ints(int lo, int hi) {
   return __byte_perm(bf16_bits_hi(lo), bf16_bits_hi(hi), 0x7632);
 }
 
+// quantize_per_tensor of 8 values and the bf16 of their q - zp, together:
+// u = x * inv is clamped first to [-128 - zp, 127 - zp] (integer bounds, so
+// rint(clamp(u)) + zp = clamp(rint(u) + zp, -128, 127), NaN taking the lower
+// bound as in quantize_one), then y = u + 1.5 * 2^23 rounds it: the low byte
+// of bits(y) + zp is q, and y - 1.5 * 2^23 is exactly the float of q - zp,
+// whose high half is its bf16.  qw: the 8 int8 q; ow: the 8 bf16.
+__device__ __forceinline__ void quantize8_operand(const float (&x)[8], float inv, int32_t zp,
+                                                  uint2& qw, uint4& ow) {
+  const float lo_f = static_cast<float>(-128 - zp), hi_f = static_cast<float>(127 - zp);
+  uint32_t qb[8], d[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float c = fminf(fmaxf(__fmul_rn(x[j], inv), lo_f), hi_f);
+    const float y = __fadd_rn(c, kRoundMagic);
+    qb[j] = __float_as_uint(y) + static_cast<uint32_t>(zp);
+    d[j] = __float_as_uint(__fsub_rn(y, kRoundMagic));
+  }
+  qw.x = __byte_perm(__byte_perm(qb[0], qb[1], 0x0040), __byte_perm(qb[2], qb[3], 0x0040), 0x5410);
+  qw.y = __byte_perm(__byte_perm(qb[4], qb[5], 0x0040), __byte_perm(qb[6], qb[7], 0x0040), 0x5410);
+  ow.x = __byte_perm(d[0], d[1], 0x7632);
+  ow.y = __byte_perm(d[2], d[3], 0x7632);
+  ow.z = __byte_perm(d[4], d[5], 0x7632);
+  ow.w = __byte_perm(d[6], d[7], 0x7632);
+}
+
 // Destination layout of the GEMM operands ("K-blocked"): dst[kb][r][kk] with
 // kb = k / 64 and kk = k % 64, so the 128 x 64 (or BN x 64) tile the tensor
 // cores read for one k-block is a single contiguous run in memory.

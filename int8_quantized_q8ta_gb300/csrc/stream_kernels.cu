@@ -497,38 +497,29 @@ __global__ void __launch_bounds__(256) quantize_rows_bf16_kernel(
       if (i >= total) break;
       const int64_t r = rr[u];
       const int64_t k0 = kk[u];
-      int8_t q[8];
-      int v[8];
+      uint4 o;
       if (vec && k0 + 8 <= K) {
-        q[0] = quantize_one(va[u].x, inv, zpf); q[1] = quantize_one(va[u].y, inv, zpf);
-        q[2] = quantize_one(va[u].z, inv, zpf); q[3] = quantize_one(va[u].w, inv, zpf);
-        q[4] = quantize_one(vb[u].x, inv, zpf); q[5] = quantize_one(vb[u].y, inv, zpf);
-        q[6] = quantize_one(vb[u].z, inv, zpf); q[7] = quantize_one(vb[u].w, inv, zpf);
-        if (xq) {
-          uint2 o;
-          o.x = pack4(q[0], q[1], q[2], q[3]);
-          o.y = pack4(q[4], q[5], q[6], q[7]);
-          *reinterpret_cast<uint2*>(xq + r * K + k0) = o;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = static_cast<int>(q[j]) - zp;
+        const float xv[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+        uint2 qw;
+        quantize8_operand(xv, inv, zpf, qw, o);
+        if (xq) *reinterpret_cast<uint2*>(xq + r * K + k0) = qw;
       } else {
+        int v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (k0 + j < K) {
-            q[j] = quantize_one(x[r * K + k0 + j], inv, zpf);
-            if (xq) xq[r * K + k0 + j] = q[j];
-            v[j] = static_cast<int>(q[j]) - zp;
+            const int8_t q = quantize_one(x[r * K + k0 + j], inv, zpf);
+            if (xq) xq[r * K + k0 + j] = q;
+            v[j] = static_cast<int>(q) - zp;
           } else {
             v[j] = 0;
           }
         }
+        o.x = bf16x2_from_ints(v[0], v[1]);
+        o.y = bf16x2_from_ints(v[2], v[3]);
+        o.z = bf16x2_from_ints(v[4], v[5]);
+        o.w = bf16x2_from_ints(v[6], v[7]);
       }
-      uint4 o;
-      o.x = bf16x2_from_ints(v[0], v[1]);
-      o.y = bf16x2_from_ints(v[2], v[3]);
-      o.z = bf16x2_from_ints(v[4], v[5]);
-      o.w = bf16x2_from_ints(v[6], v[7]);
       dst[kblocked_index16(r, k0, static_cast<int64_t>(rows))] = o;
     }
   }

@@ -192,6 +192,32 @@ def test_linear_chain_8x64x32():
     np.testing.assert_array_equal(H(fout), ref)
 
 
+# The quantize -> operand kernel of the prefill chain on the values where a
+# rounding or clamping slip would show: ties (x * inv = k + 1/2), +-0, +-inf,
+# NaN, values far past the int8 range, for zero points at both ends and an
+# odd one; K = 64 and 72 (8-element items from 16-byte loads; 72 also pads
+# its last k-block with zeros) and K = 70 (rows not 16-byte aligned: one
+# element at a time).  x_q and the GEMM's result both equal the oracle's.
+@pytest.mark.parametrize("zp", [-128, -7, 0, 3, 127])
+@pytest.mark.parametrize("K", [64, 72, 70])
+def test_quantize_to_operand_special_values(zp, K):
+    special = np.array([0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 0.0, -0.0, np.inf, -np.inf, np.nan,
+                        1e30, -1e30, 127.5, -128.5, 126.5, -127.5, 255.5, -255.5, 3e9],
+                       np.float32)
+    M = 6
+    x = synth.normal(11 + K, "qs", (M, K), 0.0, 60.0)
+    flat = x.reshape(-1)
+    flat[: special.size] = special
+    flat[-special.size:] = special[::-1]
+    p = dict(ws_lo=0.002, ws_hi=0.01, b_mean=0.0, b_var=0.1)
+    _, w, ws, b = synth.linear_inputs(5 + K, M, K, 8, x_kind="int8", p=p)
+    packed = q8.pack_weight(T(w))
+    xq, out = q8.quantize_linear_packed(T(x), 1.0, zp, packed, T(ws), T(b), 0.3, -1)
+    xq_ref = oracle.quantize_per_tensor(x, 1.0, zp)
+    np.testing.assert_array_equal(H(xq), xq_ref)
+    np.testing.assert_array_equal(H(out), oracle.linear(xq_ref, 1.0, zp, w, ws, b, 0.3, -1))
+
+
 def _mismatches(got, ref):
     """Count of differing elements and the first few (index, got, ref)."""
     bad = np.argwhere(got != ref)
