@@ -327,6 +327,57 @@ def gemv_chain_measure(path, copies=GEMV_CHAIN_COPIES, reps=GEMV_CHAIN_REPS, pac
     return us, used_graph
 
 
+def unpacked_forms_measure(path, h, reps=10, warm=2):
+    """The schema entry points with raw int8 weights, no load-time packing:
+    q8_linear on the prefill linear (x_q from the step) and
+    q8_conv2d_transposed on the 8x256x64x64 convolution.  Each call turns
+    its weight into the tensor-core operand again (and computes no weight
+    bound, so its exact chunks are the int8 worst case).  Median of `reps`
+    calls after `warm`, each bracketed by CUDA events; each output must
+    equal the packed path's."""
+    torch, q8 = path.torch, path.q8
+    lp, cp = L.params, C.params
+    lw = torch.from_numpy(np.ascontiguousarray(h["lw"])).to(path.dev)
+    lout = torch.empty_like(path.l_out)
+    lwork = torch.empty(q8.lib().q8_linear_workspace_bytes(LM, LK, LN), dtype=torch.uint8,
+                        device=path.dev)
+    cout = torch.empty_like(path.c_out)
+
+    def lin():
+        q8.linear(path.l_xq, lp["in_scale"], lp["in_zp"], lw, None, path.lws, path.lb,
+                  lp["out_scale"], lp["out_zp"], out=lout, workspace=lwork)
+
+    def conv():
+        q8.conv2d_transposed(path.cx, cp["in_scale"], cp["in_zp"], path.cw, None, path.cws,
+                             path.cb, cp["out_scale"], cp["out_zp"], (CD["Kh"], CD["Kw"]),
+                             stride=CD["s"], padding=CD["p"], output_padding=CD["op"],
+                             out=cout)
+
+    res = {}
+    for name, fn in (("linear", lin), ("conv_t", conv)):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        res[name] = float(np.median(times))
+    path.run_op("linear")
+    path.run_op("conv_t")
+    torch.cuda.synchronize()
+    if not torch.equal(lout, path.l_out):
+        raise RuntimeError("q8_linear with a raw weight differs from the packed path")
+    if not torch.equal(cout, path.c_out):
+        raise RuntimeError("q8_conv2d_transposed with a raw weight differs from the packed path")
+    del lw, lout, lwork, cout
+    return res
+
+
 def small_op_latency(fn, reps=60, warm=10):
     """Median microseconds of fn() over `reps` calls, each bracketed by CUDA
     events on the launching stream (launch gaps included), after `warm`."""
@@ -673,6 +724,18 @@ def run_ours(args, rank, world, local_rank):
     if args.only == "all" and not args.no_extra_ops:
         extra_ops = small_configs_measure(dev)
         ab = fused_chain_ab(path)
+        unp = unpacked_forms_measure(path, h)
+        extra_ops["q8ta_linear_2048x4096x11008_raw_weight"] = {
+            "us": unp["linear"], "TOPS": OPS_LINEAR / unp["linear"] / 1e6,
+            "method": "q8_linear (the pages' schema) with the raw int8 weight: each call converts "
+                      "x_q and the 45 MB weight to the bf16 operands, then the GEMM; median of 10 "
+                      "event-bracketed calls; output equal to the packed path's"}
+        extra_ops["q8ta_conv2d_transposed_8x256x64x64_raw_weight"] = {
+            "us": unp["conv_t"], "outputs/s": CONV_OUTPUTS / unp["conv_t"] * 1e6,
+            "method": "q8_conv2d_transposed (the pages' schema) with the raw int8 weight: each call "
+                      "converts the weight (no k-block bound: worst-case exact chunks), relayouts x, "
+                      "then the GEMM; "
+                      "median of 10 event-bracketed calls; output equal to the packed path's"}
         extra_ops["quantize_q8ta_linear_2048x4096x11008_two_vs_one_kernel"] = {
             "us_two_kernels": ab["two_kernels"], "us_one_kernel": ab["one_kernel"],
             "method": "the prefill chain alone, each call bracketed by CUDA events, median of 10 "
