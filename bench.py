@@ -802,7 +802,8 @@ def run_ours(args, rank, world, local_rank):
                          "from the previous step",
                    "weights": "linear and conv_t weights packed to bf16 once, outside the "
                               "timed region (load time, as the pages' ahead-of-time weight "
-                              "reshape); gemv weight raw int8",
+                              "reshape); the gemv weight copied once into a packed (never rewritten) "
+                              "int8 buffer, also outside the timed region",
                    "parallelism": f"replicas x{world}"},
         "ops": ops, "roofline": roofline, "clocks": clocks,
         "gpu_launches": path.launches_per_step() * K,
