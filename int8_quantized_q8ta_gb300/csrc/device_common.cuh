@@ -66,6 +66,25 @@ __device__ __forceinline__ int32_t round_clamp_first(float u, int32_t zp, float 
   return __float_as_int(__fadd_rn(c, kRoundMagic)) - (0x4B400000 - zp);
 }
 
+// The same result with only the floor taken on the float: u is raised to
+// at least lo - zp (NaN takes it, as fmaxf does), 1.5 * 2^23 is added and
+// the integer read off the encoding; that integer is rint(u) + zp below
+// 2^22 and only larger above, so a saturating conversion to int8 (see
+// pack4_sat) supplies the upper clamp.  Returns the unsaturated int32.
+__device__ __forceinline__ int32_t round_floor_first(float u, int32_t zp, float lo_f) {
+  return __float_as_int(__fadd_rn(fmaxf(u, lo_f), kRoundMagic)) - (0x4B400000 - zp);
+}
+
+// Four int32 values saturated to [-128, 127] as bytes 0..3 of a word: two
+// cvt.pack.sat (each converts two values with saturation into the low 16
+// bits and copies the low bits of its third operand above them).
+__device__ __forceinline__ uint32_t pack4_sat(int32_t a, int32_t b, int32_t c, int32_t d) {
+  uint32_t hi, r;
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(d), "r"(c), "r"(0u));
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
+  return r;
+}
+
 // The fused epilogue of one accumulator, in the order of "Add q8ta_linear op"
 // (Solution paragraph): ((acc * input_scale) * weight_scale + bias) *
 // (1 / output_scale), rounded, plus the output zero point, clamped (from

@@ -527,11 +527,16 @@ __device__ __forceinline__ PixRun pix_run(const TcParams& p, const TileInfo& ti,
 }
 
 // Four f32 accumulators of one output channel -> one word of four
-// requantized bytes.
+// requantized bytes: the epilogue's arithmetic in the order of requant_f,
+// the floor on the float and the upper clamp in the saturating pack.
+__device__ __forceinline__ int32_t rq_unclamped(float a, float ws, float b, const Requant& rq) {
+  const float u = __fmul_rn(__fadd_rn(__fmul_rn(__fmul_rn(a, rq.s_in), ws), b), rq.inv_out);
+  return round_floor_first(u, rq.ozp_i, rq.lo_f);
+}
 __device__ __forceinline__ uint32_t rq_pack4(float a0, float a1, float a2, float a3, float ws,
                                              float b, const Requant& rq) {
-  return pack4_i(requant_f(a0, ws, b, rq), requant_f(a1, ws, b, rq), requant_f(a2, ws, b, rq),
-                 requant_f(a3, ws, b, rq));
+  return pack4_sat(rq_unclamped(a0, ws, b, rq), rq_unclamped(a1, ws, b, rq),
+                   rq_unclamped(a2, ws, b, rq), rq_unclamped(a3, ws, b, rq));
 }
 
 // Output pixel of run column c (generic placement).
@@ -1371,10 +1376,10 @@ __global__ void __launch_bounds__(cta_threads(EPI), 1)
                   const float4 w4 = *reinterpret_cast<const float4*>(sws + 16 * g + 4 * q);
                   const float4 b4 = *reinterpret_cast<const float4*>(sbs + 16 * g + 4 * q);
                   const int s0 = 16 * g + 4 * q;
-                  wds[q] = pack4_i(requant_f(__int_as_float(sum[s0 + 0]), w4.x, b4.x, p.rq),
-                                   requant_f(__int_as_float(sum[s0 + 1]), w4.y, b4.y, p.rq),
-                                   requant_f(__int_as_float(sum[s0 + 2]), w4.z, b4.z, p.rq),
-                                   requant_f(__int_as_float(sum[s0 + 3]), w4.w, b4.w, p.rq));
+                  wds[q] = pack4_sat(rq_unclamped(__int_as_float(sum[s0 + 0]), w4.x, b4.x, p.rq),
+                                     rq_unclamped(__int_as_float(sum[s0 + 1]), w4.y, b4.y, p.rq),
+                                     rq_unclamped(__int_as_float(sum[s0 + 2]), w4.z, b4.z, p.rq),
+                                     rq_unclamped(__int_as_float(sum[s0 + 3]), w4.w, b4.w, p.rq));
                 }
                 if (p.store_mode == 2 && c + 16 <= p.N) {
                   *reinterpret_cast<uint4*>(dst + c) = make_uint4(wds[0], wds[1], wds[2], wds[3]);

@@ -6,7 +6,10 @@ relu) without a float->int conversion instruction, in two forms:
     (round to nearest even), read the integer from the sum's encoding and
     clamp it as an integer;
   * the GEMM and gemv epilogues clamp u first, to [lo - zp, 127 - zp], then
-    add 1.5 * 2^23 and read the integer, already in range.
+    add 1.5 * 2^23 and read the integer, already in range;
+  * the exchanged-operand convolution epilogue takes only the floor on the
+    float (u raised to lo - zp), adds 1.5 * 2^23, reads the integer and
+    leaves the upper clamp to a saturating conversion to int8.
 This test replays the forms in numpy float32 -- whose
 addition rounds to nearest even like the GPU's __fadd_rn -- over every
 rounding tie near the int8 range, their float neighbours, random bit
@@ -53,6 +56,17 @@ def clamp_first(u, zp, lo):
     return q.astype(np.int32)
 
 
+def floor_first(u, zp, lo):
+    c = np.where(np.isnan(u), F(lo - zp), u).astype(F)            # fmaxf(NaN, c) = c
+    c = np.maximum(c, F(lo - zp)).astype(F)
+    y = (c + F(12582912.0)).astype(F)
+    bits = y.view(np.int32).astype(np.int64)
+    assert (bits > 0).all()                                         # y stays positive
+    q = bits - (0x4B400000 - zp)
+    assert (q >= lo).all() and (q < 2 ** 31).all()                  # an int32, at least lo
+    return np.clip(q, -128, 127).astype(np.int32)                   # the saturating pack
+
+
 def _samples():
     ties = np.arange(-400, 400, dtype=np.float64) + 0.5
     ints = np.arange(-400, 400, dtype=np.float64)
@@ -84,6 +98,16 @@ def test_clamp_first_matches_rint_add_clamp_for_every_zero_point_and_floor():
             np.testing.assert_array_equal(clamp_first(u, zp, -128), plain(u, zp),
                                           err_msg=f"zp={zp}")
             np.testing.assert_array_equal(clamp_first(u, zp, zp), plain_lo(u, zp, zp),
+                                          err_msg=f"relu zp={zp}")
+
+
+def test_floor_first_with_saturation_matches_rint_add_clamp():
+    u = _samples()
+    with np.errstate(invalid="ignore", over="ignore"):
+        for zp in range(-128, 128):
+            np.testing.assert_array_equal(floor_first(u, zp, -128), plain(u, zp),
+                                          err_msg=f"zp={zp}")
+            np.testing.assert_array_equal(floor_first(u, zp, zp), plain_lo(u, zp, zp),
                                           err_msg=f"relu zp={zp}")
 
 
