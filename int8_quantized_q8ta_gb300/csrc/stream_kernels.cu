@@ -530,7 +530,10 @@ cudaError_t launch_quantize_rows_bf16(const float* x, int64_t rows, int64_t K, f
                                       int32_t* bound_word) {
   if (rows == 0) return cudaSuccess;
   const int64_t items = rows * (Kp / 8);
-  constexpr int U = 4;
+  // one item per thread per round: fewer registers, more threads resident;
+  // a sweep of 1 / 2 / 3 / 4 items per thread measured 9.0 / 9.6 / 10.0 /
+  // 9.9 us on 2048 x 4096 (medians of nine launches)
+  constexpr int U = 1;
   if (items + 256 * U < (int64_t(1) << 31)) {
     static int occ[64];
     const int grid = resident_grid(quantize_rows_bf16_kernel<U, uint32_t>, occ, (items + U - 1) / U, 256);
